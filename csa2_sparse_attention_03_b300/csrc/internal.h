@@ -1,0 +1,108 @@
+// Host-side launchers shared between the CSA2 translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace csa2 {
+
+// ---- step 1: quantise-and-write ------------------------------------------
+struct QuantJob {
+    const float *src;         // [n_seqs][rows_per_seq][C]
+    const int32_t *start_pos; // [n_seqs] or null
+    const int32_t *seq_lens;  // [n_seqs] or null
+    CacheView dst;
+    int64_t rows_per_seq;
+    int32_t n_seqs;
+    int32_t append_last;      // 1: position = seq_lens[b] - 1 (decode append)
+};
+constexpr int kMaxQuantJobs = 64;
+// Enqueue quantisation of every job (one launch per call).
+cudaError_t launch_quantize(const QuantJob *jobs, int n_jobs, int *flags, cudaStream_t stream);
+
+// ---- step 2: indexer scan + Top-K ----------------------------------------
+// One scan job: one indexer-key cache scored by up to two indexing layers
+// (a Full layer and a pool-free Reindex layer over the same keys share one
+// pass over the keys).
+struct ScanJob {
+    CacheView keys;
+    const float *q_idx[2];    // [B][4][64]
+    const float *w[2];        // [B][4]
+    const int32_t *pool;      // [B][pool_len] candidate positions or null (= all)
+    int32_t pool_len;
+    int32_t n_q;              // 1 or 2
+    int32_t row[2];           // selection-row block of each query (row id = block*B + b)
+};
+constexpr int kMaxScanJobs = 16;
+
+// Per-row selection buffers inside the workspace.
+struct SelectBufs {
+    uint32_t *keys;       // [n_rows][cand_cap]    order-preserving score keys
+    uint32_t *hist;       // [n_rows][kHistBins]   first-level histogram
+    uint32_t *bitmap;     // [n_rows][2][bm_words] selected positions (topk, pool)
+    uint64_t *cand;       // [n_rows][2][cand_max] boundary-bin candidates (key, pos)
+    uint32_t *cand_count; // [n_rows][2]
+    int64_t cand_cap;     // candidates per row (max_seq_len or pool_len)
+    int32_t bm_words;     // bitmap words per row (ceil(max_seq_len/32))
+    int32_t cand_max;     // boundary candidate capacity per row and target
+};
+
+// A selection row: which targets (topk, pool) it produces.
+struct SelectRow {
+    int32_t *out_idx;     // [B][topk]
+    int32_t *out_pool;    // [B][pool_out_len] or null
+    const int32_t *pool;  // candidate positions when scanning a pool, else null
+    int32_t pool_len;
+    float *out_scores;    // optional [B][cand_cap]
+};
+constexpr int kMaxSelectRows = 16;
+
+struct SelectPlan {
+    SelectBufs bufs;
+    SelectRow rows[kMaxSelectRows];  // per row block
+    int32_t n_row_blocks;
+    int32_t batch;
+    int32_t topk;
+    int32_t pool_out_len;            // 0 = no pool target in this plan
+    int32_t max_len;                 // max_seq_len of the call
+    const int32_t *seq_lens;
+};
+
+// scores: optional per job and query fp32 outputs (row stride scores_stride).
+cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan, int max_cand,
+                        float *const (*scores)[2], int64_t scores_stride, int *flags,
+                        cudaStream_t stream);
+cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cudaStream_t stream,
+                          cudaEvent_t mid_event);
+size_t select_bytes(int n_rows, int64_t cand_cap, int max_seq_len);
+SelectBufs carve_select(uint8_t *base, int n_rows, int64_t cand_cap, int max_seq_len);
+
+// ---- step 3: sparse attention --------------------------------------------
+struct AttnEntry {
+    CacheView kv;
+    CacheView swa;
+    const float *q;        // [B][16][512]
+    const int32_t *idx;    // [B][topk] or null
+    float *out;            // [B][16][512]
+    float *lse;            // [B][16] or null
+    int32_t has_kv;
+    int32_t has_swa;
+};
+constexpr int kMaxAttnEntries = 48;
+
+struct AttnPlan {
+    const AttnEntry *entries;
+    int n_entries;
+    int batch;
+    int topk;
+    int window;
+    const int32_t *seq_lens;
+    int n_chunks;          // chunks per (entry, sequence); 1 = no merge pass
+    float *partials;       // [n_entries][B][n_chunks][16][512 + 2]
+};
+
+int attn_chunks(int n_entries, int batch, int topk, int window);
+size_t attn_partial_bytes(int n_entries, int batch, int n_chunks);
+cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
+                             cudaEvent_t mid_event);
+
+}  // namespace csa2

@@ -1,0 +1,213 @@
+"""Device state for one CSA2 decode step over a static layer-mode schedule.
+
+Allocates the packed caches (through torch), fills them through
+``csa2_quantize_kv`` from seeded synthetic values, and assembles the
+``csa2_layer_desc`` array that ``csa2_decode_layers`` consumes.  All
+arithmetic of the path runs in the CUDA library; this module only moves
+memory and builds descriptors.
+
+Mode semantics follow the Helmcode "DeepSeek V4.1 Flash" explainer,
+"03 · CSA2" (Full / Reindex / Reuse / SWA-only; Reuse layers keep their own
+query and SWA state) and Louis Bouchard's KV-cache report, "Share the cache
+and the search work" (pool-restricted Reindex).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import (FMT_FP4_IDX, FMT_FP4_KV, FMT_FP8_SWA, MODE_FULL, MODE_REINDEX, MODE_REUSE, MODE_SWA_ONLY,
+               Cache, csa2_cache, csa2_decode_layers, csa2_decode_layers_workspace, csa2_layer_desc,
+               csa2_quantize_kv, layer_array, synth)
+
+_MODE = {synth.FULL: MODE_FULL, synth.REINDEX: MODE_REINDEX, synth.REUSE: MODE_REUSE,
+         synth.SWA_ONLY: MODE_SWA_ONLY}
+BUILD_CHUNK = 65536
+
+
+def _round_up(x, m):
+    return (x + m - 1) // m * m
+
+
+class DecodeStep:
+    """Caches, per-layer inputs/outputs and descriptors of one workload.
+
+    fill="host": values come from synth's numpy streams (bit-identical to what
+    the oracle sees); fill="device": from seeded torch CUDA generators (bench
+    sizes).  The token at position L_b - 1 is left out of the build and passed
+    as the step's append input, so every step re-writes it (idempotent).
+    """
+
+    def __init__(self, w: synth.Workload, device="cuda", fill="host", append=True):
+        self.w = w
+        self.device = device
+        self.fill = fill
+        B, Lmax = w.batch, w.max_len
+        self.B, self.Lmax = B, Lmax
+        self.seq_lens = torch.tensor(w.seq_lens, dtype=torch.int32, device=device)
+        self.window = w.window
+        self.topk = w.topk
+        self.pool_len = w.pool_len
+        self.caches = {}      # full layer -> (kv Cache, idx Cache)
+        self.swa = {}         # layer -> Cache
+        self.new_rows = {}    # (kind, layer) -> [B, C] fp32 device
+        self.page_tables = {}
+        L_list = [int(x) for x in w.seq_lens]
+        for f, ly in enumerate(w.layers):
+            if ly.mode != synth.FULL:
+                continue
+            if w.paged:
+                pages_per = [(_round_up(L, 64)) // 64 for L in L_list]
+                n_pages = sum(pages_per)
+                perm = synth.page_permutation(w, n_pages, f)
+                maxp = max(pages_per)
+                table = np.full((B, maxp), -1, np.int32)
+                k = 0
+                for b in range(B):
+                    table[b, :pages_per[b]] = perm[k:k + pages_per[b]]
+                    k += pages_per[b]
+                t = torch.from_numpy(table).to(device)
+                self.page_tables[f] = t
+                kv = Cache.paged(FMT_FP4_KV, n_pages, 64, t, device)
+                ik = Cache.paged(FMT_FP4_IDX, n_pages, 64, t, device)
+            else:
+                stride = _round_up(Lmax, 64)
+                kv = Cache.contiguous(FMT_FP4_KV, B, stride, device)
+                ik = Cache.contiguous(FMT_FP4_IDX, B, stride, device)
+            self.caches[f] = (kv, ik)
+            self._build_full(f, kv, ik, append)
+        for l, ly in enumerate(w.layers):
+            ring = Cache.contiguous(FMT_FP8_SWA, B, _round_up(max(w.window, 4), 4), device)
+            self.swa[l] = ring
+            self._build_swa(l, ring, append)
+        self._alloc_layers()
+        self.descs = self._descs()
+        self.arr = layer_array(self.descs)
+        self.ws_bytes = csa2_decode_layers_workspace(self.descs, B, Lmax, self.topk, self.pool_len, self.window)
+        if self.ws_bytes == 0:
+            from . import csa2_last_error
+            raise RuntimeError("workspace query failed: " + csa2_last_error())
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    # ---- value sources ----
+    def _rows(self, kind, layer, b, row0, n, width, scale=1.0):
+        if self.fill == "host":
+            name = {"kv": "kv", "idxk": "idxk", "swa": "swa"}[kind]
+            if kind == "swa":
+                v = synth.swa_values(self.w, layer, b)[row0:row0 + n]
+            else:
+                v = synth.normal_rows(self.w.seed, name, (layer, b), row0, n, width)
+            return torch.from_numpy(np.ascontiguousarray(v)).to(self.device)
+        t = torch.empty((n, width), dtype=torch.float32, device=self.device)
+        return synth.device_normal_(t, self.w.seed, kind, layer, b, row0, scale=scale)
+
+    def _build_full(self, f, kv, ik, append):
+        B = self.B
+        new_kv = torch.zeros((B, 512), dtype=torch.float32, device=self.device)
+        new_ik = torch.zeros((B, 64), dtype=torch.float32, device=self.device)
+        start = torch.zeros(1, dtype=torch.int32, device=self.device)
+        for b, L in enumerate(self.w.seq_lens):
+            L = int(L)
+            n_build = L - 1 if append else L
+            kv_b, ik_b = kv.seq_view(b), ik.seq_view(b)
+            for r0 in range(0, n_build, BUILD_CHUNK):
+                n = min(BUILD_CHUNK, n_build - r0)
+                start.fill_(r0)
+                csa2_quantize_kv(self._rows("kv", f, b, r0, n, 512)[None], kv_b, start_pos=start)
+                csa2_quantize_kv(self._rows("idxk", f, b, r0, n, 64)[None], ik_b, start_pos=start)
+            if L >= 1:
+                new_kv[b] = self._rows("kv", f, b, L - 1, 1, 512)[0]
+                new_ik[b] = self._rows("idxk", f, b, L - 1, 1, 64)[0]
+        torch.cuda.synchronize()
+        if append:
+            self.new_rows[("kv", f)] = new_kv
+            self.new_rows[("idxk", f)] = new_ik
+
+    def _build_swa(self, l, ring, append):
+        """Window rows: synth row i of sequence b is position L_b - W + i (kept when >= 0)."""
+        B, W = self.B, self.window
+        src = torch.zeros((B, W, 512), dtype=torch.float32, device=self.device)
+        new = torch.zeros((B, 512), dtype=torch.float32, device=self.device)
+        start = torch.zeros((B,), dtype=torch.int32, device=self.device)
+        lens = torch.zeros((B,), dtype=torch.int32, device=self.device)
+        for b, L in enumerate(self.w.seq_lens):
+            L = int(L)
+            n = min(W, L)
+            rows = self._rows("swa", l, b, W - n, n, 512)
+            n_build = n - 1 if append else n
+            src[b, :n_build] = rows[:n_build]
+            start[b] = L - n
+            lens[b] = L - n + n_build
+            if n >= 1:
+                new[b] = rows[n - 1]
+        csa2_quantize_kv(src, ring, start_pos=start, seq_lens=lens)
+        torch.cuda.synchronize()
+        if append:
+            self.new_rows[("swa", l)] = new
+
+    def _alloc_layers(self):
+        B, dev = self.B, self.device
+        self.q, self.q_idx, self.wts, self.out, self.lse, self.idx, self.pool = {}, {}, {}, {}, {}, {}, {}
+        for l, ly in enumerate(self.w.layers):
+            if self.fill == "host":
+                self.q[l] = torch.from_numpy(synth.query(self.w, l)).to(dev)
+            else:
+                self.q[l] = synth.device_normal_(torch.empty((B, 16, 512), device=dev), self.w.seed, "q", l,
+                                                 scale=1.0 / np.sqrt(512))
+            self.out[l] = torch.zeros((B, 16, 512), dtype=torch.float32, device=dev)
+            self.lse[l] = torch.zeros((B, 16), dtype=torch.float32, device=dev)
+            if ly.mode in (synth.FULL, synth.REINDEX):
+                if self.fill == "host":
+                    self.q_idx[l] = torch.from_numpy(synth.index_query(self.w, l)).to(dev)
+                    self.wts[l] = torch.from_numpy(synth.index_weights(self.w, l)).to(dev)
+                else:
+                    self.q_idx[l] = synth.device_normal_(torch.empty((B, 4, 64), device=dev), self.w.seed,
+                                                         "qidx", l, scale=1.0 / 8.0)
+                    self.wts[l] = synth.device_uniform_(torch.empty((B, 4), device=dev), self.w.seed, "widx", l)
+                self.idx[l] = torch.full((B, self.topk), -7, dtype=torch.int32, device=dev)
+                if ly.mode == synth.FULL and self.pool_len:
+                    self.pool[l] = torch.full((B, self.pool_len), -7, dtype=torch.int32, device=dev)
+
+    def _descs(self):
+        descs = []
+        P = lambda t: t.data_ptr() if t is not None else None
+        for l, ly in enumerate(self.w.layers):
+            d = csa2_layer_desc()
+            d.mode = _MODE[ly.mode]
+            d.kv_src = ly.kv_src
+            d.idx_src = ly.idx_src
+            d.use_pool = 1 if ly.use_pool else 0
+            if ly.mode == synth.FULL:
+                kv, ik = self.caches[l]
+                d.kv = ctypes.pointer(kv.desc)
+                d.idx_keys = ctypes.pointer(ik.desc)
+                d.new_kv = P(self.new_rows.get(("kv", l)))
+                d.new_idx_key = P(self.new_rows.get(("idxk", l)))
+            d.swa = ctypes.pointer(self.swa[l].desc)
+            d.new_swa = P(self.new_rows.get(("swa", l)))
+            d.q = P(self.q[l])
+            d.q_idx = P(self.q_idx.get(l))
+            d.w = P(self.wts.get(l))
+            d.out = P(self.out[l])
+            d.lse = P(self.lse[l])
+            d.idx_out = P(self.idx.get(l))
+            d.pool_out = P(self.pool.get(l))
+            descs.append(d)
+        return descs
+
+    def run(self, stream=None):
+        csa2_decode_layers(self.descs, self.B, self.seq_lens, self.Lmax, self.topk, self.pool_len, self.window,
+                           self.workspace, stream=stream, arr=self.arr)
+
+    # ---- inputs/outputs moved per step in the end-to-end measurement ----
+    def step_inputs(self):
+        """Tensors a caller supplies per decode step (queries, indexer queries,
+        weights and the appended token rows)."""
+        ts = list(self.q.values()) + list(self.q_idx.values()) + list(self.wts.values())
+        ts += list(self.new_rows.values())
+        return ts
+
+    def step_outputs(self):
+        return list(self.out.values()) + list(self.lse.values()) + list(self.idx.values())

@@ -1,0 +1,72 @@
+"""Step 4 parity: one decode step over each workload's schedule (shrunk
+lengths), against the oracle layer by layer; graph capture and determinism."""
+import numpy as np
+import pytest
+import torch
+
+from csa2_sparse_attention_03_b300 import synth
+from csa2_sparse_attention_03_b300.schedule import DecodeStep
+from helpers import oracle_step, within_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(step, ref, w):
+    for l, ly in enumerate(w.layers):
+        if ly.mode in (synth.FULL, synth.REINDEX):
+            got = step.idx[l].cpu().numpy()
+            assert np.array_equal(got, ref[l]["idx"]), f"layer {l}: indices differ"
+        if ref[l]["pool"] is not None:
+            assert np.array_equal(step.pool[l].cpu().numpy(), ref[l]["pool"]), f"layer {l}: pool differs"
+        ok, ex = within_tol(step.out[l].cpu().numpy(), ref[l]["out"])
+        assert ok, f"layer {l}: output excess {ex:.3e}"
+        lse = step.lse[l].cpu().numpy()
+        assert np.allclose(lse, ref[l]["lse"], atol=2e-3, rtol=1e-3), f"layer {l}: lse"
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_decode_step_small(cuda, orc, cfg):
+    w = synth.workload(cfg, small=True)
+    step = DecodeStep(w, fill="host")
+    step.run()
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags, cuda.csa2_last_error())
+    ref, caches, _ = oracle_step(orc, w)
+    _compare(step, ref, w)
+    # after the step the caches hold every token, appended one included
+    for f, (kv, ik) in step.caches.items():
+        gv = kv.data.cpu().numpy().reshape(-1, 288)
+        gk = ik.data.cpu().numpy()
+        for b, L in enumerate(w.seq_lens):
+            if w.paged:
+                slots = orc.slots_paged(step.page_tables[f][b].cpu().numpy(), np.arange(L), 64)
+            else:
+                slots = orc.slots_contiguous(b, np.arange(L), kv.desc.seq_stride)
+            c = caches[f][b]
+            assert np.array_equal(gv[slots], orc.kv_rows(c["kv_codes"], c["kv_scales"]))
+            rc, rs = orc.read_idx(gk, slots)
+            assert np.array_equal(rc, c["k_codes"]) and np.array_equal(rs, c["k_scales"])
+
+
+def test_graph_replay_and_determinism(cuda, orc):
+    w = synth.workload(1, small=True)
+    step = DecodeStep(w, fill="host")
+    step.run()
+    torch.cuda.synchronize()
+    first = [t.clone() for t in step.step_outputs()]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step.run(stream=s)  # warm-up on the capture stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            step.run(stream=s)
+    for _ in range(3):
+        for t in step.step_outputs():
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(first, step.step_outputs()):
+            assert torch.equal(a, b)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0
