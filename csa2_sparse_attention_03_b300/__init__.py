@@ -82,6 +82,8 @@ def load():
     L.csa2_last_device_flags.argtypes = []
     L.csa2_set_phase_events.restype = i32
     L.csa2_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+    L.csa2_launch_count.restype = i64
+    L.csa2_launch_count.argtypes = []
     L.csa2_version.restype = i32
     L.csa2_version.argtypes = []
     _lib = L
@@ -233,6 +235,10 @@ def csa2_set_phase_events(events):
     n = len(events)
     arr = (ctypes.c_void_p * max(n, 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(L.csa2_set_phase_events(arr, n))
+
+
+def csa2_launch_count() -> int:
+    return int(load().csa2_launch_count())
 
 
 def csa2_last_error() -> str:

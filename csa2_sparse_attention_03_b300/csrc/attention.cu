@@ -444,14 +444,16 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
             p.partials = plan.partials + (size_t)first * plan.batch * plan.n_chunks * kPartFloats;
         dim3 grid((unsigned)plan.n_chunks, (unsigned)plan.batch, (unsigned)n);
         attn_kernel<<<grid, kAttnThreads, smem, stream>>>(ab, p, flags);
+        count_launches(1);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (mid_event && first + n >= plan.n_entries) {
-            e = cudaEventRecord(mid_event, stream);
+            e = record_event(mid_event, stream);
             if (e != cudaSuccess) return e;
         }
         if (plan.n_chunks > 1) {
             merge_kernel<<<dim3((unsigned)n, (unsigned)plan.batch), 256, 0, stream>>>(ab, p);
+            count_launches(1);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }

@@ -3,6 +3,7 @@
 // schedule (Helmcode "DeepSeek V4.1 Flash" explainer, "03 · CSA2": Full,
 // Reindex, Reuse and SWA-only layers; Louis Bouchard's KV-cache report,
 // "Share the cache and the search work": pool-restricted Reindex).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -12,6 +13,11 @@
 #include "internal.h"
 
 using namespace csa2;
+
+namespace csa2 {
+static std::atomic<int64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace csa2
 
 namespace {
 
@@ -56,7 +62,7 @@ int g_n_events = 0;
 cudaError_t mark(int phase, cudaStream_t s)
 {
     if (phase < g_n_events && g_events[phase])
-        return cudaEventRecord(static_cast<cudaEvent_t>(g_events[phase]), s);
+        return record_event(static_cast<cudaEvent_t>(g_events[phase]), s);
     return cudaSuccess;
 }
 
@@ -117,6 +123,8 @@ size_t select_head_bytes(int n_rows) { return round256((size_t)n_rows * kHistBin
 extern "C" {
 
 int32_t csa2_version(void) { return 100; }
+
+int64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *csa2_last_error(void) { return g_err.c_str(); }
 

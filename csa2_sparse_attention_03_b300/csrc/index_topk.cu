@@ -589,6 +589,7 @@ cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan,
                   (unsigned)sb.n_jobs);
         scan_kernel<<<grid, kScanWarps * 32, 0, stream>>>(sb, plan.bufs, plan.seq_lens, plan.batch,
                                                          plan.max_len, flags);
+        count_launches(1);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -602,6 +603,7 @@ cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cuda
     dim3 cgrid((unsigned)ceil_div(max_cand > 0 ? max_cand : 1, kCollectChunk), (unsigned)plan.batch,
                (unsigned)plan.n_row_blocks);
     collect_kernel<<<cgrid, 256, 0, stream>>>(plan, max_len, flags);
+    count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = 8 * (size_t)plan.bufs.cand_max + 4 * kHistBins;
@@ -616,6 +618,7 @@ cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cuda
     }
     dim3 fgrid((unsigned)plan.batch, (unsigned)plan.n_row_blocks, 2u);
     finish_kernel<<<fgrid, kFinishThreads, smem, stream>>>(plan, max_len, flags);
+    count_launches(1);
     (void)mid_event;
     return cudaGetLastError();
 }

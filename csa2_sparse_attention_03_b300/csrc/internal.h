@@ -5,6 +5,21 @@
 
 namespace csa2 {
 
+// Records a profiling event on `s`.  Inside a stream capture the record
+// becomes an external event node, so the event is re-recorded (with its
+// timestamp) on every replay of the captured graph.
+inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(ev, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                               : cudaEventRecordDefault);
+}
+
+// Kernels enqueued by this library since load (process-wide, relaxed).
+void count_launches(int n);
+
 // ---- step 1: quantise-and-write ------------------------------------------
 struct QuantJob {
     const float *src;         // [n_seqs][rows_per_seq][C]

@@ -170,6 +170,7 @@ cudaError_t launch_quantize(const QuantJob *jobs, int n_jobs, int *flags, cudaSt
         int64_t blocks = ceil_div(units, 8);
         if (blocks > 148 * 32) blocks = 148 * 32;
         quantize_kernel<<<(unsigned)blocks, 256, 0, stream>>>(qb, flags);
+        count_launches(1);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

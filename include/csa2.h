@@ -230,6 +230,10 @@ int32_t csa2_last_device_flags(void);
  * scoring, 2 level-0 selection, 3 level-1 scoring+selection, 4 attention,
  * 5 merge.  Pass n = 0 to disable.  Process-wide; not thread-safe. */
 csa2_status csa2_set_phase_events(void *const *events, int32_t n);
+/* Kernels this library has enqueued since it was loaded, all threads and
+ * devices together (a stream capture counts its launches once; replays of
+ * the captured graph add nothing). */
+int64_t csa2_launch_count(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t csa2_version(void);
 

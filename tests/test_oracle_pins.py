@@ -264,6 +264,69 @@ def test_score_scaling_and_symmetry(orc):
     assert np.allclose(s1.astype(np.float64) + sn, both, rtol=1e-6, atol=1e-30)
 
 
+def _f32(x):
+    """Round an exact rational to the nearest fp32 (ties to even)."""
+    return float(np.float32(float(x))) if x == 0 else _round_f32(x)
+
+
+def _round_f32(x):
+    from fractions import Fraction
+    x = Fraction(x)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    # make 2^e <= a < 2^(e+1) exactly
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126)
+    q = Fraction(2) ** (e - 23)          # spacing of fp32 values at this binade
+    n = a / q
+    fl = math.floor(n)
+    r = n - fl
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * float(fl * q)
+
+
+def test_score_rounding_points_exact_rational(orc):
+    """The score's stated rounding points, evaluated in exact rational
+    arithmetic with an fp32 rounding after each step (block sums are exact; the
+    head sum rounds after each add; the weighted sum is an fp32 product then
+    three fused multiply-adds).  The oracle must agree bit for bit; the
+    independent decode uses the golden E2M1 table and torch's E4M3."""
+    from fractions import Fraction
+    x = synth.normal_rows(5, "pin", (20,), 0, 60, 64)
+    kc, ks = orc.quant_fp4(x)
+    table = _golden_e2m1()
+    for trial in range(4):
+        q = synth.normal_rows(5, "pin", (21, trial), 0, 4, 64, scale=1 / 8)
+        w = synth.uniform(5, "pin", (22, trial), (4,))
+        got = orc.index_scores(q, w, kc, ks)
+        qc, qs = orc.quant_fp4(q)
+        qsd = _e4m3_lib(qs.reshape(-1)).reshape(qs.shape)
+        ksd = _e4m3_lib(ks.reshape(-1)).reshape(ks.shape)
+        for p in range(kc.shape[0]):
+            r = []
+            for h in range(4):
+                s = None
+                for blk in range(4):
+                    P = Fraction(0)
+                    for c in range(16 * blk, 16 * blk + 16):
+                        qn = (int(qc[h, c // 2]) >> (4 * (c % 2))) & 15
+                        kn = (int(kc[p, c // 2]) >> (4 * (c % 2))) & 15
+                        P += Fraction(table[qn]) * Fraction(table[kn])
+                    t = Fraction(qsd[h, blk]) * Fraction(ksd[p, blk]) * P
+                    assert _f32(t) == float(t)              # each block term is exact in fp32
+                    s = t if s is None else Fraction(_f32(s + t))
+                r.append(max(Fraction(_f32(s)), Fraction(0)))
+            acc = Fraction(_f32(Fraction(float(w[0])) * r[0]))
+            for h in (1, 2, 3):
+                acc = Fraction(_f32(Fraction(float(w[h])) * r[h] + acc))
+            assert float(got[p]) == float(acc), (trial, p)
+
+
 def test_score_zero_is_positive_zero(orc):
     q = -np.ones((4, 64), np.float32)
     kc, ks = orc.quant_fp4(np.ones((1, 64), np.float32))
