@@ -404,6 +404,9 @@ def run_csa2(args):
     ph = [torch.cuda.Event(enable_timing=True) for _ in range(n_ph)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for e in ph:  # torch only times events it has seen recorded once
+            e.record(stream)
     csa2.csa2_set_phase_events(ph)
     with torch.cuda.stream(stream):
         step.run(stream=stream)
