@@ -70,6 +70,8 @@ def load():
     L.csa2_sparse_attn_workspace.argtypes = [i32, i32, i32]
     L.csa2_sparse_attn.restype = i32
     L.csa2_sparse_attn.argtypes = [C, C, P, i32, i32, i32, P, i32, P, i32, i32, P, P, P, sz, P]
+    L.csa2_sparse_attn_noalloc.restype = i32
+    L.csa2_sparse_attn_noalloc.argtypes = [C, C, P, i32, i32, i32, P, i32, P, i32, i32, P, P, P]
     L.csa2_decode_layers_workspace.restype = sz
     L.csa2_decode_layers_workspace.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, i32, i32, i32, i32]
     L.csa2_decode_layers.restype = i32
@@ -198,6 +200,23 @@ def csa2_sparse_attn(kv, swa, q, seq_lens, max_seq_len, idx, topk, swa_window, o
                               _ptr(q), B, q.shape[1], q.shape[2], _ptr(seq_lens), max_seq_len, _ptr(idx),
                               topk, swa_window, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                               _stream(stream)))
+    return out, lse
+
+
+def csa2_sparse_attn_noalloc(kv, swa, q, seq_lens, max_seq_len, idx, topk, swa_window, out=None, lse=None,
+                             stream=None):
+    """csa2_sparse_attn without a workspace (the library's fixed scratch
+    array stands in for it).  Returns (out [B, 16, 512], lse [B, 16])."""
+    import torch
+    L = load()
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, q.shape[1]), dtype=torch.float32, device=q.device)
+    _check(L.csa2_sparse_attn_noalloc(kv.ref if kv is not None else None, swa.ref if swa is not None else None,
+                                      _ptr(q), B, q.shape[1], q.shape[2], _ptr(seq_lens), max_seq_len, _ptr(idx),
+                                      topk, swa_window, _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -35,6 +35,21 @@ csa2_status fail(csa2_status s, const char *fmt, ...)
     return s;
 }
 
+}  // namespace
+
+csa2_status csa2::set_error(csa2_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+namespace {
+
 csa2_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(CSA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

@@ -20,6 +20,9 @@ inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t s)
 // Kernels enqueued by this library since load (process-wide, relaxed).
 void count_launches(int n);
 
+// Sets the calling thread's csa2_last_error() message; returns `s`.
+csa2_status set_error(csa2_status s, const char *fmt, ...);
+
 // ---- step 1: quantise-and-write ------------------------------------------
 struct QuantJob {
     const float *src;         // [n_seqs][rows_per_seq][C]

@@ -175,6 +175,28 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
                              float *out, float *lse, void *workspace, size_t workspace_bytes,
                              void *stream);
 
+/* Attention without a workspace, for callers that cannot allocate device
+ * memory: a serving process that reserved nearly all HBM for its cache pool
+ * up front (cudaMalloc would fail there, and it synchronises the device), or
+ * a plugin living inside another runtime's allocator.  The paper has no
+ * counterpart; this is a deployment convenience of this library.
+ * Arguments, layouts, numerics and error codes are those of
+ * csa2_sparse_attn minus the workspace.  The split partials go to a 4 MiB
+ * array the library holds on every device that loads it, until exit; a call
+ * whose partials need more than that (csa2_sparse_attn_workspace() > 4 MiB,
+ * e.g. beyond about 24 sequences at topk 2048) returns CSA2_ERR_UNSUPPORTED
+ * with a message.  It calls no allocator.  Every call on a device shares the
+ * array, so calls that overlap on the GPU (other streams, other threads) race
+ * and give wrong results: serialise them.  Each call rewrites every partial
+ * it reads, so nothing needs clearing between calls.  The first call on each
+ * device looks the array's device address up (with that device current);
+ * make that first call before any stream capture. */
+csa2_status csa2_sparse_attn_noalloc(const csa2_cache *kv, const csa2_cache *swa, const float *q,
+                                     int32_t batch, int32_t n_heads, int32_t head_dim,
+                                     const int32_t *seq_lens, int32_t max_seq_len,
+                                     const int32_t *idx, int32_t topk, int32_t swa_window,
+                                     float *out, float *lse, void *stream);
+
 /* ---- step 4: one decode step over a static mode schedule --------------- */
 /* [HC] "03 · CSA2": static per-layer modes; a Reuse layer consumes another
  * layer's Top-K over a Full layer's KV with its own query and SWA state;
