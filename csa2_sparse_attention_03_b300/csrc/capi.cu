@@ -130,8 +130,8 @@ csa2_status check_ws(void *ws, size_t have, size_t need)
 
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// bytes of the hist + counter head of a select region (zeroed per call)
-size_t select_head_bytes(int n_rows) { return round256((size_t)n_rows * kHistBins * 4) + round256((size_t)n_rows * 8); }
+// bytes at the head of a select region that are zeroed per call (the histograms)
+size_t select_head_bytes(int n_rows) { return select_hist_bytes(n_rows); }
 
 }  // namespace
 
@@ -510,9 +510,6 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
         const int64_t row_off = (int64_t)rb0 * batch;
         plan.bufs.keys += row_off * bufs.cand_cap;
         plan.bufs.hist += row_off * kHistBins;
-        plan.bufs.bitmap += row_off * 2 * bufs.bm_words;
-        plan.bufs.cand += row_off * 2 * bufs.cand_max;
-        plan.bufs.cand_count += row_off * 2;
         std::vector<ScanJob> jobs;
         int max_cand = 1;
         for (int l = 0; l < n_layers; ++l) {

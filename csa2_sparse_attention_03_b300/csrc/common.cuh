@@ -25,12 +25,12 @@ constexpr int kKvRow = 288;     // bytes per FP4 main-KV row
 constexpr int kKvCodes = 256;   // code bytes in a main-KV row
 constexpr int kIdxTile = 64;    // tokens per indexer-key tile
 constexpr int kIdxTileBytes = 2304;
-constexpr int kHistBins = 4096; // first-level Top-K histogram (key >> 20)
+constexpr int kHistBits = 11;   // first Top-K radix digit: the key's top 11 bits
+constexpr int kHistBins = 1 << kHistBits;
 
 // Device flag bits, OR-ed into one word read by csa2_check_device().
 constexpr int kFlagBounds = 1;    // an index / page / slot out of range was skipped
 constexpr int kFlagTimeout = 2;   // a bounded wait gave up
-constexpr int kFlagOverflow = 4;  // candidate buffer overflow (slow path taken)
 
 struct CacheView {
     uint8_t *data;

@@ -3,36 +3,49 @@
 // Helmcode "DeepSeek V4.1 Flash" explainer, "03 · CSA2": a Full layer scores
 // every position, a Reindex layer rescores a Full layer's keys with its own
 // query; Louis Bouchard's KV-cache report, "Share the cache and the search
-// work": the decoder's first indexing layer keeps a pool of up to 16,384
-// candidates that later indexing layers search; 0x0moeen's note: layers
-// share the indexer keys.  The score form and its rounding points are this
-// library's choice (see include/csa2.h) and make the result exact up to a
-// fixed fp32 sequence, so the selected index sets are reproducible bit for bit.
+// work": the decoder's first indexing layer keeps a candidate pool that later
+// indexing layers search; 0x0moeen's note: layers share the indexer keys.
+// The score form and its rounding points are this library's choice (see
+// include/csa2.h) and make the result exact up to a fixed fp32 sequence, so
+// the selected index sets are reproducible bit for bit.
 //
 // Kernels
-//  scan     one pass over FP4 keys (HBM-bound, 36 B per position).  A warp
-//           scores 16 keys per step: the E2M1 block dot products of up to two
-//           queries (a Full layer and the pool-free Reindex layer that shares
-//           its keys) x 4 heads run as one m16n8k16 fp16 MMA per 16-channel
-//           block -- exact, because the E2M1 codes and the block-scaled query
-//           (scale x code, <= 6 significant bits) are exact in fp16 and every
-//           partial sum is a small multiple of the block's quantum.  The
-//           epilogue applies the key scales and head weights in the fixed
-//           order on CUDA cores, writes an order-preserving uint32 key per
-//           candidate and builds a 4096-bin histogram of the key's top bits.
-//  collect  per row: the histogram's boundary bin; positions above it are
-//           set in a bitmap, boundary-bin candidates are appended to a list.
-//  finish   one CTA per row and target: radix select inside the boundary bin
-//           over (key, ~position), then bitmap -> ascending positions.
+//  scan    HBM-bound pass over the FP4 keys (36 B per position).  A CTA owns
+//          1,024 candidates: for a full-context scan it pulls its 16 key
+//          tiles (2,304 B each) into shared memory with bulk async copies
+//          completing on one mbarrier, so every tile is in flight at once;
+//          for a pool scan it gathers each key.  A warp scores 16 keys per
+//          step: the E2M1 block dot products of up to two queries (a Full
+//          layer and the pool-free Reindex layer that shares its keys) x 4
+//          heads run as one m16n8k16 fp16 MMA per 16-channel block -- exact,
+//          because E2M1 codes and the block-scaled query (scale x code, <= 6
+//          significant bits) are exact in fp16 and every partial sum is a
+//          small multiple of the block's quantum.  The epilogue applies the
+//          key scales and head weights in the fixed order on CUDA cores,
+//          writes an order-preserving uint32 key per candidate (0 = not a
+//          candidate) and adds its CTA's 2,048-bin histogram of the keys'
+//          top 11 bits into the row's global histogram.
+//  select  one cluster of 8 CTAs per (row, target): an exact radix select
+//          of the K-th largest key (11 + 11 + 10 bit digits) with the
+//          histograms reduced across the cluster through distributed shared
+//          memory, the ties at the threshold resolved to the lowest
+//          positions by a prefix over the cluster's slices, and the winners
+//          written as ascending positions (-1 padded).
+#include <cooperative_groups.h>
+
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa2 {
 namespace {
 
 constexpr int kScanWarps = 8;
-constexpr int kScanChunk = 2048;     // candidates per scan CTA
-constexpr int kCollectChunk = 4096;  // candidates per collect CTA
-constexpr int kFinishThreads = 1024;
+constexpr int kScanKeys = 1024;                 // candidates per scan CTA
+constexpr int kScanTiles = kScanKeys / kIdxTile;  // 16 key tiles
+constexpr int kSelCluster = 8;
+constexpr int kSelThreads = 512;
+constexpr uint32_t kWaitLimit = 1u << 24;       // mbarrier polls before giving up
 
 struct ScanBatch {
     ScanJob jobs[kMaxScanJobs];
@@ -55,15 +68,68 @@ __device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, u
 __device__ __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
                                            -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
 
-// Key of one candidate: cached-code words this thread needs (see below) and
-// the four block scales.
+// ---- mbarrier + bulk copy (sm_90+ PTX) ----------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`; false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Codes (the 4 words this thread needs) and the 4 block scales of one key.
 struct KeyLoad {
     uint32_t w[4];
     uint32_t sc;
     bool ok;
 };
 
-__device__ __forceinline__ KeyLoad load_key(const CacheView &keys, int b, int64_t pos, int t, int *flags)
+// thread t of a quad uses bytes 8j+2t, 8j+2t+1 of block j: word 2j + t/2, half t%2
+__device__ __forceinline__ KeyLoad key_from_tile(const uint8_t *tile, int rr, int t)
+{
+    KeyLoad k;
+    const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k.w[j] = codes[2 * j + (t >> 1)];
+    k.sc = *reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4);
+    k.ok = true;
+    return k;
+}
+
+__device__ __forceinline__ KeyLoad key_from_global(const CacheView &keys, int b, int64_t pos, int t, int *flags)
 {
     KeyLoad k;
     k.ok = false;
@@ -78,7 +144,6 @@ __device__ __forceinline__ KeyLoad load_key(const CacheView &keys, int b, int64_
     const uint8_t *tile = keys.data + (slot / kIdxTile) * kIdxTileBytes;
     const int rr = (int)(slot % kIdxTile);
     const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
-    // thread t uses bytes 8j+2t, 8j+2t+1 of block j: word 2j + t/2, half t%2
 #pragma unroll
     for (int j = 0; j < 4; ++j) k.w[j] = __ldg(codes + 2 * j + (t >> 1));
     k.sc = __ldg(reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4));
@@ -86,14 +151,21 @@ __device__ __forceinline__ KeyLoad load_key(const CacheView &keys, int b, int64_
     return k;
 }
 
+struct __align__(128) ScanSmem {
+    uint8_t tiles[kScanTiles][kIdxTileBytes];  // 36,864 B
+    uint32_t hist[2][kHistBins];
+    __half qpre[2][kIdxHeads][kIdxDim];
+    float wq[2][kIdxHeads];
+    int32_t tile_ok[kScanTiles];
+    uint64_t bar;
+};
+
 __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_constant__ ScanBatch sb,
                                                                  SelectBufs bufs, const int32_t *seq_lens,
                                                                  int batch, int max_len, int *flags)
 {
-    __shared__ uint32_t hist[2][kHistBins];
-    __shared__ __half qpre[2][kIdxHeads][kIdxDim];
-    __shared__ float wq[2][kIdxHeads];
-
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    ScanSmem &S = *reinterpret_cast<ScanSmem *>(smem_raw);
     const ScanJob &job = sb.jobs[blockIdx.z];
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
@@ -101,26 +173,43 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
     const int g = lane >> 2, t = lane & 3;
     int L = __ldg(seq_lens + b);
     if (L < 0 || L > max_len) {
-        if (tid == 0) raise_flag(flags, kFlagBounds);
+        if (tid == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBounds);
         L = L < 0 ? 0 : max_len;
     }
     const int64_t n_cand = job.pool ? job.pool_len : L;
+    const int64_t base = (int64_t)blockIdx.x * kScanKeys;
+    if (base >= n_cand) return;
+    const bool direct = job.pool == nullptr;
 
-    for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&hist[0][0])[i] = 0u;
-    // zero this CTA's slice of the rows' bitmaps (both targets)
-    {
-        const int per = (int)ceil_div(bufs.bm_words, gridDim.x);
-        const int w0 = blockIdx.x * per;
-        const int w1 = min(bufs.bm_words, w0 + per);
-        for (int qi = 0; qi < job.n_q; ++qi) {
-            const int64_t row = (int64_t)job.row[qi] * batch + b;
-            uint32_t *bm = bufs.bitmap + row * 2 * bufs.bm_words;
-            for (int w = w0 + tid; w < w1; w += blockDim.x) {
-                bm[w] = 0u;
-                bm[bufs.bm_words + w] = 0u;
+    // 1. issue the bulk copies of this CTA's key tiles (full-context scans)
+    if (direct && tid == 0) {
+        mbar_init(&S.bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        uint32_t bytes = 0;
+        const uint8_t *src[kScanTiles];
+        for (int i = 0; i < kScanTiles; ++i) {
+            src[i] = nullptr;
+            const int64_t p0 = base + (int64_t)i * kIdxTile;
+            int ok = 0;
+            if (p0 < n_cand) {
+                const int64_t slot = slot_of(job.keys, b, p0);
+                // a 64-aligned position block maps to one whole tile (page and stride are multiples of 64)
+                if (slot >= 0 && slot + kIdxTile <= job.keys.n_slots) {
+                    src[i] = job.keys.data + (slot / kIdxTile) * kIdxTileBytes;
+                    bytes += kIdxTileBytes;
+                    ok = 1;
+                } else {
+                    raise_flag(flags, kFlagBounds);
+                }
             }
+            S.tile_ok[i] = ok;
         }
+        mbar_expect_tx(&S.bar, bytes);
+        for (int i = 0; i < kScanTiles; ++i)
+            if (src[i]) bulk_g2s(S.tiles[i], src[i], kIdxTileBytes, &S.bar);
     }
+
+    for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&S.hist[0][0])[i] = 0u;
     // quantise the queries (FP4 rule) and pre-scale: qpre = scale * E2M1(code), exact in fp16
     if (tid < 32) {
         const int qi = tid >> 4, h = (tid >> 2) & 3, blk = tid & 3;
@@ -137,13 +226,13 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float e = (s != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v[i], s))] : 0.0f;
-                qpre[qi][h][blk * 16 + i] = __float2half_rn(e * s);
+                S.qpre[qi][h][blk * 16 + i] = __float2half_rn(e * s);
             }
-            if (blk == 0) wq[qi][h] = __ldg(job.w[qi] + (int64_t)b * kIdxHeads + h);
+            if (blk == 0) S.wq[qi][h] = __ldg(job.w[qi] + (int64_t)b * kIdxHeads + h);
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) qpre[qi][h][blk * 16 + i] = __float2half_rn(0.0f);
-            if (blk == 0) wq[qi][h] = 0.0f;
+            for (int i = 0; i < 16; ++i) S.qpre[qi][h][blk * 16 + i] = __float2half_rn(0.0f);
+            if (blk == 0) S.wq[qi][h] = 0.0f;
         }
     }
     __syncthreads();
@@ -155,32 +244,54 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
         const int qi = g >> 2, h = g & 3;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const __half *q = &qpre[qi][h][j * 16 + 4 * t];
+            const __half *q = &S.qpre[qi][h][j * 16 + 4 * t];
             bfrag[j][0] = (uint32_t)__half_as_ushort(q[0]) | ((uint32_t)__half_as_ushort(q[1]) << 16);
             bfrag[j][1] = (uint32_t)__half_as_ushort(q[2]) | ((uint32_t)__half_as_ushort(q[3]) << 16);
         }
     }
     const int my_q = t >> 1;  // query of this thread's two columns
     const bool finisher = (t & 1) != 0;
-    const float w0 = wq[my_q][0], w1 = wq[my_q][1], w2 = wq[my_q][2], w3 = wq[my_q][3];
+    const float w0 = S.wq[my_q][0], w1 = S.wq[my_q][1], w2 = S.wq[my_q][2], w3 = S.wq[my_q][3];
     const int64_t my_row = (int64_t)job.row[my_q < job.n_q ? my_q : 0] * batch + b;
     uint32_t *key_out = bufs.keys + my_row * bufs.cand_cap;
     float *score_out = (my_q < job.n_q) ? sb.out_scores[blockIdx.z][my_q] : nullptr;
     if (score_out) score_out += (int64_t)b * sb.scores_stride;
     const int32_t *pool = job.pool ? job.pool + (int64_t)b * job.pool_len : nullptr;
 
-    const int64_t base = (int64_t)blockIdx.x * kScanChunk;
-    for (int grp = warp; grp < kScanChunk / 16; grp += kScanWarps) {
+    // 2. wait for the tiles (bounded)
+    bool have_tiles = true;
+    if (direct) {
+        have_tiles = mbar_wait_bounded(&S.bar, 0);
+        if (!have_tiles) {
+            if (tid == 0) raise_flag(flags, kFlagTimeout);
+            mbar_wait_bounded(&S.bar, 0);  // give copies in flight a last chance to land
+        }
+    }
+
+    for (int grp = warp; grp < kScanKeys / 16; grp += kScanWarps) {
         const int64_t c0 = base + grp * 16;
         if (c0 >= n_cand) break;
         const int64_t cA = c0 + g, cB = c0 + g + 8;
-        int64_t pA = -1, pB = -1;
-        if (cA < n_cand) pA = pool ? (int64_t)__ldg(pool + cA) : cA;
-        if (cB < n_cand) pB = pool ? (int64_t)__ldg(pool + cB) : cB;
-        if (pA >= L) pA = -1;
-        if (pB >= L) pB = -1;
-        const KeyLoad kA = load_key(job.keys, b, pA, t, flags);
-        const KeyLoad kB = load_key(job.keys, b, pB, t, flags);
+        KeyLoad kA, kB;
+        if (direct) {
+            const int ti = grp >> 2;  // 4 groups of 16 keys per 64-key tile
+            const bool ok = have_tiles && S.tile_ok[ti];
+            const int r0 = (grp & 3) * 16;
+            kA = key_from_tile(S.tiles[ti], r0 + g, t);
+            kB = key_from_tile(S.tiles[ti], r0 + g + 8, t);
+            kA.ok = ok && cA < n_cand;
+            kB.ok = ok && cB < n_cand;
+            if (!kA.ok) kA.w[0] = kA.w[1] = kA.w[2] = kA.w[3] = kA.sc = 0u;
+            if (!kB.ok) kB.w[0] = kB.w[1] = kB.w[2] = kB.w[3] = kB.sc = 0u;
+        } else {
+            int64_t pA = -1, pB = -1;
+            if (cA < n_cand) pA = (int64_t)__ldg(pool + cA);
+            if (cB < n_cand) pB = (int64_t)__ldg(pool + cB);
+            if (pA >= L) pA = -1;
+            if (pB >= L) pB = -1;
+            kA = key_from_global(job.keys, b, pA, t, flags);
+            kB = key_from_global(job.keys, b, pB, t, flags);
+        }
 
         float d[4][4];
 #pragma unroll
@@ -225,7 +336,7 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
                 const uint32_t key = kA.ok ? score_key(scA) : 0u;
                 key_out[cA] = key;
                 if (kA.ok) {
-                    atomicAdd(&hist[my_q][key >> 20], 1u);
+                    atomicAdd(&S.hist[my_q][key >> (32 - kHistBits)], 1u);
                     if (score_out) score_out[cA] = scA;
                 }
             }
@@ -233,7 +344,7 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
                 const uint32_t key = kB.ok ? score_key(scB) : 0u;
                 key_out[cB] = key;
                 if (kB.ok) {
-                    atomicAdd(&hist[my_q][key >> 20], 1u);
+                    atomicAdd(&S.hist[my_q][key >> (32 - kHistBits)], 1u);
                     if (score_out) score_out[cB] = scB;
                 }
             }
@@ -243,16 +354,16 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
     for (int qi = 0; qi < job.n_q; ++qi) {
         uint32_t *gh = bufs.hist + ((int64_t)job.row[qi] * batch + b) * kHistBins;
         for (int i = tid; i < kHistBins; i += blockDim.x) {
-            const uint32_t c = hist[qi][i];
+            const uint32_t c = S.hist[qi][i];
             if (c) atomicAdd(gh + i, c);
         }
     }
 }
 
 // ---- threshold search over a histogram (block-wide) --------------------------
-// Finds bin d with above(d) < need <= above(d) + hist[d], where above(d) is the
-// count in bins > d.  If the total is < need, returns d = -1, above = total.
-// Requires blockDim.x * per == nbins.
+// Finds bin d with above(d) < need <= above(d) + h[d], where above(d) is the
+// count in bins > d.  If the total is < need, returns bin = -1, above = total.
+// Requires nbins % NT == 0.
 struct Thresh {
     int bin;
     uint32_t above;
@@ -267,7 +378,6 @@ __device__ Thresh find_threshold(const uint32_t *h, int nbins, uint32_t need, ui
     const int hi = nbins - tid * per;  // this thread covers [hi - per, hi), descending from the top
     uint32_t local = 0;
     for (int i = 1; i <= per; ++i) local += h[hi - i];
-    // inclusive scan over threads (thread 0 = top bins)
     uint32_t incl = local;
     const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -285,7 +395,7 @@ __device__ Thresh find_threshold(const uint32_t *h, int nbins, uint32_t need, ui
             uint32_t u = __shfl_up_sync(0xFFFFFFFFu, s, o);
             if (lane >= o) s += u;
         }
-        if (lane < NT / 32) scratch[lane] = s - v;  // exclusive warp offsets
+        if (lane < NT / 32) scratch[lane] = s - v;      // exclusive warp offsets
         if (lane == NT / 32 - 1) scratch[NT / 32] = s;  // total
     }
     __syncthreads();
@@ -324,258 +434,241 @@ __device__ __forceinline__ int row_len(const int32_t *seq_lens, int b, int max_l
     return L < 0 ? 0 : (L > max_len ? max_len : L);
 }
 
-// ---- collect ------------------------------------------------------------------
-__global__ void __launch_bounds__(256) collect_kernel(SelectPlan plan, int max_len, int *flags)
+struct SelSmem {
+    uint32_t h1[2048];   // local histogram of digit 2 (read by the cluster)
+    uint32_t h2[1024];   // local histogram of digit 3 (read by the cluster)
+    uint32_t red[2048];  // cluster-reduced histogram (this CTA's copy)
+    uint32_t cnt[4];     // [0] keys above T in this CTA, [1] ties at T (read by the cluster)
+    uint32_t wabove[kSelThreads / 32];
+    uint32_t wties[kSelThreads / 32];
+    uint32_t scratch[48];
+};
+
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelUnroll = 4;  // independent key loads in flight per lane
+
+// Visits a warp's contiguous range [r0, r1) in order, 32 keys per step (lane
+// = key), kSelUnroll steps of loads in flight: f(c, key, in_range) is called
+// by every lane of the warp for every step (f may use warp collectives).
+template <class F>
+__device__ __forceinline__ void for_range(const uint32_t *src, int64_t base, int64_t r0, int64_t r1, F &&f)
 {
-    __shared__ uint32_t hsm[kHistBins];
-    __shared__ uint32_t scratch[16];
-    const int b = blockIdx.y, rb = blockIdx.z;
+    const int lane = threadIdx.x & 31;
+    for (int64_t c0 = r0; c0 < r1; c0 += 32 * kSelUnroll) {
+        uint32_t k[kSelUnroll];
+#pragma unroll
+        for (int j = 0; j < kSelUnroll; ++j) {
+            const int64_t c = c0 + 32 * j + lane;
+            k[j] = (c < r1) ? src[c - base] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kSelUnroll; ++j) {
+            const int64_t c = c0 + 32 * j + lane;
+            f(c, k[j], c < r1);
+        }
+    }
+}
+
+// ---- select (one cluster of kSelCluster CTAs per row and target) ---------------
+// The row's candidates are split into kSelCluster contiguous slices (one per
+// CTA) and each slice into kSelWarps contiguous warp ranges, so position
+// order is (CTA rank, warp, lane).  Dynamic shared memory holds the CTA's
+// slice of keys when it fits (staged); otherwise the passes read it from
+// global memory (L2).
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+    select_kernel(SelectPlan plan, int max_len, int64_t stage_cap, int *flags)
+{
+    __shared__ SelSmem S;
+    __shared__ uint64_t stage_bar;
+    extern __shared__ __align__(16) uint32_t staged_keys[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const uint32_t rank = cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rb = blockIdx.y / plan.batch, b = blockIdx.y % plan.batch, tg = blockIdx.z;
     const SelectRow &R = plan.rows[rb];
+    if (tg == 1 && !(R.out_pool && plan.pool_out_len > 0)) return;  // uniform across the cluster
     const int64_t row = (int64_t)rb * plan.batch + b;
     const int L = row_len(plan.seq_lens, b, max_len);
     const int64_t n_cand = R.pool ? R.pool_len : L;
-    const int64_t base = (int64_t)blockIdx.x * kCollectChunk;
-    if (base >= n_cand) return;
-
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
-        hsm[i] = plan.bufs.hist[row * kHistBins + i];
-    __syncthreads();
-    const int n_targets = (R.out_pool && plan.pool_out_len > 0) ? 2 : 1;
-    Thresh th[2];
-    th[0] = find_threshold<256>(hsm, kHistBins, (uint32_t)plan.topk, scratch);
-    th[1] = th[0];
-    if (n_targets == 2) th[1] = find_threshold<256>(hsm, kHistBins, (uint32_t)plan.pool_out_len, scratch);
-
+    const uint32_t K = (uint32_t)(tg == 0 ? plan.topk : plan.pool_out_len);
+    int32_t *out = (tg == 0 ? R.out_idx : R.out_pool) + (int64_t)b * K;
     const uint32_t *keys = plan.bufs.keys + row * plan.bufs.cand_cap;
     const int32_t *pool = R.pool ? R.pool + (int64_t)b * R.pool_len : nullptr;
-    const int lane = threadIdx.x & 31;
-    const int64_t end = min(n_cand, base + (int64_t)kCollectChunk);
-    for (int64_t c0 = base + (threadIdx.x & ~31); c0 < end; c0 += blockDim.x) {
-        const int64_t c = c0 + lane;
-        uint32_t key = 0;
-        int64_t pos = -1;
-        if (c < end) {
-            key = keys[c];
-            pos = pool ? (int64_t)__ldg(pool + c) : c;
-        }
-        const bool valid = key != 0u && pos >= 0 && pos < L;
-        const int bin = (int)(key >> 20);
-        for (int tg = 0; tg < n_targets; ++tg) {
-            uint32_t *bm = plan.bufs.bitmap + (row * 2 + tg) * plan.bufs.bm_words;
-            const bool sel = valid && bin > th[tg].bin;
-            const bool eq = valid && bin == th[tg].bin;
-            if (!pool) {
-                const uint32_t word = __ballot_sync(0xFFFFFFFFu, sel);
-                if (lane == 0) bm[c0 >> 5] = word;
-            } else if (sel) {
-                atomicOr(bm + (pos >> 5), 1u << (pos & 31));
-            }
-            const uint32_t m = __ballot_sync(0xFFFFFFFFu, eq);
-            if (m) {
-                uint32_t *cnt = plan.bufs.cand_count + row * 2 + tg;
-                uint32_t off = 0;
-                if (lane == 0) off = atomicAdd(cnt, (uint32_t)__popc(m));
-                off = __shfl_sync(0xFFFFFFFFu, off, 0);
-                if (eq) {
-                    const uint32_t at = off + __popc(m & ((1u << lane) - 1u));
-                    if (at < (uint32_t)plan.bufs.cand_max)
-                        plan.bufs.cand[(row * 2 + tg) * plan.bufs.cand_max + at] =
-                            ((uint64_t)key << 32) | (uint32_t)pos;
-                }
-            }
-        }
+    // slices of a multiple of 32 keys, so each starts 128-B aligned
+    const int64_t chunk = ceil_div(ceil_div(n_cand, kSelCluster), 32) * 32;
+    const int64_t s0 = min(n_cand, (int64_t)rank * chunk), s1 = min(n_cand, s0 + chunk);
+    const int64_t span = ceil_div(s1 - s0, kSelWarps);
+    const int64_t r0 = min(s1, s0 + warp * span), r1 = min(s1, r0 + span);
+    const bool staged = (s1 - s0) <= stage_cap;
+    const uint32_t *src = staged ? staged_keys : keys;
+    const int64_t base = staged ? s0 : 0;
+
+    // digit 1: the global histogram of the top 11 bits (built by the scan)
+    for (int i = tid; i < 2048; i += kSelThreads) S.red[i] = plan.bufs.hist[row * kHistBins + i];
+    for (int i = tid; i < 2048; i += kSelThreads) S.h1[i] = 0u;
+    for (int i = tid; i < 1024; i += kSelThreads) S.h2[i] = 0u;
+    // stage the slice with bulk async copies (16-B multiples; the row is padded to 64 keys)
+    const uint32_t stage_bytes = staged ? (uint32_t)(ceil_div(s1 - s0, 4) * 16) : 0u;
+    if (stage_bytes && tid == 0) {
+        mbar_init(&stage_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        mbar_expect_tx(&stage_bar, stage_bytes);
+        for (uint32_t off = 0; off < stage_bytes; off += 16384u)
+            bulk_g2s(reinterpret_cast<uint8_t *>(staged_keys) + off,
+                     reinterpret_cast<const uint8_t *>(keys + s0) + off, min(16384u, stage_bytes - off), &stage_bar);
     }
-}
-
-// ---- finish -------------------------------------------------------------------
-// Composite order inside the boundary bin: (low 20 key bits, then ~position),
-// 52 bits, larger = earlier.  Unique per candidate.
-__device__ __forceinline__ uint64_t composite(uint32_t key, uint32_t pos)
-{
-    return ((uint64_t)(key & 0xFFFFFu) << 32) | (uint64_t)(~pos);
-}
-
-__global__ void __launch_bounds__(kFinishThreads) finish_kernel(SelectPlan plan, int max_len, int *flags)
-{
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t *elem = reinterpret_cast<uint64_t *>(smem);                                // cand_max
-    uint32_t *hsm = reinterpret_cast<uint32_t *>(smem + 8 * (size_t)plan.bufs.cand_max);  // 4096
-    __shared__ uint32_t scratch[48];
-    __shared__ uint64_t s_prefix;
-    __shared__ int s_nb;
-    __shared__ uint32_t s_need;
-
-    const int b = blockIdx.x, rb = blockIdx.y, tg = blockIdx.z;
-    const SelectRow &R = plan.rows[rb];
-    if (tg == 1 && !(R.out_pool && plan.pool_out_len > 0)) return;
-    const int64_t row = (int64_t)rb * plan.batch + b;
-    const int L = row_len(plan.seq_lens, b, max_len);
-    const int64_t n_cand = R.pool ? R.pool_len : L;
-    const int K = tg == 0 ? plan.topk : plan.pool_out_len;
-    int32_t *out = (tg == 0 ? R.out_idx : R.out_pool) + (int64_t)b * K;
-    uint32_t *bm = plan.bufs.bitmap + (row * 2 + tg) * plan.bufs.bm_words;
-    const int tid = threadIdx.x;
-
-    for (int i = tid; i < kHistBins; i += blockDim.x) hsm[i] = plan.bufs.hist[row * kHistBins + i];
     __syncthreads();
-    const Thresh th = find_threshold<kFinishThreads>(hsm, kHistBins, (uint32_t)K, scratch);
-    const uint32_t need0 = (th.bin >= 0) ? (uint32_t)K - th.above : 0u;
-
-    if (need0 > 0) {
-        const uint32_t count = plan.bufs.cand_count[row * 2 + tg];
-        const bool in_smem = count <= (uint32_t)plan.bufs.cand_max;
-        const uint64_t *gcand = plan.bufs.cand + (row * 2 + tg) * plan.bufs.cand_max;
-        const uint32_t *keys = plan.bufs.keys + row * plan.bufs.cand_cap;
-        const int32_t *pool = R.pool ? R.pool + (int64_t)b * R.pool_len : nullptr;
-        if (in_smem) {
-            for (uint32_t i = tid; i < count; i += blockDim.x) {
-                const uint64_t v = gcand[i];
-                elem[i] = composite((uint32_t)(v >> 32), (uint32_t)v);
-            }
-        } else if (tid == 0) {
-            raise_flag(flags, kFlagOverflow);
-        }
-        // Visit every boundary-bin candidate's composite (smem list, or a rescan of the
-        // row on the overflow path).
-        auto for_each = [&](auto &&f) {
-            if (in_smem) {
-                for (uint32_t i = tid; i < count; i += blockDim.x) f(elem[i]);
-            } else {
-                for (int64_t c = tid; c < n_cand; c += blockDim.x) {
-                    const uint32_t key = keys[c];
-                    const int64_t pos = pool ? (int64_t)__ldg(pool + c) : c;
-                    if (key != 0u && pos >= 0 && pos < L && (int)(key >> 20) == th.bin)
-                        f(composite(key, (uint32_t)pos));
-                }
-            }
-        };
-        if (tid == 0) {
-            s_prefix = 0;
-            s_nb = 0;
-            s_need = need0;
+    if (stage_bytes && !mbar_wait_bounded(&stage_bar, 0)) {
+        if (tid == 0) raise_flag(flags, kFlagTimeout);
+        mbar_wait_bounded(&stage_bar, 0);  // give copies in flight a last chance to land
+    }
+    const Thresh t0 = find_threshold<kSelThreads>(S.red, 2048, K, S.scratch);
+    const bool all_valid = t0.bin < 0;  // fewer candidates than K: take every valid one
+    uint32_t T = 0;                      // threshold key: select key > T, plus ties at T
+    uint32_t ties_needed = 0;
+    if (!all_valid) {
+        // digit 2: histogram of the threshold bin's keys
+        const uint32_t d0 = (uint32_t)t0.bin;
+        for_range(src, base, r0, r1, [&](int64_t, uint32_t k, bool) {
+            if (k != 0u && (k >> 21) == d0) atomicAdd(&S.h1[(k >> 10) & 2047u], 1u);
+        });
+        __syncthreads();
+        cluster.sync();
+        for (int i = tid; i < 2048; i += kSelThreads) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int r = 0; r < kSelCluster; ++r) v += cluster.map_shared_rank(S.h1, r)[i];
+            S.red[i] = v;
         }
         __syncthreads();
-        // radix select of the need0-th largest composite, 11-bit digits from bit 51
-        for (;;) {
-            const int nb = s_nb;
-            const uint64_t prefix = s_prefix;
-            const uint32_t need = s_need;
-            const int wbits = (52 - nb) < 11 ? (52 - nb) : 11;
-            const int shift = 52 - nb - wbits;
-            const int nbins = 1 << wbits;
-            for (int i = tid; i < 2048; i += blockDim.x) hsm[i] = 0u;
-            __syncthreads();
-            for_each([&](uint64_t cp) {
-                if ((cp >> (52 - nb)) == prefix || nb == 0)
-                    atomicAdd(&hsm[(cp >> shift) & (uint64_t)(nbins - 1)], 1u);
-            });
-            __syncthreads();
-            // bins above nbins are zero, so searching 2048 bins is equivalent
-            const Thresh d = find_threshold<kFinishThreads>(hsm, 2048, need, scratch);
-            if (tid == 0) {
-                s_prefix = (prefix << wbits) | (uint64_t)(d.bin < 0 ? 0 : d.bin);
-                s_nb = nb + wbits;
-                s_need = need - d.above;
-            }
-            __syncthreads();
-            if (d.bin < 0 || d.at == s_need || s_nb >= 52) break;
-        }
-        const uint64_t T = s_prefix << (52 - s_nb);
-        for_each([&](uint64_t cp) {
-            if (cp >= T) {
-                const uint32_t pos = ~(uint32_t)cp;
-                atomicOr(bm + (pos >> 5), 1u << (pos & 31));
-            }
+        const Thresh t1 = find_threshold<kSelThreads>(S.red, 2048, K - t0.above, S.scratch);
+        // digit 3
+        const uint32_t p01 = (d0 << 11) | (uint32_t)t1.bin;
+        for_range(src, base, r0, r1, [&](int64_t, uint32_t k, bool) {
+            if (k != 0u && (k >> 10) == p01) atomicAdd(&S.h2[k & 1023u], 1u);
         });
+        __syncthreads();
+        cluster.sync();
+        for (int i = tid; i < 1024; i += kSelThreads) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int r = 0; r < kSelCluster; ++r) v += cluster.map_shared_rank(S.h2, r)[i];
+            S.red[i] = v;
+        }
+        __syncthreads();
+        const Thresh t2 = find_threshold<kSelThreads>(S.red, 1024, K - t0.above - t1.above, S.scratch);
+        T = (p01 << 10) | (uint32_t)t2.bin;
+        ties_needed = K - t0.above - t1.above - t2.above;
+    }
+    // per-warp counts of keys above T and of ties at T, in position order
+    uint32_t wa = 0, wt = 0;
+    for_range(src, base, r0, r1, [&](int64_t, uint32_t k, bool) {
+        const bool valid = k != 0u;
+        wa += __popc(__ballot_sync(0xFFFFFFFFu, valid && (all_valid || k > T)));
+        wt += __popc(__ballot_sync(0xFFFFFFFFu, valid && !all_valid && k == T));
+    });
+    if (lane == 0) {
+        S.wabove[warp] = wa;
+        S.wties[warp] = wt;
     }
     __syncthreads();
+    if (tid == 0) {
+        uint32_t a = 0, t = 0;
+        for (int w = 0; w < kSelWarps; ++w) {
+            a += S.wabove[w];
+            t += S.wties[w];
+        }
+        S.cnt[0] = a;
+        S.cnt[1] = t;
+    }
+    __syncthreads();
+    cluster.sync();
+    // CTA-level prefixes over the cluster (rank order = position order)
+    uint32_t tie_before = 0, sel_before = 0, total = 0;
+    {
+        uint32_t tb = 0;
+        for (int r = 0; r < kSelCluster; ++r) {
+            const uint32_t *c = cluster.map_shared_rank(S.cnt, r);
+            const uint32_t ab = c[0], ti = c[1];
+            const uint32_t q = (ties_needed > tb) ? min(ties_needed - tb, ti) : 0u;
+            if ((uint32_t)r < rank) {
+                tie_before += ti;
+                sel_before += ab + q;
+            }
+            total += ab + q;
+            tb += ti;
+        }
+    }
+    __syncthreads();
+    cluster.sync();  // no remote shared-memory reads after this point
+    // warp-level prefixes inside the CTA
+    uint32_t wtie_before = tie_before, wsel_before = sel_before;
+    for (int w = 0; w < warp; ++w) {
+        const uint32_t ti = S.wties[w];
+        const uint32_t q = (ties_needed > wtie_before) ? min(ties_needed - wtie_before, ti) : 0u;
+        wsel_before += S.wabove[w] + q;
+        wtie_before += ti;
+    }
+    const uint32_t quota = (ties_needed > wtie_before) ? min(ties_needed - wtie_before, wt) : 0u;
 
-    // bitmap -> ascending positions
-    const int words = (int)ceil_div(L, 32);
-    const int per = (int)ceil_div(words, kFinishThreads);
-    const int w0 = tid * per, w1 = min(words, w0 + per);
-    uint32_t local = 0;
-    for (int w = w0; w < w1; ++w) {
-        uint32_t v = bm[w];
-        if (w == words - 1 && (L & 31)) v &= (1u << (L & 31)) - 1u;
-        local += __popc(v);
-    }
-    uint32_t incl = local;
-    const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) scratch[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t v = scratch[lane];
-        uint32_t s = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, s, o);
-            if (lane >= o) s += u;
+    // write this warp's winners in position order
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t written = 0, ties_seen = 0;
+    for_range(src, base, r0, r1, [&](int64_t c, uint32_t k, bool) {
+        const bool valid = k != 0u;
+        const bool is_tie = valid && !all_valid && k == T;
+        const uint32_t tm = __ballot_sync(0xFFFFFFFFu, is_tie);
+        const uint32_t tie_rank = ties_seen + __popc(tm & lt);
+        const bool sel = valid && (all_valid || k > T || (is_tie && tie_rank < quota));
+        const uint32_t sm = __ballot_sync(0xFFFFFFFFu, sel);
+        if (sel) {
+            const uint32_t at = wsel_before + written + __popc(sm & lt);
+            if (at < K) out[at] = pool ? __ldg(pool + c) : (int32_t)c;
         }
-        scratch[lane] = s - v;
-        if (lane == 31) scratch[32] = s;
-    }
-    __syncthreads();
-    uint32_t at = scratch[warp] + incl - local;
-    const uint32_t total = scratch[32];
-    for (int w = w0; w < w1; ++w) {
-        uint32_t v = bm[w];
-        if (w == words - 1 && (L & 31)) v &= (1u << (L & 31)) - 1u;
-        while (v) {
-            const int bit = __ffs(v) - 1;
-            v &= v - 1u;
-            if (at < (uint32_t)K) out[at] = w * 32 + bit;
-            ++at;
-        }
-    }
-    for (int i = (int)total + tid; i < K; i += blockDim.x) out[i] = -1;
-    if (tid == 0 && total > (uint32_t)K) raise_flag(flags, kFlagBounds);
+        written += __popc(sm);
+        ties_seen += __popc(tm);
+    });
+    for (uint32_t i = total + rank * kSelThreads + tid; i < K; i += kSelCluster * kSelThreads) out[i] = -1;
 }
 
 }  // namespace
 
+// Key rows are padded to a multiple of 64 candidates (256 B) so every row and
+// every select slice starts 16-B aligned for bulk copies.
+static int64_t padded_cap(int64_t cand_cap) { return ceil_div(cand_cap, 64) * 64; }
+
 size_t select_bytes(int n_rows, int64_t cand_cap, int max_seq_len)
 {
-    const int64_t bm_words = ceil_div(max_seq_len, 32);
-    const int64_t cand_max = 8192;
-    size_t bytes = 0;
-    auto add = [&](size_t n) { bytes += (n + 255) & ~(size_t)255; };
-    add((size_t)n_rows * kHistBins * 4);        // hist
-    add((size_t)n_rows * 2 * 4);                // cand_count
-    add((size_t)n_rows * cand_cap * 4);         // keys
-    add((size_t)n_rows * 2 * bm_words * 4);     // bitmaps
-    add((size_t)n_rows * 2 * cand_max * 8);     // boundary candidates
-    return bytes;
+    (void)max_seq_len;
+    auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    return r256((size_t)n_rows * kHistBins * 4) + r256((size_t)n_rows * padded_cap(cand_cap) * 4);
 }
 
 SelectBufs carve_select(uint8_t *base, int n_rows, int64_t cand_cap, int max_seq_len)
 {
+    (void)max_seq_len;
     SelectBufs s;
-    s.cand_cap = cand_cap;
-    s.bm_words = (int32_t)ceil_div(max_seq_len, 32);
-    s.cand_max = 8192;
-    size_t off = 0;
-    auto take = [&](size_t n) {
-        uint8_t *p = base + off;
-        off += (n + 255) & ~(size_t)255;
-        return p;
-    };
-    s.hist = reinterpret_cast<uint32_t *>(take((size_t)n_rows * kHistBins * 4));
-    s.cand_count = reinterpret_cast<uint32_t *>(take((size_t)n_rows * 2 * 4));
-    s.keys = reinterpret_cast<uint32_t *>(take((size_t)n_rows * cand_cap * 4));
-    s.bitmap = reinterpret_cast<uint32_t *>(take((size_t)n_rows * 2 * s.bm_words * 4));
-    s.cand = reinterpret_cast<uint64_t *>(take((size_t)n_rows * 2 * s.cand_max * 8));
+    s.cand_cap = padded_cap(cand_cap);
+    s.hist = reinterpret_cast<uint32_t *>(base);
+    s.keys = reinterpret_cast<uint32_t *>(base + (((size_t)n_rows * kHistBins * 4 + 255) & ~(size_t)255));
     return s;
 }
+
+size_t select_hist_bytes(int n_rows) { return (size_t)n_rows * kHistBins * 4; }
 
 cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan, int max_cand,
                         float *const (*scores)[2], int64_t scores_stride, int *flags, cudaStream_t stream)
 {
+    const size_t smem = sizeof(ScanSmem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
     for (int first = 0; first < n_jobs; first += kMaxScanJobs) {
         ScanBatch sb;
         sb.n_jobs = (n_jobs - first < kMaxScanJobs) ? n_jobs - first : kMaxScanJobs;
@@ -585,12 +678,12 @@ cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan,
             sb.out_scores[j][0] = scores ? scores[first + j][0] : nullptr;
             sb.out_scores[j][1] = scores ? scores[first + j][1] : nullptr;
         }
-        dim3 grid((unsigned)ceil_div(max_cand > 0 ? max_cand : 1, kScanChunk), (unsigned)plan.batch,
+        dim3 grid((unsigned)ceil_div(max_cand > 0 ? max_cand : 1, kScanKeys), (unsigned)plan.batch,
                   (unsigned)sb.n_jobs);
-        scan_kernel<<<grid, kScanWarps * 32, 0, stream>>>(sb, plan.bufs, plan.seq_lens, plan.batch,
-                                                         plan.max_len, flags);
+        scan_kernel<<<grid, kScanWarps * 32, smem, stream>>>(sb, plan.bufs, plan.seq_lens, plan.batch,
+                                                             plan.max_len, flags);
         count_launches(1);
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -599,27 +692,25 @@ cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan,
 cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cudaStream_t stream,
                           cudaEvent_t mid_event)
 {
-    const int max_len = plan.max_len;
-    dim3 cgrid((unsigned)ceil_div(max_cand > 0 ? max_cand : 1, kCollectChunk), (unsigned)plan.batch,
-               (unsigned)plan.n_row_blocks);
-    collect_kernel<<<cgrid, 256, 0, stream>>>(plan, max_len, flags);
-    count_launches(1);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const size_t smem = 8 * (size_t)plan.bufs.cand_max + 4 * kHistBins;
+    (void)mid_event;
+    // stage each CTA's slice of keys in shared memory when it fits in 160 KB
+    constexpr int64_t kStageMax = 40960;
+    const int64_t slice = ceil_div(ceil_div(max_cand > 0 ? max_cand : 1, kSelCluster), 32) * 32;
+    const int64_t cap = slice <= kStageMax ? slice : 0;
+    const size_t smem = (size_t)cap * 4;
     int dev = 0;
-    e = cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kStageMax * 4));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_set[dev] = true;
     }
-    dim3 fgrid((unsigned)plan.batch, (unsigned)plan.n_row_blocks, 2u);
-    finish_kernel<<<fgrid, kFinishThreads, smem, stream>>>(plan, max_len, flags);
+    dim3 grid((unsigned)kSelCluster, (unsigned)(plan.n_row_blocks * plan.batch), 2u);
+    select_kernel<<<grid, kSelThreads, smem, stream>>>(plan, plan.max_len, cap, flags);
     count_launches(1);
-    (void)mid_event;
     return cudaGetLastError();
 }
 

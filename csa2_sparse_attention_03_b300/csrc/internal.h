@@ -54,14 +54,9 @@ constexpr int kMaxScanJobs = 16;
 
 // Per-row selection buffers inside the workspace.
 struct SelectBufs {
-    uint32_t *keys;       // [n_rows][cand_cap]    order-preserving score keys
-    uint32_t *hist;       // [n_rows][kHistBins]   first-level histogram
-    uint32_t *bitmap;     // [n_rows][2][bm_words] selected positions (topk, pool)
-    uint64_t *cand;       // [n_rows][2][cand_max] boundary-bin candidates (key, pos)
-    uint32_t *cand_count; // [n_rows][2]
+    uint32_t *hist;       // [n_rows][kHistBins] histogram of the keys' top bits (zeroed per call)
+    uint32_t *keys;       // [n_rows][cand_cap]  order-preserving score keys, 0 = not a candidate
     int64_t cand_cap;     // candidates per row (max_seq_len or pool_len)
-    int32_t bm_words;     // bitmap words per row (ceil(max_seq_len/32))
-    int32_t cand_max;     // boundary candidate capacity per row and target
 };
 
 // A selection row: which targets (topk, pool) it produces.
@@ -92,6 +87,7 @@ cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan,
 cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cudaStream_t stream,
                           cudaEvent_t mid_event);
 size_t select_bytes(int n_rows, int64_t cand_cap, int max_seq_len);
+size_t select_hist_bytes(int n_rows);  // the leading part of the region to zero before a scan
 SelectBufs carve_select(uint8_t *base, int n_rows, int64_t cand_cap, int max_seq_len);
 
 // ---- step 3: sparse attention --------------------------------------------

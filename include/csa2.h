@@ -28,9 +28,10 @@
  *  - Functions return a csa2_status and never throw.  On failure nothing was
  *    enqueued (argument errors) or a launch failed (CSA2_ERR_CUDA);
  *    csa2_last_error() returns a message for the calling thread.
- *  - Data-dependent faults (an index or page outside its cache, a candidate
- *    buffer overflow handled on the slow path) never fault the GPU: the
- *    kernel skips the access and records a flag read by csa2_check_device().
+ *  - Data-dependent faults (an index or page outside its cache) never fault
+ *    the GPU: the kernel skips the access and records a flag read by
+ *    csa2_check_device().  Waits on asynchronous copies are bounded: one that
+ *    gives up records a flag instead of hanging.
  *  - Widths are fixed: attention 16 heads x 512 channels (MQA over one shared
  *    512-channel row that is both key and value); indexer 4 heads x 64.
  *  - Positions of sequence b are 0 .. seq_lens[b]-1; the current decode
@@ -244,8 +245,7 @@ const char *csa2_last_error(void);
  * range and skipped) or CSA2_ERR_TIMEOUT. */
 csa2_status csa2_check_device(void *stream);
 /* Raw flag bits seen by the calling thread's last csa2_check_device():
- * 1 = out-of-range access skipped, 2 = wait gave up, 4 = a Top-K boundary bin
- * overflowed its candidate buffer and the exact slow path ran (not an error). */
+ * 1 = out-of-range access skipped, 2 = a bounded wait gave up. */
 int32_t csa2_last_device_flags(void);
 /* Profiling hook: when n > 0, csa2_decode_layers records events[i] (cudaEvent_t
  * created by the caller) on its stream after phase i: 0 appends, 1 level-0

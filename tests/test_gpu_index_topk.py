@@ -1,6 +1,6 @@
 """Step 2 parity: indexer scores bit-exact and Top-K index sets identical to the
 oracle (Full, Reindex over a pool, the Full layer's pool, ties, tiny and
-overflowing boundary bins)."""
+ties that span the select cluster's slices)."""
 import numpy as np
 import pytest
 import torch
@@ -94,9 +94,9 @@ def test_ties_take_lower_positions(cuda, orc):
     assert np.array_equal(idx[0].cpu().numpy(), orc.topk(s, np.arange(L, dtype=np.int32), K))
 
 
-def test_all_equal_scores_take_overflow_path(cuda, orc):
-    """20,000 identical keys: the boundary bin holds every candidate (> the
-    8,192-entry buffer), the exact slow path runs, positions 0..K-1 win."""
+def test_all_equal_scores_take_lowest_positions(cuda, orc):
+    """20,000 identical keys: every radix digit ties, the tie quota spreads over
+    the select cluster's slices, and positions 0..K-1 win."""
     L, K = 20000, 100
     x = np.tile(synth.normal_rows(14, "tk", (0,), 0, 1, 64), (L, 1))
     cache, _ = _keys(cuda, orc, [x], 20032)
@@ -105,8 +105,13 @@ def test_all_equal_scores_take_overflow_path(cuda, orc):
     idx, _, _ = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(),
                                      seq, L, K)
     st, flags = cuda.csa2_check_device()
-    assert st == 0 and (flags & 4)
+    assert st == 0, (st, flags)
     assert np.array_equal(idx[0].cpu().numpy(), np.arange(K))
+    # a quota that crosses slice boundaries: K larger than one slice (L / 8)
+    K2 = 5000
+    idx2, _, _ = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(),
+                                      torch.from_numpy(w).cuda(), seq, L, K2)
+    assert np.array_equal(idx2[0].cpu().numpy(), np.arange(K2))
 
 
 def test_extreme_codes_are_exact(cuda, orc):
