@@ -3,462 +3,737 @@
 // both (Louis Bouchard's KV-cache report, "Share the cache and the search
 // work": the selected global entries beside a local 128-token window;
 // Helmcode "DeepSeek V4.1 Flash" explainer, "04 · FP4": FP4 global KV, FP8
-// window KV).  16 query heads attend over one shared 512-channel row that is
-// both key and value.
+// window KV; "03 · CSA2": a Reuse layer attends with its own query over the
+// selection of another layer).  16 query heads attend over one shared
+// 512-channel row that is both key and value.
 //
-// Work item = (layer entry, sequence, chunk of the row list).  A CTA streams
-// its chunk in 64-row tiles:
-//   gather   cp.async 16-B copies of the raw rows into a double-buffered
-//            staging area (288 B per FP4 row, 512 B per FP8 row), so the next
-//            tile's HBM reads overlap this tile's math;
-//   dequant  E2M1 x E4M3 -> fp16 and E4M3 -> fp16 are exact (<= 6 and 4
-//            significant bits); the FP8 per-token scale is applied to the
-//            logits and folded into the softmax weights instead;
-//   QK, PV   m16n8k16 fp16 MMAs with fp32 accumulation; fp32 online softmax.
-// Chunks of one (entry, sequence) are merged by log-sum-exp in a second kernel.
+// Work decomposition.  Layers that attend over the same selected rows (an
+// indexing layer and the Reuse layers that take its Top-K) form a *row unit*
+// of up to 8 layers: their 8 x 16 = 128 query rows share every gathered row,
+// so a row is read and dequantised once for all of them and QK^T and PV are
+// 128-row tensor-core products.  Each layer's own window rows form a *window
+// unit*.  A CTA takes one (unit, chunk of rows, half of the output channels,
+// sequence) and produces a partial (running max, sum, unnormalised output);
+// the last CTA to finish a (layer, sequence, half) merges its partials.
+//
+// One CTA, 9 warps:
+//   warps 4-7  producers: cp.async gather of the raw rows of a 32-row tile,
+//              exact dequantisation to fp16 (E2M1 x E4M3 and E4M3 are exact
+//              in fp16) into the tile's core-matrix layout;
+//   warp 8     tensor-memory allocation and tcgen05.mma issue:
+//              S[b] = Q V^T (M 128, N 32, K 512) into tensor memory, then
+//              O += P V (M 128, N 256, K 32) with O resident in tensor memory;
+//   warps 0-3  one thread per query row: S from tensor memory, fp32 online
+//              softmax with lazy rescaling of O (only when the running max
+//              grows by more than e^8), P to shared memory as fp16.
+// V and S are double-buffered, P single; every hand-off is an mbarrier with
+// a bounded wait (a wait that gives up raises the timeout flag and the CTA
+// drains and exits).
+#include <algorithm>
+#include <cstring>
+#include <utility>
+#include <vector>
+
 #include "internal.h"
+#include "tc.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kAttnThreads = 128;  // 4 warps
-constexpr int kTileRows = 64;
-constexpr int kVStride = kDim + 8;    // halves per dequantised row (1,040 B: ldmatrix conflict-free)
-constexpr int kPStride = kTileRows + 8;
-constexpr int kStageRow = 512;        // staging bytes per row (FP4 rows use 288)
-constexpr int kPartFloats = kHeads * kDim + 2 * kHeads;
+constexpr int kTile = 32;                  // rows per tile
+constexpr int kThreads = 288;              // 9 warps
+constexpr int kQRowsBytes = kHeads * kDim * 2;  // 16 KB: one layer's 16 query rows in fp16
+constexpr int kQBytes = 8 * kQRowsBytes;   // 131,072: 128 query rows
+constexpr int kVBytes = kTile * kDim * 2;  // 32,768 per buffer
+constexpr int kPBytes = 128 * kTile * 2;   // 8,192
+constexpr int kRawHalf = 9216;             // one tile of 32 FP4 rows (288 B each)
+constexpr int kRawBytes = 2 * kRawHalf;    // two FP4 tiles, or one tile of 32 FP8 rows (16 KB)
+constexpr int kOffV = kQBytes;
+constexpr int kOffP = kOffV + 2 * kVBytes;
+constexpr int kOffRaw = kOffP + kPBytes;
+constexpr int kOffMisc = kOffRaw + kRawBytes;
+constexpr int kPartFloats = 64 + kHeads * kDim;  // m[2][16], l[2][16], O[16][512]
+constexpr int kMaxUnits = 2 * kMaxAttnEntries;
+constexpr float kRescaleGap = 8.0f;        // lazy O rescale threshold (natural log)
+constexpr uint32_t kTmemCols = 512;        // S[0] cols 0-31, S[1] cols 32-63, O cols 256-511
+constexpr uint32_t kColO = 256;
+// Instruction descriptors: QK^T (both operands K-major), PV (B = V read MN-major).
+constexpr uint32_t kIdescQK = tc::idesc_f16(128, kTile, false, false);
+constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, false, true);
 
-struct AttnBatch {
-    AttnEntry e[kMaxAttnEntries];
+struct AttnMisc {
+    const uint8_t *rowptr[2][kTile];  // per raw buffer
+    float rscale[2][kTile];
+    int32_t rvalid[2][kTile];
+    float mscale[2][kTile];           // per V buffer (read by the softmax warps)
+    int32_t mvalid[2][kTile];
+    uint64_t q_bar, full_v[2], s_full[2], s_free[2], p_full, pv_done[2];
+    uint32_t tmem_slot;
+    int32_t last[8];
+};
+static_assert(kOffMisc + (int)sizeof(AttnMisc) <= 232448, "attention shared memory over the 227 KB limit");
+
+struct UnitDev {
+    CacheView cache;        // FP4_KV cache (row unit) or FP8_SWA ring (window unit)
+    const int32_t *idx;     // row unit: [B][topk]
+    int32_t is_window;
+    int32_t n_layers;       // consumer layers (1..8)
+    int32_t entry[8];
+    int32_t cta_begin;      // first flat CTA (x) index of this unit
 };
 
-struct __align__(16) AttnSmem {
-    __half V[kTileRows * kVStride];
-    __half Q[kHeads * kVStride];
-    __half P[kHeads * kPStride];
-    uint8_t stage[2][kTileRows * kStageRow];
-    const uint8_t *rowptr[2][kTileRows];
-    float rowscale[2][kTileRows];
-    int32_t rowtype[2][kTileRows];  // 0 invalid, 1 FP4 main row, 2 FP8 window row
-    float red[2][4][kHeads];
+struct EntryDev {
+    float *out;             // [B][16][512]
+    float *lse;             // [B][16] or null
+    int32_t n_parts;        // partials of this layer: row chunks + window
+    int32_t part_win;       // part id of the window partial (or -1); row chunk c has part id c
 };
 
-__device__ __forceinline__ void mma_acc(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+struct AttnParams {
+    UnitDev units[kMaxUnits];
+    EntryDev entries[kMaxAttnEntries];
+    int32_t n_units;
+    int32_t batch, topk, window, rows_per_chunk, max_parts;
+    const int32_t *seq_lens;
+    const uint8_t *q16;     // [entry][B][16 KB] fp16 query rows in core-matrix layout
+    float *partials;        // [entry][B][max_parts][kPartFloats]
+    uint32_t *counters;     // [entry][B][2]
+};
+
+struct QList {
+    const float *q[kMaxAttnEntries];
+};
+
+// Byte offset of fp16 element (row r, channel c) of an operand with 512-channel
+// rows in the no-swizzle core-matrix layout: 8-row groups 8,192 B apart,
+// 8-channel groups 128 B apart.
+__device__ __forceinline__ uint32_t cm_off512(uint32_t r, uint32_t c)
 {
+    return (r >> 3) * 8192u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
+}
+
+__device__ __forceinline__ uint32_t pack_h2(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
+
+// q (fp32 [B][16][512]) -> fp16 core-matrix rows, 16 KB per layer and sequence.
+__global__ void __launch_bounds__(256) pack_q_kernel(const __grid_constant__ QList qs, uint8_t *q16, int batch)
+{
+    const int e = blockIdx.x, b = blockIdx.y;
+    const float *q = qs.q[e] + (int64_t)b * kHeads * kDim;
+    uint8_t *dst = q16 + ((int64_t)e * batch + b) * kQRowsBytes;
+    for (int it = threadIdx.x; it < kHeads * kDim / 8; it += blockDim.x) {
+        const int r = it / (kDim / 8), c = (it % (kDim / 8)) * 8;
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(q + r * kDim + c));
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(q + r * kDim + c + 4));
+        *reinterpret_cast<uint4 *>(dst + cm_off512(r, c)) =
+            make_uint4(pack_h2(__floats2half2_rn(a.x, a.y)), pack_h2(__floats2half2_rn(a.z, a.w)),
+                       pack_h2(__floats2half2_rn(d.x, d.y)), pack_h2(__floats2half2_rn(d.z, d.w)));
+    }
+}
+
+// OR-reduction of a predicate over the 128 threads of named barrier `id`
+// (also a barrier); every participant gets the same result.
+__device__ __forceinline__ bool bar_any(uint32_t id, bool p)
+{
+    uint32_t r;
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, %2, 128, a;\n selp.u32 %0, 1, 0, o;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)p), "r"(id)
+        : "memory");
+    return r != 0;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void *p)
-{
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], const void *p)
-{
-    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
-{
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
-
-// Row list of one (entry, sequence): [0, nsel) selected FP4 rows, then the window.
-struct RowList {
-    const AttnEntry *e;
-    const int32_t *idx;
-    int b, L, nsel, window;
+// Everything one CTA needs to know about its work item.
+struct Ctx {
+    const AttnParams *P;
+    const UnitDev *U;
+    AttnMisc *M;
+    uint8_t *Qs, *Vs, *Ps, *Raw;
+    int *flags;
+    uint32_t tmem;
+    int b, L, W, row0, n_rows, n_tiles, chunk, half;
+    bool fp8;
 };
 
-__device__ __forceinline__ void row_meta(const RowList &rl, int64_t v, const uint8_t *&ptr, int &type,
-                                         float &rs, int *flags)
+// ---- producers (warps 4-7): gather + dequantise 32-row tiles -------------------------
+__device__ __forceinline__ void produce(const Ctx &c)
 {
-    ptr = nullptr;
-    type = 0;
-    rs = 0.0f;
-    if (v < rl.nsel) {
-        const int32_t pos = __ldg(rl.idx + v);
-        if (pos < 0) return;
-        if (pos >= rl.L) {
-            raise_flag(flags, kFlagBounds);
-            return;
-        }
-        const int64_t slot = slot_of(rl.e->kv, rl.b, pos);
-        if (slot < 0) {
-            raise_flag(flags, kFlagBounds);
-            return;
-        }
-        ptr = rl.e->kv.data + slot * kKvRow;
-        type = 1;
-        rs = 1.0f;
-    } else if (v < (int64_t)rl.nsel + rl.window) {
-        const int64_t pos = (int64_t)rl.L - rl.window + (v - rl.nsel);
-        if (pos < 0) return;
-        const int64_t slot = slot_of(rl.e->swa, rl.b, pos);
-        if (slot < 0) {
-            raise_flag(flags, kFlagBounds);
-            return;
-        }
-        ptr = rl.e->swa.data + slot * kDim;
-        type = 2;
-        rs = __ldg(reinterpret_cast<const float *>(rl.e->swa.data + rl.e->swa.n_slots * kDim) + slot);
-    }
-}
-
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const __grid_constant__ AttnBatch ab, AttnPlan plan,
-                                                             int *flags)
-{
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    AttnSmem &S = *reinterpret_cast<AttnSmem *>(smem_raw);
-    const int chunk = blockIdx.x, b = blockIdx.y, ei = blockIdx.z;
-    const AttnEntry &E = ab.e[ei];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
-
-    RowList rl;
-    rl.e = &E;
-    rl.b = b;
-    rl.L = __ldg(plan.seq_lens + b);
-    if (rl.L < 0) rl.L = 0;
-    rl.nsel = (E.has_kv && E.idx) ? plan.topk : 0;
-    rl.idx = E.idx ? E.idx + (int64_t)b * plan.topk : nullptr;
-    rl.window = E.has_swa ? plan.window : 0;
-    const int total_rows = rl.nsel + rl.window;
-    const int tiles = (total_rows + kTileRows - 1) / kTileRows;
-    const int per = (tiles + plan.n_chunks - 1) / plan.n_chunks;
-    const int t0 = chunk * per;
-    const int t1 = min(tiles, t0 + per);
-
-    // query -> fp16 in shared memory
-    const float *q = E.q + (int64_t)b * kHeads * kDim;
-    for (int i = tid; i < kHeads * kDim / 4; i += kAttnThreads) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(q) + i);
-        const int h = (4 * i) / kDim, c = (4 * i) % kDim;
-        __half2 *dst = reinterpret_cast<__half2 *>(&S.Q[h * kVStride + c]);
-        dst[0] = __floats2half2_rn(v.x, v.y);
-        dst[1] = __floats2half2_rn(v.z, v.w);
-    }
-
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-
-    auto issue = [&](int tile, int buf) {
-        if (tid < kTileRows) {
-            const uint8_t *p;
-            int ty;
-            float rs;
-            row_meta(rl, (int64_t)tile * kTileRows + tid, p, ty, rs, flags);
-            S.rowptr[buf][tid] = p;
-            S.rowtype[buf][tid] = ty;
-            S.rowscale[buf][tid] = rs;
-        }
-        __syncthreads();
-        for (int k = tid; k < kTileRows * 32; k += kAttnThreads) {
-            const int j = k >> 5, c = k & 31;
-            const int ty = S.rowtype[buf][j];
-            if (ty == 0 || (ty == 1 && c >= kKvRow / 16)) continue;
-            cp_async16(&S.stage[buf][j * kStageRow + c * 16], S.rowptr[buf][j] + c * 16);
-        }
-        cp_async_commit();
-    };
-
-    if (t0 < t1) issue(t0, 0);
-    for (int tile = t0; tile < t1; ++tile) {
-        const int cb = (tile - t0) & 1;
-        if (tile + 1 < t1) {
-            issue(tile + 1, cb ^ 1);
-        } else {
-            cp_async_commit();  // empty group keeps the wait count uniform
-        }
-        cp_async_wait1();
-        __syncthreads();
-
-        // dequantise the staged tile into V (fp16); invalid rows become zeros
-        for (int k = tid; k < kTileRows * 16; k += kAttnThreads) {
-            const int j = k >> 4, grp = k & 15;  // 32 channels per task
-            const int ty = S.rowtype[cb][j];
-            uint4 *dst = reinterpret_cast<uint4 *>(&S.V[j * kVStride + grp * 32]);
-            const uint8_t *src = &S.stage[cb][j * kStageRow];
-            if (ty == 1) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(src + grp * 16);
-                const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(src + kKvCodes + 2 * grp);
-                const __half2 s0 = __half2half2(__ushort_as_half(__half_as_ushort(__float2half_rn(e4m3_value(sc2 & 0xFFu)))));
-                const __half2 s1 = __half2half2(__ushort_as_half(__half_as_ushort(__float2half_rn(e4m3_value(sc2 >> 8)))));
-                const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t h[16];
-#pragma unroll
-                for (int wd = 0; wd < 4; ++wd) {
-#pragma unroll
-                    for (int by = 0; by < 4; ++by) {
-                        const uint32_t bits = e2m1x2_half2_bits((words[wd] >> (8 * by)) & 0xFFu);
-                        __half2 v = *reinterpret_cast<const __half2 *>(&bits);
-                        v = __hmul2(v, wd < 2 ? s0 : s1);
-                        h[wd * 4 + by] = *reinterpret_cast<uint32_t *>(&v);
+    AttnMisc &M = *c.M;
+    const UnitDev &U = *c.U;
+    const int ptid = threadIdx.x - 128;
+    // row metadata of tile t into raw buffer rb, then cp.async of its bytes
+    auto gather = [&](int t, int rb) {
+        if (ptid < kTile) {
+            const int v = c.row0 + t * kTile + ptid;
+            const uint8_t *ptr = nullptr;
+            float sc = 0.0f;
+            if (v < c.row0 + c.n_rows) {
+                if (!c.fp8) {
+                    const int32_t pos = __ldg(U.idx + (int64_t)c.b * c.P->topk + v);
+                    if (pos >= 0) {
+                        const int64_t slot = pos < c.L ? slot_of(U.cache, c.b, pos) : -1;
+                        if (slot < 0) {
+                            raise_flag(c.flags, kFlagBounds);
+                        } else {
+                            ptr = U.cache.data + slot * kKvRow;
+                            sc = 1.0f;
+                        }
+                    }
+                } else {
+                    const int64_t pos = (int64_t)c.L - c.W + v;
+                    if (pos >= 0) {
+                        const int64_t slot = slot_of(U.cache, c.b, pos);
+                        if (slot < 0) {
+                            raise_flag(c.flags, kFlagBounds);
+                        } else {
+                            ptr = U.cache.data + slot * kDim;
+                            sc = __ldg(reinterpret_cast<const float *>(U.cache.data + U.cache.n_slots * kDim) + slot);
+                        }
                     }
                 }
+            }
+            M.rowptr[rb][ptid] = ptr;
+            M.rscale[rb][ptid] = sc;
+            M.rvalid[rb][ptid] = ptr != nullptr;
+        }
+        tc::named_sync(1, 128);
+        if (!c.fp8) {
+            uint8_t *raw = c.Raw + rb * kRawHalf;
+            for (int k = ptid; k < kTile * (kKvRow / 16); k += 128) {
+                const int j = k / (kKvRow / 16), g = k % (kKvRow / 16);
+                const uint8_t *src = M.rowptr[rb][j];
+                if (src) tc::cp_async16(raw + j * kKvRow + g * 16, src + g * 16);
+            }
+        } else {
+            for (int k = ptid; k < kTile * (kDim / 16); k += 128) {
+                const int j = k / (kDim / 16), g = k % (kDim / 16);
+                const uint8_t *src = M.rowptr[0][j];
+                if (src) tc::cp_async16(c.Raw + j * kDim + g * 16, src + g * 16);
+            }
+        }
+        tc::cp_async_commit();
+    };
+
+    if (c.n_tiles > 0) gather(0, 0);
+    for (int t = 0; t < c.n_tiles; ++t) {
+        const int vb = t & 1;
+        const int rb = c.fp8 ? 0 : (t & 1);
+        if (!c.fp8) {
+            if (t + 1 < c.n_tiles) gather(t + 1, (t + 1) & 1);
+            else tc::cp_async_commit();  // keep one group per iteration
+            tc::cp_async_wait_one();
+        } else {
+            if (t > 0) gather(t, 0);
+            tc::cp_async_wait_all();
+        }
+        // V[vb] and its row metadata are free once PV(t-2) has finished
+        const bool bad = (t >= 2) && !tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
+        if (bar_any(1, bad)) {  // also the barrier after every producer's rows have landed
+            if (ptid == 0) raise_flag(c.flags, kFlagTimeout);
+            break;
+        }
+        uint8_t *V = c.Vs + vb * kVBytes;
+        if (!c.fp8) {
+            const uint8_t *raw = c.Raw + rb * kRawHalf;
+            for (int k = ptid; k < kTile * 16; k += 128) {
+                const int j = k & (kTile - 1), g = k >> 5;  // row j, channels 32g..32g+31
+                uint4 o[4];
+                if (M.rvalid[rb][j]) {
+                    const uint8_t *src = raw + j * kKvRow;
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(src + g * 16);
+                    const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(src + kKvCodes + 2 * g);
+                    const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(sc2 & 0xFFu)));
+                    const __half2 s1 = __half2half2(__float2half_rn(e4m3_value(sc2 >> 8)));
+                    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+                    uint32_t h[16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-            } else if (ty == 2) {
-                const uint4 r0 = *reinterpret_cast<const uint4 *>(src + grp * 32);
-                const uint4 r1 = *reinterpret_cast<const uint4 *>(src + grp * 32 + 16);
-                const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-                uint32_t h[16];
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t bits = e2m1x2_half2_bits((w[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+                        const __half2 x = *reinterpret_cast<const __half2 *>(&bits);
+                        h[i] = pack_h2(__hmul2(x, i < 8 ? s0 : s1));
+                    }
 #pragma unroll
-                for (int wd = 0; wd < 8; ++wd) {
-                    __half2 lo = e4m3x2_half2(words[wd] & 0xFFFFu);
-                    __half2 hi = e4m3x2_half2(words[wd] >> 16);
-                    h[2 * wd] = *reinterpret_cast<uint32_t *>(&lo);
-                    h[2 * wd + 1] = *reinterpret_cast<uint32_t *>(&hi);
+                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(V + cm_off512(j, 32 * g + 8 * i)) = o[i];
+            }
+        } else {
+            for (int k = ptid; k < kTile * 32; k += 128) {
+                const int j = k & (kTile - 1), g = k >> 5;  // row j, channels 16g..16g+15
+                uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+                if (M.rvalid[0][j]) {
+                    const uint4 cw = *reinterpret_cast<const uint4 *>(c.Raw + j * kDim + g * 16);
+                    o0 = make_uint4(pack_h2(e4m3x2_half2(cw.x & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.x >> 16)),
+                                    pack_h2(e4m3x2_half2(cw.y & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.y >> 16)));
+                    o1 = make_uint4(pack_h2(e4m3x2_half2(cw.z & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.z >> 16)),
+                                    pack_h2(e4m3x2_half2(cw.w & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.w >> 16)));
+                }
+                *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g)) = o0;
+                *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g + 8)) = o1;
             }
         }
-        __syncthreads();
-
-        // S = Q K^T for keys 16w .. 16w+15
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 8
-        for (int ks = 0; ks < kDim / 16; ++ks) {
-            uint32_t a[4], bq[4];
-            ldsm_x4(a, &S.Q[(lane & 15) * kVStride + ks * 16 + 8 * (lane >> 4)]);
-            ldsm_x4(bq, &S.V[(16 * warp + (lane & 7) + 8 * (lane >> 4)) * kVStride + ks * 16 + 8 * ((lane >> 3) & 1)]);
-            mma_acc(s[0], a, bq[0], bq[1]);
-            mma_acc(s[1], a, bq[2], bq[3]);
+        if (ptid < kTile) {
+            M.mvalid[vb][ptid] = M.rvalid[rb][ptid];
+            M.mscale[vb][ptid] = M.rscale[rb][ptid];
         }
-        // logits: per-row scale (FP8 rows), masking of invalid rows
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int key = 16 * warp + 8 * nt + 2 * t + (e & 1);
-                const float v = S.rowtype[cb][key] ? s[nt][e] * S.rowscale[cb][key] : -INFINITY;
-                s[nt][e] = v;
-                mx[e >> 1] = fmaxf(mx[e >> 1], v);
-            }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
-        }
-        if (t == 0) {
-            S.red[0][warp][g] = mx[0];
-            S.red[0][warp][g + 8] = mx[1];
-        }
-        __syncthreads();
-        float alpha[2], mnew[2], sum[2] = {0.0f, 0.0f};
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = g + 8 * r;
-            float tm = fmaxf(fmaxf(S.red[0][0][row], S.red[0][1][row]), fmaxf(S.red[0][2][row], S.red[0][3][row]));
-            mnew[r] = fmaxf(m_run[r], tm);
-            alpha[r] = (mnew[r] == -INFINITY) ? 1.0f : __expf(m_run[r] - mnew[r]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float pv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = e >> 1;
-                const float p = (s[nt][e] == -INFINITY) ? 0.0f : __expf(s[nt][e] - mnew[r]);
-                sum[r] += p;
-                const int key = 16 * warp + 8 * nt + 2 * t + (e & 1);
-                pv[e] = p * S.rowscale[cb][key];
-            }
-            *reinterpret_cast<__half2 *>(&S.P[g * kPStride + 16 * warp + 8 * nt + 2 * t]) = __floats2half2_rn(pv[0], pv[1]);
-            *reinterpret_cast<__half2 *>(&S.P[(g + 8) * kPStride + 16 * warp + 8 * nt + 2 * t]) = __floats2half2_rn(pv[2], pv[3]);
-        }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            sum[r] += __shfl_xor_sync(0xFFFFFFFFu, sum[r], 1);
-            sum[r] += __shfl_xor_sync(0xFFFFFFFFu, sum[r], 2);
-        }
-        if (t == 0) {
-            S.red[1][warp][g] = sum[0];
-            S.red[1][warp][g + 8] = sum[1];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = g + 8 * r;
-            const float ts = (S.red[1][0][row] + S.red[1][1][row]) + (S.red[1][2][row] + S.red[1][3][row]);
-            l_run[r] = l_run[r] * alpha[r] + ts;
-            m_run[r] = mnew[r];
-        }
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-        }
-        // O += P V for channels 128w .. 128w+127
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {
-            uint32_t a[4];
-            ldsm_x4(a, &S.P[(lane & 15) * kPStride + kk * 16 + 8 * (lane >> 4)]);
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                uint32_t bv[4];
-                ldsm_x4_t(bv, &S.V[(kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * kVStride + 128 * warp + 16 * np + 8 * (lane >> 4)]);
-                mma_acc(o[2 * np], a, bv[0], bv[1]);
-                mma_acc(o[2 * np + 1], a, bv[2], bv[3]);
-            }
-        }
-        __syncthreads();
+        tc::fence_async_smem();
+        tc::mbar_arrive(&M.full_v[vb]);
+        tc::named_sync(1, 128);  // raw[rb] may be refilled after this
     }
+    tc::cp_async_wait_all();
+}
 
-    // epilogue
-    if (plan.n_chunks == 1) {
-        float *out = E.out + (int64_t)b * kHeads * kDim;
-        const float inv0 = l_run[0] > 0.0f ? 1.0f / l_run[0] : 0.0f;
-        const float inv1 = l_run[1] > 0.0f ? 1.0f / l_run[1] : 0.0f;
+// ---- MMA issuer (warp 8, lane 0) -----------------------------------------------------
+__device__ __forceinline__ void issue_mmas(const Ctx &c)
+{
+    AttnMisc &M = *c.M;
+    const UnitDev &U = *c.U;
+    // query rows of the consumer layers: layer slot j -> rows 16j..16j+15 (16 KB each)
+    tc::mbar_expect_tx(&M.q_bar, (uint32_t)U.n_layers * kQRowsBytes);
+    for (int j = 0; j < U.n_layers; ++j)
+        tc::bulk_g2s(c.Qs + j * kQRowsBytes, c.P->q16 + ((int64_t)U.entry[j] * c.P->batch + c.b) * kQRowsBytes,
+                     kQRowsBytes, &M.q_bar);
+    bool ok = tc::mbar_wait(&M.q_bar, 0);
+    if (!ok) tc::mbar_wait(&M.q_bar, 0);  // let copies in flight land before giving up
+    uint64_t *last_bar = nullptr;
+    uint32_t last_par = 0;
+    const uint32_t qa = tc::smem_u32(c.Qs), pa = tc::smem_u32(c.Ps);
+    auto issue_pv = [&](int t) {
+        if (!tc::mbar_wait(&M.p_full, t & 1)) {
+            ok = false;
+            return;
+        }
+        tc::fence_after_sync();
+        // B = V[t&1] read MN-major: N = this CTA's 256 channels (8-channel groups 128 B apart),
+        // K = 32 keys (8-key groups 8,192 B apart)
+        const uint32_t vb = tc::smem_u32(c.Vs + (t & 1) * kVBytes) + c.half * (256 / 8) * 128;
+        for (int ks = 0; ks < kTile / 16; ++ks)
+            tc::mma_f16(c.tmem + kColO, tc::sdesc(pa + ks * 256, 128, 512), tc::sdesc(vb + ks * 2 * 8192, 8192, 128),
+                        kIdescPV, (t > 0 || ks > 0) ? 1u : 0u);
+        tc::mma_commit(&M.pv_done[t & 1]);
+        last_bar = &M.pv_done[t & 1];
+        last_par = (t >> 1) & 1;
+    };
+    for (int t = 0; t < c.n_tiles && ok; ++t) {
+        const int vb = t & 1;
+        if (!tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) ||
+            (t >= 2 && !tc::mbar_wait(&M.s_free[vb], ((t - 2) >> 1) & 1))) {
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
+        const uint32_t va = tc::smem_u32(c.Vs + vb * kVBytes);
+        for (int ks = 0; ks < kDim / 16; ++ks)
+            tc::mma_f16(c.tmem + 32 * vb, tc::sdesc(qa + ks * 256, 128, 8192), tc::sdesc(va + ks * 256, 128, 8192),
+                        kIdescQK, ks > 0 ? 1u : 0u);
+        tc::mma_commit(&M.s_full[vb]);
+        last_bar = &M.s_full[vb];
+        last_par = (t >> 1) & 1;
+        if (t >= 1) issue_pv(t - 1);
+    }
+    if (ok && c.n_tiles > 0) issue_pv(c.n_tiles - 1);
+    if (!ok) raise_flag(c.flags, kFlagTimeout);
+    // every issued MMA must have finished before the tensor memory is released
+    if (last_bar) tc::mbar_wait(last_bar, last_par);
+}
+
+// ---- softmax rows (warps 0-3, thread = tensor-memory lane = query row) ----------------
+__device__ __forceinline__ void softmax_rows(const Ctx &c)
+{
+    AttnMisc &M = *c.M;
+    const UnitDev &U = *c.U;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot_layer = tid >> 4, head = tid & 15;
+    const bool active = slot_layer < U.n_layers;
+    const uint32_t lane_base = (uint32_t)(32 * warp);
+    float m_used = -INFINITY, l_sum = 0.0f;
+    bool ok = true;
+    for (int t = 0; t < c.n_tiles; ++t) {
+        const int vb = t & 1;
+        bool w_ok = tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) && tc::mbar_wait(&M.s_full[vb], (t >> 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
+        float s[kTile];
+        tc::tmem_ld32(tc::taddr(c.tmem, lane_base, 32 * vb), s);
+        tc::fence_before_sync();
+        tc::mbar_arrive(&M.s_free[vb]);
+        float mt = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int c = 128 * warp + 8 * nt + 2 * t;
-            *reinterpret_cast<float2 *>(out + g * kDim + c) = make_float2(o[nt][0] * inv0, o[nt][1] * inv0);
-            *reinterpret_cast<float2 *>(out + (g + 8) * kDim + c) = make_float2(o[nt][2] * inv1, o[nt][3] * inv1);
+        for (int j = 0; j < kTile; ++j) {
+            s[j] = M.mvalid[vb][j] ? s[j] * M.mscale[vb][j] : -INFINITY;
+            mt = fmaxf(mt, s[j]);
         }
-        if (E.lse && warp == 0 && t == 0) {
-            E.lse[(int64_t)b * kHeads + g] = l_run[0] > 0.0f ? m_run[0] + logf(l_run[0]) : -INFINITY;
-            E.lse[(int64_t)b * kHeads + g + 8] = l_run[1] > 0.0f ? m_run[1] + logf(l_run[1]) : -INFINITY;
+        // PV(t-1) must be done: O is then current and the P buffer free
+        w_ok = (t == 0) || tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+            ok = false;
+            break;
         }
-    } else {
-        float *part = plan.partials + (((int64_t)ei * plan.batch + b) * plan.n_chunks + chunk) * kPartFloats;
+        tc::fence_after_sync();
+        const float m_new = active ? fmaxf(m_used, mt) : m_used;
+        // lazy rescale, warp-uniform: every lane of the warp joins the tensor-memory traffic
+        if (__any_sync(0xFFFFFFFFu, active && m_new > m_used + kRescaleGap)) {
+            const float alpha = (active && m_used != -INFINITY) ? __expf(m_used - m_new) : (active ? 0.0f : 1.0f);
+            if (t >= 1) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    float o[32];
+                    tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            const int c = 128 * warp + 8 * nt + 2 * t;
-            *reinterpret_cast<float2 *>(part + g * kDim + c) = make_float2(o[nt][0], o[nt][1]);
-            *reinterpret_cast<float2 *>(part + (g + 8) * kDim + c) = make_float2(o[nt][2], o[nt][3]);
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+                }
+            }
+            if (active) {
+                l_sum *= alpha;
+                m_used = m_new;
+            }
         }
-        if (warp == 0 && t == 0) {
-            part[kHeads * kDim + g] = m_run[0];
-            part[kHeads * kDim + g + 8] = m_run[1];
-            part[kHeads * kDim + kHeads + g] = l_run[0];
-            part[kHeads * kDim + kHeads + g + 8] = l_run[1];
+        uint32_t ph[kTile / 2];
+#pragma unroll
+        for (int j = 0; j < kTile; j += 2) {
+            float p0 = 0.0f, p1 = 0.0f;
+            if (active) {
+                p0 = (s[j] == -INFINITY) ? 0.0f : __expf(s[j] - m_used);
+                p1 = (s[j + 1] == -INFINITY) ? 0.0f : __expf(s[j + 1] - m_used);
+                l_sum += p0 + p1;
+            }
+            // window rows hold raw E4M3 codes: their per-token scale joins the weight
+            ph[j >> 1] = pack_h2(__floats2half2_rn(p0 * M.mscale[vb][j], p1 * M.mscale[vb][j + 1]));
         }
+        // P row into its K-major core-matrix layout: 4 groups of 8 keys, 512 B per 8-row group
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            *reinterpret_cast<uint4 *>(c.Ps + (tid >> 3) * 512 + g * 128 + (tid & 7) * 16) =
+                make_uint4(ph[4 * g], ph[4 * g + 1], ph[4 * g + 2], ph[4 * g + 3]);
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&M.p_full);
+    }
+    if (ok && c.n_tiles > 0) {
+        const int last = c.n_tiles - 1;
+        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait(&M.pv_done[last & 1], (last >> 1) & 1));
+    }
+    if (!ok && (tid & 31) == 0) raise_flag(c.flags, kFlagTimeout);
+    tc::fence_after_sync();
+    // this chunk's partial for its channel half: (m, l, unnormalised O)
+    const bool have = ok && c.n_tiles > 0;
+    float *orow = nullptr;
+    if (active) {
+        const int e = U.entry[slot_layer];
+        const EntryDev &E = c.P->entries[e];
+        const int part = U.is_window ? E.part_win : c.chunk;
+        float *rec = c.P->partials + (((int64_t)e * c.P->batch + c.b) * c.P->max_parts + part) * kPartFloats;
+        const bool any = have && l_sum > 0.0f;
+        rec[c.half * 16 + head] = any ? m_used : -INFINITY;
+        rec[32 + c.half * 16 + head] = any ? l_sum : 0.0f;
+        orow = rec + 64 + head * kDim + c.half * 256;
+    }
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+        float o[32];
+        if (have) tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+        if (active) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(orow + c0 + i) =
+                    have ? make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    tc::fence_before_sync();
+}
+
+// ---- merge: the last CTA to finish a (layer, sequence, half) combines its partials ----
+__device__ __forceinline__ void merge_if_last(const Ctx &c)
+{
+    AttnMisc &M = *c.M;
+    const UnitDev &U = *c.U;
+    const AttnParams &P = *c.P;
+    const int tid = threadIdx.x;
+    tc::named_sync(2, 128);  // every row of this CTA has written its partial
+    if (tid < U.n_layers) {
+        const int e = U.entry[tid];
+        __threadfence();
+        const uint32_t old = atomicAdd(P.counters + ((int64_t)e * P.batch + c.b) * 2 + c.half, 1u);
+        M.last[tid] = (old + 1 == (uint32_t)P.entries[e].n_parts) ? 1 : 0;
+    }
+    tc::named_sync(2, 128);
+    for (int j = 0; j < U.n_layers; ++j) {
+        if (!M.last[j]) continue;
+        __threadfence();
+        const int e = U.entry[j];
+        const EntryDev &E = P.entries[e];
+        const float *recs = P.partials + ((int64_t)e * P.batch + c.b) * P.max_parts * kPartFloats;
+        const int h = tid >> 3, c0 = c.half * 256 + (tid & 7) * 32;  // head, 32 output channels
+        float mx = -INFINITY;
+        for (int p = 0; p < E.n_parts; ++p) {
+            const float *rp = recs + (int64_t)p * kPartFloats;
+            if (__ldcg(rp + 32 + c.half * 16 + h) > 0.0f) mx = fmaxf(mx, __ldcg(rp + c.half * 16 + h));
+        }
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        float ls = 0.0f;
+        for (int p = 0; p < E.n_parts; ++p) {
+            const float *rp = recs + (int64_t)p * kPartFloats;
+            const float lp = __ldcg(rp + 32 + c.half * 16 + h);
+            if (!(lp > 0.0f)) continue;
+            const float wp = __expf(__ldcg(rp + c.half * 16 + h) - mx);
+            ls += wp * lp;
+            const float4 *op = reinterpret_cast<const float4 *>(rp + 64 + h * kDim + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldcg(op + i);
+                acc[4 * i] += wp * v.x;
+                acc[4 * i + 1] += wp * v.y;
+                acc[4 * i + 2] += wp * v.z;
+                acc[4 * i + 3] += wp * v.w;
+            }
+        }
+        const float inv = ls > 0.0f ? 1.0f / ls : 0.0f;
+        float4 *out = reinterpret_cast<float4 *>(E.out + ((int64_t)c.b * kHeads + h) * kDim + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            out[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+        if (c.half == 0 && E.lse && (tid & 7) == 0)
+            E.lse[(int64_t)c.b * kHeads + h] = ls > 0.0f ? mx + logf(ls) : -INFINITY;
     }
 }
 
-// Log-sum-exp merge of the chunk partials of one (entry, sequence).
-__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ AttnBatch ab, AttnPlan plan)
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams P, int *flags)
 {
-    const int ei = blockIdx.x, b = blockIdx.y;
-    const AttnEntry &E = ab.e[ei];
-    const float *part = plan.partials + ((int64_t)ei * plan.batch + b) * plan.n_chunks * kPartFloats;
-    __shared__ float wsm[64][kHeads];
-    __shared__ float inv_l[kHeads];
-    const int tid = threadIdx.x;
-    if (tid < kHeads) {
-        float M = -INFINITY;
-        for (int c = 0; c < plan.n_chunks; ++c) M = fmaxf(M, part[c * kPartFloats + kHeads * kDim + tid]);
-        float l = 0.0f;
-        for (int c = 0; c < plan.n_chunks; ++c) {
-            const float mc = part[c * kPartFloats + kHeads * kDim + tid];
-            const float wc = (mc == -INFINITY) ? 0.0f : __expf(mc - M);
-            wsm[c][tid] = wc;
-            l += wc * part[c * kPartFloats + kHeads * kDim + kHeads + tid];
-        }
-        inv_l[tid] = l > 0.0f ? 1.0f / l : 0.0f;
-        if (E.lse) E.lse[(int64_t)b * kHeads + tid] = l > 0.0f ? M + logf(l) : -INFINITY;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx c;
+    c.P = &P;
+    c.M = reinterpret_cast<AttnMisc *>(smem + kOffMisc);
+    c.Qs = smem;
+    c.Vs = smem + kOffV;
+    c.Ps = smem + kOffP;
+    c.Raw = smem + kOffRaw;
+    c.flags = flags;
+    c.b = blockIdx.y;
+    int u = 0;
+    while (u + 1 < P.n_units && (int)blockIdx.x >= P.units[u + 1].cta_begin) ++u;
+    c.U = &P.units[u];
+    const int local = (int)blockIdx.x - c.U->cta_begin;
+    c.chunk = local >> 1;
+    c.half = local & 1;
+    c.L = max(0, __ldg(P.seq_lens + c.b));
+    c.W = P.window;
+    c.fp8 = c.U->is_window != 0;
+    if (c.fp8) {
+        c.row0 = 0;
+        c.n_rows = c.W;
+    } else {
+        c.row0 = c.chunk * P.rows_per_chunk;
+        c.n_rows = max(0, min(P.rows_per_chunk, P.topk - c.row0));
     }
+    c.n_tiles = (c.n_rows + kTile - 1) / kTile;
+    AttnMisc &M = *c.M;
+
+    if (tid == 0) {
+        tc::mbar_init(&M.q_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&M.full_v[i], 128);
+            tc::mbar_init(&M.s_full[i], 1);
+            tc::mbar_init(&M.s_free[i], 128);
+            tc::mbar_init(&M.pv_done[i], 1);
+        }
+        tc::mbar_init(&M.p_full, 128);
+        tc::mbar_init_fence();
+    }
+    if (warp == 8) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
+    tc::fence_before_sync();
     __syncthreads();
-    float *out = E.out + (int64_t)b * kHeads * kDim;
-    for (int i = tid; i < kHeads * kDim / 4; i += blockDim.x) {
-        const int h = (4 * i) / kDim;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < plan.n_chunks; ++c) {
-            const float wc = wsm[c][h];
-            if (wc == 0.0f) continue;
-            const float4 v = reinterpret_cast<const float4 *>(part + c * kPartFloats)[i];
-            acc.x += wc * v.x;
-            acc.y += wc * v.y;
-            acc.z += wc * v.z;
-            acc.w += wc * v.w;
-        }
-        const float il = inv_l[h];
-        reinterpret_cast<float4 *>(out)[i] = make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+    tc::fence_after_sync();
+    c.tmem = M.tmem_slot;
+
+    if (warp >= 4 && warp < 8) {
+        produce(c);
+    } else if (warp == 8) {
+        if (lane == 0) issue_mmas(c);
+        __syncwarp();
+    } else {
+        softmax_rows(c);
     }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 8) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(c.tmem, kTmemCols);
+    }
+    if (warp < 4) merge_if_last(c);
 }
 
 }  // namespace
 
-int attn_chunks(int n_entries, int batch, int topk, int window)
+// ---- host planning ---------------------------------------------------------------------
+namespace {
+
+struct UnitPlan {
+    std::vector<std::vector<int>> row_units;  // entry ids per row unit (<= 8 each)
+    std::vector<int> window_units;            // entry id per window unit
+};
+
+// Row units: entries that read the same index list over the same cache, in
+// groups of at most 8; window units: one per entry with a window.
+UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
 {
-    const int rows = topk + window;
-    const int tiles = (rows + kTileRows - 1) / kTileRows;
-    const int items = n_entries * batch;
-    // aim for about two waves of 148 SMs, at least 4 tiles per chunk, at most 64 chunks
-    int chunks = (2 * 148 + items - 1) / items;
-    const int max_by_tiles = tiles / 4 > 0 ? tiles / 4 : 1;
-    if (chunks > max_by_tiles) chunks = max_by_tiles;
-    if (chunks > 64) chunks = 64;
-    if (chunks < 1) chunks = 1;
-    return chunks;
+    UnitPlan up;
+    std::vector<std::pair<const void *, const void *>> keys;
+    std::vector<std::vector<int>> groups;
+    for (int e = 0; e < n_entries; ++e) {
+        const AttnEntry &en = entries[e];
+        if (en.has_kv && en.idx) {
+            const std::pair<const void *, const void *> k(en.idx, en.kv.data);
+            size_t g = 0;
+            while (g < keys.size() && keys[g] != k) ++g;
+            if (g == keys.size()) {
+                keys.push_back(k);
+                groups.emplace_back();
+            }
+            groups[g].push_back(e);
+        }
+        if (en.has_swa && window > 0) up.window_units.push_back(e);
+    }
+    for (auto &g : groups)
+        for (size_t i = 0; i < g.size(); i += 8)
+            up.row_units.emplace_back(g.begin() + i, g.begin() + std::min(g.size(), i + 8));
+    return up;
 }
 
-size_t attn_partial_bytes(int n_entries, int batch, int n_chunks)
+// Rows per chunk of a row unit: 256 (8 tiles), doubled while the grid would
+// exceed 8 waves of one CTA per SM (large batches need no split).
+int rows_per_chunk(int n_row_units, int n_window_units, int batch, int topk)
 {
-    if (n_chunks <= 1) return 0;
-    return (size_t)n_entries * batch * n_chunks * kPartFloats * sizeof(float);
+    int rpc = 256;
+    auto ctas = [&](int r) {
+        return (int64_t)batch * 2 * ((int64_t)n_row_units * ((topk + r - 1) / r) + n_window_units);
+    };
+    while (rpc < topk && ctas(rpc) > 8 * 148) rpc *= 2;
+    return rpc;
+}
+
+struct WsLayout {
+    size_t counters = 0, q16 = 0, partials = 0, total = 0;
+    int rpc = 256, chunks = 0, max_parts = 1;
+};
+
+WsLayout ws_layout(const UnitPlan &up, int n_entries, int batch, int topk, int window)
+{
+    WsLayout w;
+    w.rpc = rows_per_chunk((int)up.row_units.size(), (int)up.window_units.size(), batch, topk);
+    w.chunks = (topk > 0 && !up.row_units.empty()) ? (topk + w.rpc - 1) / w.rpc : 0;
+    w.max_parts = std::max(1, w.chunks + (window > 0 ? 1 : 0));
+    auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    w.counters = r256((size_t)n_entries * batch * 2 * 4);
+    w.q16 = r256((size_t)n_entries * batch * kQRowsBytes);
+    w.partials = r256((size_t)n_entries * batch * w.max_parts * kPartFloats * 4);
+    w.total = w.counters + w.q16 + w.partials;
+    return w;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window)
+{
+    const UnitPlan up = group_units(entries, n_entries, window);
+    return ws_layout(up, n_entries, batch, topk, window).total;
 }
 
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream, cudaEvent_t mid_event)
 {
-    const size_t smem = sizeof(AttnSmem);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (plan.n_entries <= 0 || plan.n_entries > kMaxAttnEntries) return cudaErrorInvalidValue;
+    const UnitPlan up = group_units(plan.entries, plan.n_entries, plan.window);
+    const WsLayout wl = ws_layout(up, plan.n_entries, plan.batch, plan.topk, plan.window);
+    if (plan.workspace_bytes < wl.total || (int)(up.row_units.size() + up.window_units.size()) > kMaxUnits)
+        return cudaErrorInvalidValue;
+    uint8_t *ws = static_cast<uint8_t *>(plan.workspace);
+
+    std::vector<uint8_t> pbuf(sizeof(AttnParams), 0);
+    AttnParams &p = *reinterpret_cast<AttnParams *>(pbuf.data());
+    p.batch = plan.batch;
+    p.topk = plan.topk;
+    p.window = plan.window;
+    p.rows_per_chunk = wl.rpc;
+    p.max_parts = wl.max_parts;
+    p.seq_lens = plan.seq_lens;
+    p.counters = reinterpret_cast<uint32_t *>(ws);
+    p.q16 = ws + wl.counters;
+    p.partials = reinterpret_cast<float *>(ws + wl.counters + wl.q16);
+    for (int e = 0; e < plan.n_entries; ++e) {
+        p.entries[e].out = plan.entries[e].out;
+        p.entries[e].lse = plan.entries[e].lse;
+        p.entries[e].n_parts = 0;
+        p.entries[e].part_win = -1;
     }
-    for (int first = 0; first < plan.n_entries; first += kMaxAttnEntries) {
-        AttnBatch ab;
-        const int n = (plan.n_entries - first < kMaxAttnEntries) ? plan.n_entries - first : kMaxAttnEntries;
-        for (int i = 0; i < n; ++i) ab.e[i] = plan.entries[first + i];
-        AttnPlan p = plan;
-        p.n_entries = n;
-        if (plan.partials)
-            p.partials = plan.partials + (size_t)first * plan.batch * plan.n_chunks * kPartFloats;
-        dim3 grid((unsigned)plan.n_chunks, (unsigned)plan.batch, (unsigned)n);
-        attn_kernel<<<grid, kAttnThreads, smem, stream>>>(ab, p, flags);
+    int cta = 0, nu = 0;
+    for (const auto &g : up.row_units) {
+        UnitDev &U = p.units[nu++];
+        U.cache = plan.entries[g[0]].kv;
+        U.idx = plan.entries[g[0]].idx;
+        U.is_window = 0;
+        U.n_layers = (int)g.size();
+        for (size_t j = 0; j < g.size(); ++j) {
+            U.entry[j] = g[j];
+            p.entries[g[j]].n_parts = wl.chunks;  // row chunk c is part c
+        }
+        U.cta_begin = cta;
+        cta += 2 * wl.chunks;
+    }
+    for (int e : up.window_units) {
+        UnitDev &U = p.units[nu++];
+        U.cache = plan.entries[e].swa;
+        U.idx = nullptr;
+        U.is_window = 1;
+        U.n_layers = 1;
+        U.entry[0] = e;
+        U.cta_begin = cta;
+        cta += 2;
+        p.entries[e].part_win = p.entries[e].n_parts;
+        p.entries[e].n_parts += 1;
+    }
+    p.n_units = nu;
+
+    cudaError_t err = cudaSuccess;
+    // a layer with neither selected rows nor a window attends over nothing
+    for (int e = 0; e < plan.n_entries && err == cudaSuccess; ++e)
+        if (p.entries[e].n_parts == 0)
+            err = cudaMemsetAsync(plan.entries[e].out, 0, (size_t)plan.batch * kHeads * kDim * 4, stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(ws, 0, wl.counters, stream);
+    if (err == cudaSuccess && cta > 0) {
+        QList qs;
+        std::memset(&qs, 0, sizeof(qs));
+        for (int e = 0; e < plan.n_entries; ++e) qs.q[e] = plan.entries[e].q;
+        pack_q_kernel<<<dim3((unsigned)plan.n_entries, (unsigned)plan.batch), 256, 0, stream>>>(
+            qs, const_cast<uint8_t *>(p.q16), plan.batch);
         count_launches(1);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if (mid_event && first + n >= plan.n_entries) {
-            e = record_event(mid_event, stream);
-            if (e != cudaSuccess) return e;
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess && cta > 0) {
+        const size_t smem = kOffMisc + sizeof(AttnMisc);
+        int dev = 0;
+        err = cudaGetDevice(&dev);
+        static bool attr_set[64] = {};
+        if (err == cudaSuccess && (dev < 0 || dev >= 64 || !attr_set[dev])) {
+            err = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (err == cudaSuccess && dev >= 0 && dev < 64) attr_set[dev] = true;
         }
-        if (plan.n_chunks > 1) {
-            merge_kernel<<<dim3((unsigned)n, (unsigned)plan.batch), 256, 0, stream>>>(ab, p);
+        if (err == cudaSuccess) {
+            attn_tc_kernel<<<dim3((unsigned)cta, (unsigned)plan.batch), kThreads, smem, stream>>>(p, flags);
             count_launches(1);
-            e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
+            err = cudaGetLastError();
         }
     }
-    return cudaSuccess;
+    if (err == cudaSuccess && mid_event) err = record_event(mid_event, stream);
+    return err;
 }
 
 }  // namespace csa2

@@ -283,7 +283,13 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window)
 {
     if (batch <= 0 || topk < 0 || swa_window < 0) return 0;
-    return round256(attn_partial_bytes(1, batch, attn_chunks(1, batch, topk, swa_window)));
+    static const int32_t any_index = 0;  // stands for "an index list is given"
+    AttnEntry en;
+    memset(&en, 0, sizeof(en));
+    en.has_kv = topk > 0 ? 1 : 0;
+    en.idx = topk > 0 ? &any_index : nullptr;
+    en.has_swa = swa_window > 0 ? 1 : 0;
+    return attn_workspace_bytes(&en, 1, batch, topk, swa_window);
 }
 
 csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const float *q, int32_t batch,
@@ -309,9 +315,6 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
         if (st) return st;
     }
     const int eff_topk = idx ? topk : 0;
-    const int n_chunks = attn_chunks(1, batch, eff_topk, swa_window);
-    st = check_ws(workspace, workspace_bytes, attn_partial_bytes(1, batch, n_chunks));
-    if (st) return st;
     int *fp = flags_ptr();
     if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
     AttnEntry en;
@@ -324,6 +327,8 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     en.lse = lse;
     en.has_kv = idx ? 1 : 0;
     en.has_swa = swa_window > 0 ? 1 : 0;
+    st = check_ws(workspace, workspace_bytes, attn_workspace_bytes(&en, 1, batch, eff_topk, swa_window));
+    if (st) return st;
     AttnPlan plan;
     plan.entries = &en;
     plan.n_entries = 1;
@@ -331,8 +336,8 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     plan.topk = eff_topk;
     plan.window = swa_window;
     plan.seq_lens = seq_lens;
-    plan.n_chunks = n_chunks;
-    plan.partials = n_chunks > 1 ? static_cast<float *>(workspace) : nullptr;
+    plan.workspace = workspace;
+    plan.workspace_bytes = workspace_bytes;
     cudaError_t e = launch_attention(plan, fp, static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
 }
@@ -341,12 +346,33 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
 
 namespace {
 
+// Attention entries of a step, one per layer (sources already validated).
+std::vector<AttnEntry> step_entries(const csa2_layer_desc *layers, int n_layers, int swa_window)
+{
+    std::vector<AttnEntry> entries(n_layers);
+    for (int l = 0; l < n_layers; ++l) {
+        const csa2_layer_desc &d = layers[l];
+        AttnEntry &en = entries[l];
+        memset(&en, 0, sizeof(en));
+        en.q = d.q;
+        en.out = d.out;
+        en.lse = d.lse;
+        en.has_swa = swa_window > 0 ? 1 : 0;
+        if (swa_window > 0) en.swa = view_of(*d.swa);
+        if (d.mode != CSA2_MODE_SWA_ONLY) {
+            en.kv = view_of(*layers[d.kv_src].kv);
+            en.has_kv = 1;
+            en.idx = (d.mode == CSA2_MODE_REUSE) ? layers[d.idx_src].idx_out : d.idx_out;
+        }
+    }
+    return entries;
+}
+
 struct StepLayout {
     int n_idx = 0;              // indexing layers (FULL + REINDEX)
     std::vector<int> row_block; // per layer: row block id or -1
     int n_level0 = 0, n_level1 = 0;
     int64_t cand_cap = 1;
-    int n_chunks = 1;
     size_t select_off = 0, select_size = 0, part_off = 0, part_size = 0, total = 0;
 };
 
@@ -422,11 +448,14 @@ csa2_status plan_step(const csa2_layer_desc *layers, int32_t n_layers, int32_t b
         }
     }
     P.cand_cap = max_seq_len > pool_len ? max_seq_len : pool_len;
-    P.n_chunks = attn_chunks(n_layers, batch, topk, swa_window);
     P.select_off = 0;
     P.select_size = P.n_idx ? round256(select_bytes(P.n_idx * batch, P.cand_cap, max_seq_len)) : 0;
     P.part_off = P.select_size;
-    P.part_size = round256(attn_partial_bytes(n_layers, batch, P.n_chunks));
+    if (n_layers > kMaxAttnEntries) return fail(CSA2_ERR_UNSUPPORTED, "at most %d layers per step", kMaxAttnEntries);
+    {
+        const std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
+        P.part_size = round256(attn_workspace_bytes(entries.data(), n_layers, batch, topk, swa_window));
+    }
     P.total = P.part_off + P.part_size;
     return CSA2_OK;
 }
@@ -561,22 +590,7 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "event");
 
     // attention of every layer
-    std::vector<AttnEntry> entries(n_layers);
-    for (int l = 0; l < n_layers; ++l) {
-        const csa2_layer_desc &d = layers[l];
-        AttnEntry &en = entries[l];
-        memset(&en, 0, sizeof(en));
-        en.q = d.q;
-        en.out = d.out;
-        en.lse = d.lse;
-        en.has_swa = swa_window > 0 ? 1 : 0;
-        if (swa_window > 0) en.swa = view_of(*d.swa);
-        if (d.mode != CSA2_MODE_SWA_ONLY) {
-            en.kv = view_of(*layers[d.kv_src].kv);
-            en.has_kv = 1;
-            en.idx = (d.mode == CSA2_MODE_REUSE) ? layers[d.idx_src].idx_out : d.idx_out;
-        }
-    }
+    std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
     AttnPlan ap;
     ap.entries = entries.data();
     ap.n_entries = n_layers;
@@ -584,8 +598,8 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     ap.topk = topk;
     ap.window = swa_window;
     ap.seq_lens = seq_lens;
-    ap.n_chunks = P.n_chunks;
-    ap.partials = P.n_chunks > 1 ? reinterpret_cast<float *>(ws + P.part_off) : nullptr;
+    ap.workspace = ws + P.part_off;
+    ap.workspace_bytes = P.part_size;
     cudaEvent_t mid = (g_n_events > 4) ? static_cast<cudaEvent_t>(g_events[4]) : nullptr;
     e = launch_attention(ap, fp, s, mid);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");

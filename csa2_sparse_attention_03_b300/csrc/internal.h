@@ -107,15 +107,16 @@ struct AttnPlan {
     const AttnEntry *entries;
     int n_entries;
     int batch;
-    int topk;
+    int topk;              // rows per index list (0 when no entry has one)
     int window;
     const int32_t *seq_lens;
-    int n_chunks;          // chunks per (entry, sequence); 1 = no merge pass
-    float *partials;       // [n_entries][B][n_chunks][16][512 + 2]
+    void *workspace;       // attn_workspace_bytes() bytes, 256-B aligned
+    size_t workspace_bytes;
 };
 
-int attn_chunks(int n_entries, int batch, int topk, int window);
-size_t attn_partial_bytes(int n_entries, int batch, int n_chunks);
+// Workspace of one launch_attention call: per-(layer, sequence, half) merge
+// counters (zeroed by the launch), fp16 query rows, and split partials.
+size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window);
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
                              cudaEvent_t mid_event);
 
