@@ -17,17 +17,20 @@
 // the last CTA to finish a (layer, sequence, half) merges its partials.
 //
 // One CTA, 9 warps:
-//   warps 4-7  producers: cp.async gather of the raw rows of a 32-row tile,
-//              exact dequantisation to fp16 (E2M1 x E4M3 and E4M3 are exact
-//              in fp16) into the tile's core-matrix layout;
-//   warp 8     tensor-memory allocation and tcgen05.mma issue:
-//              S[b] = Q V^T (M 128, N 32, K 512) into tensor memory, then
-//              O += P V (M 128, N 256, K 32) with O resident in tensor memory;
+//   warps 4-7  producers: each thread owns one row of a 32-row tile and a
+//              quarter of its bytes; it loads the next tile's bytes into
+//              registers while it dequantises the current one (E2M1 x E4M3
+//              and E4M3 are exact in fp16) into the core-matrix layout;
+//   warp 8     tensor-memory allocation and tcgen05.mma issue, descriptors
+//              precomputed: S[b] = Q V^T (M 128, N 32, K 512) into tensor
+//              memory, then O += P V (M 128, N 256, K 32), O resident in
+//              tensor memory;
 //   warps 0-3  one thread per query row: S from tensor memory, fp32 online
 //              softmax with lazy rescaling of O (only when the running max
 //              grows by more than e^8), P to shared memory as fp16.
-// V and S are double-buffered, P single; every hand-off is an mbarrier with
-// a bounded wait (a wait that gives up raises the timeout flag and the CTA
+// V, S and P are double-buffered, so the softmax of tile t+1 does not wait
+// for PV(t) unless O must be rescaled.  Every hand-off is an mbarrier with a
+// bounded wait (a wait that gives up raises the timeout flag and the CTA
 // drains and exits).
 #include <algorithm>
 #include <cstring>
@@ -41,20 +44,22 @@ namespace csa2 {
 namespace {
 
 constexpr int kTile = 32;                  // rows per tile
-constexpr int kThreads = 288;              // 9 warps
+constexpr int kProducers = 256;            // producer threads (warps 4-11)
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 416;              // 13 warps
+constexpr int kMaxChunkRows = 2048;        // rows per chunk of a row unit (indices staged in smem)
 constexpr int kQRowsBytes = kHeads * kDim * 2;  // 16 KB: one layer's 16 query rows in fp16
 constexpr int kQBytes = 8 * kQRowsBytes;   // 131,072: 128 query rows
 constexpr int kVBytes = kTile * kDim * 2;  // 32,768 per buffer
-constexpr int kPBytes = 128 * kTile * 2;   // 8,192
-constexpr int kRawHalf = 9216;             // one tile of 32 FP4 rows (288 B each)
-constexpr int kRawBytes = 2 * kRawHalf;    // two FP4 tiles, or one tile of 32 FP8 rows (16 KB)
+constexpr int kPBytes = 128 * kTile * 2;   // 8,192 per buffer
 constexpr int kOffV = kQBytes;
 constexpr int kOffP = kOffV + 2 * kVBytes;
-constexpr int kOffRaw = kOffP + kPBytes;
-constexpr int kOffMisc = kOffRaw + kRawBytes;
+constexpr int kOffIdx = kOffP + 2 * kPBytes;
+constexpr int kOffMisc = kOffIdx + kMaxChunkRows * 4;
 constexpr int kPartFloats = 64 + kHeads * kDim;  // m[2][16], l[2][16], O[16][512]
 constexpr int kMaxUnits = 2 * kMaxAttnEntries;
 constexpr float kRescaleGap = 8.0f;        // lazy O rescale threshold (natural log)
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;        // S[0] cols 0-31, S[1] cols 32-63, O cols 256-511
 constexpr uint32_t kColO = 256;
 // Instruction descriptors: QK^T (both operands K-major), PV (B = V read MN-major).
@@ -62,12 +67,9 @@ constexpr uint32_t kIdescQK = tc::idesc_f16(128, kTile, false, false);
 constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, false, true);
 
 struct AttnMisc {
-    const uint8_t *rowptr[2][kTile];  // per raw buffer
-    float rscale[2][kTile];
-    int32_t rvalid[2][kTile];
-    float mscale[2][kTile];           // per V buffer (read by the softmax warps)
-    int32_t mvalid[2][kTile];
-    uint64_t q_bar, full_v[2], s_full[2], s_free[2], p_full, pv_done[2];
+    float mscale[2][kTile];   // per V buffer: per-row scale (FP8 window rows)
+    uint32_t vmask[2];        // per V buffer: valid rows
+    uint64_t q_bar, full_v[2], s_full[2], s_free[2], p_full[2], pv_done[2];
     uint32_t tmem_slot;
     int32_t last[8];
 };
@@ -107,7 +109,7 @@ struct QList {
 // Byte offset of fp16 element (row r, channel c) of an operand with 512-channel
 // rows in the no-swizzle core-matrix layout: 8-row groups 8,192 B apart,
 // 8-channel groups 128 B apart.
-__device__ __forceinline__ uint32_t cm_off512(uint32_t r, uint32_t c)
+__host__ __device__ __forceinline__ uint32_t cm_off512(uint32_t r, uint32_t c)
 {
     return (r >> 3) * 8192u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
 }
@@ -130,15 +132,15 @@ __global__ void __launch_bounds__(256) pack_q_kernel(const __grid_constant__ QLi
     }
 }
 
-// OR-reduction of a predicate over the 128 threads of named barrier `id`
+// OR-reduction of a predicate over the `count` threads of named barrier `id`
 // (also a barrier); every participant gets the same result.
-__device__ __forceinline__ bool bar_any(uint32_t id, bool p)
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool p)
 {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, %2, 128, a;\n selp.u32 %0, 1, 0, o;\n}\n"
+        "{\n .reg .pred a, o;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred o, %2, %3, a;\n selp.u32 %0, 1, 0, o;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)p), "r"(id)
+        : "r"((uint32_t)p), "r"(id), "r"(count)
         : "memory");
     return r != 0;
 }
@@ -148,146 +150,148 @@ struct Ctx {
     const AttnParams *P;
     const UnitDev *U;
     AttnMisc *M;
-    uint8_t *Qs, *Vs, *Ps, *Raw;
+    uint8_t *Qs, *Vs, *Ps;
+    int32_t *sidx;      // the chunk's row positions (row units)
     int *flags;
     uint32_t tmem;
     int b, L, W, row0, n_rows, n_tiles, chunk, half;
     bool fp8;
 };
 
-// ---- producers (warps 4-7): gather + dequantise 32-row tiles -------------------------
+// ---- producers (warps 4-11): gather + dequantise 32-row tiles ------------------------
+// Thread ptid owns row j = ptid % 32 of every tile and the eighth w = ptid / 32
+// of its 16-byte granules (FP4 rows: 16 granules of 32 channels, g = w, w + 8;
+// FP8 rows: 32 granules of 16 channels, g = w + 8i).
+constexpr int kPW = kProducers / 32;  // producer warps
+template <bool FP8>
+struct RowRegs {
+    uint4 g[FP8 ? 32 / kPW : 16 / kPW];
+    uint32_t s[FP8 ? 1 : 16 / kPW];  // FP4: two E4M3 scales per granule; FP8: the row's fp32 scale bits
+    bool valid;
+};
+
+template <bool FP8>
+__device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, RowRegs<FP8> &r)
+{
+    const UnitDev &U = *c.U;
+    const int v = t * kTile + j;  // row within this chunk
+    const uint8_t *ptr = nullptr;
+    uint32_t sc = 0u;
+    if (v < c.n_rows) {
+        if (!FP8) {
+            const int32_t pos = c.sidx[v];
+            if (pos >= 0) {
+                const int64_t slot = pos < c.L ? slot_of(U.cache, c.b, pos) : -1;
+                if (slot < 0) {
+                    if (w == 0) raise_flag(c.flags, kFlagBounds);
+                } else {
+                    ptr = U.cache.data + slot * kKvRow;
+                }
+            }
+        } else {
+            const int64_t pos = (int64_t)c.L - c.W + c.row0 + v;
+            if (pos >= 0) {
+                const int64_t slot = slot_of(U.cache, c.b, pos);
+                if (slot < 0) {
+                    if (w == 0) raise_flag(c.flags, kFlagBounds);
+                } else {
+                    ptr = U.cache.data + slot * kDim;
+                    sc = __ldg(reinterpret_cast<const uint32_t *>(U.cache.data + U.cache.n_slots * kDim) + slot);
+                }
+            }
+        }
+    }
+    r.valid = ptr != nullptr;
+    if (FP8) {
+        r.s[0] = sc;
+#pragma unroll
+        for (int i = 0; i < 32 / kPW; ++i)
+            r.g[i] = ptr ? __ldg(reinterpret_cast<const uint4 *>(ptr + 16 * (w + kPW * i))) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16 / kPW; ++i) {
+            r.g[i] = ptr ? __ldg(reinterpret_cast<const uint4 *>(ptr + 16 * (w + kPW * i))) : make_uint4(0u, 0u, 0u, 0u);
+            r.s[i] = ptr ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(ptr + kKvCodes + 2 * (w + kPW * i)))
+                         : 0u;
+        }
+    }
+}
+
+template <bool FP8>
+__device__ __forceinline__ void store_row(uint8_t *V, int j, int w, const RowRegs<FP8> &r)
+{
+    if (FP8) {
+#pragma unroll
+        for (int i = 0; i < 32 / kPW; ++i) {
+            const int g = w + kPW * i;  // channels 16g..16g+15
+            const uint4 cw = r.g[i];
+            *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g)) =
+                make_uint4(pack_h2(e4m3x2_half2(cw.x & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.x >> 16)),
+                           pack_h2(e4m3x2_half2(cw.y & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.y >> 16)));
+            *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g + 8)) =
+                make_uint4(pack_h2(e4m3x2_half2(cw.z & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.z >> 16)),
+                           pack_h2(e4m3x2_half2(cw.w & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.w >> 16)));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16 / kPW; ++i) {
+            const int g = w + kPW * i;  // channels 32g..32g+31, scales 2g (first 16) and 2g+1
+            const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(r.s[i] & 0xFFu)));
+            const __half2 s1 = __half2half2(__float2half_rn(e4m3_value((r.s[i] >> 8) & 0xFFu)));
+            const uint32_t wd[4] = {r.g[i].x, r.g[i].y, r.g[i].z, r.g[i].w};
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t bits = e2m1x2_half2_bits((wd[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+                const __half2 x = *reinterpret_cast<const __half2 *>(&bits);
+                h[k] = pack_h2(__hmul2(x, k < 8 ? s0 : s1));
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(V + cm_off512(j, 32 * g + 8 * k)) =
+                    make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
+        }
+    }
+}
+
+template <bool FP8>
 __device__ __forceinline__ void produce(const Ctx &c)
 {
     AttnMisc &M = *c.M;
-    const UnitDev &U = *c.U;
     const int ptid = threadIdx.x - 128;
-    // row metadata of tile t into raw buffer rb, then cp.async of its bytes
-    auto gather = [&](int t, int rb) {
-        if (ptid < kTile) {
-            const int v = c.row0 + t * kTile + ptid;
-            const uint8_t *ptr = nullptr;
-            float sc = 0.0f;
-            if (v < c.row0 + c.n_rows) {
-                if (!c.fp8) {
-                    const int32_t pos = __ldg(U.idx + (int64_t)c.b * c.P->topk + v);
-                    if (pos >= 0) {
-                        const int64_t slot = pos < c.L ? slot_of(U.cache, c.b, pos) : -1;
-                        if (slot < 0) {
-                            raise_flag(c.flags, kFlagBounds);
-                        } else {
-                            ptr = U.cache.data + slot * kKvRow;
-                            sc = 1.0f;
-                        }
-                    }
-                } else {
-                    const int64_t pos = (int64_t)c.L - c.W + v;
-                    if (pos >= 0) {
-                        const int64_t slot = slot_of(U.cache, c.b, pos);
-                        if (slot < 0) {
-                            raise_flag(c.flags, kFlagBounds);
-                        } else {
-                            ptr = U.cache.data + slot * kDim;
-                            sc = __ldg(reinterpret_cast<const float *>(U.cache.data + U.cache.n_slots * kDim) + slot);
-                        }
-                    }
-                }
-            }
-            M.rowptr[rb][ptid] = ptr;
-            M.rscale[rb][ptid] = sc;
-            M.rvalid[rb][ptid] = ptr != nullptr;
-        }
-        tc::named_sync(1, 128);
-        if (!c.fp8) {
-            uint8_t *raw = c.Raw + rb * kRawHalf;
-            for (int k = ptid; k < kTile * (kKvRow / 16); k += 128) {
-                const int j = k / (kKvRow / 16), g = k % (kKvRow / 16);
-                const uint8_t *src = M.rowptr[rb][j];
-                if (src) tc::cp_async16(raw + j * kKvRow + g * 16, src + g * 16);
-            }
-        } else {
-            for (int k = ptid; k < kTile * (kDim / 16); k += 128) {
-                const int j = k / (kDim / 16), g = k % (kDim / 16);
-                const uint8_t *src = M.rowptr[0][j];
-                if (src) tc::cp_async16(c.Raw + j * kDim + g * 16, src + g * 16);
-            }
-        }
-        tc::cp_async_commit();
-    };
-
-    if (c.n_tiles > 0) gather(0, 0);
+    const int j = ptid & (kTile - 1), w = ptid >> 5;
+    if (!FP8) {
+        for (int i = ptid; i < c.n_rows; i += kProducers)
+            c.sidx[i] = __ldg(c.U->idx + (int64_t)c.b * c.P->topk + c.row0 + i);
+        tc::named_sync(1, kProducers);
+    }
+    RowRegs<FP8> cur, nxt;
+    if (c.n_tiles > 0) load_row<FP8>(c, 0, j, w, cur);
     for (int t = 0; t < c.n_tiles; ++t) {
         const int vb = t & 1;
-        const int rb = c.fp8 ? 0 : (t & 1);
-        if (!c.fp8) {
-            if (t + 1 < c.n_tiles) gather(t + 1, (t + 1) & 1);
-            else tc::cp_async_commit();  // keep one group per iteration
-            tc::cp_async_wait_one();
-        } else {
-            if (t > 0) gather(t, 0);
-            tc::cp_async_wait_all();
-        }
+        if (t + 1 < c.n_tiles) load_row<FP8>(c, t + 1, j, w, nxt);  // in flight during this tile's work
         // V[vb] and its row metadata are free once PV(t-2) has finished
         const bool bad = (t >= 2) && !tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
-        if (bar_any(1, bad)) {  // also the barrier after every producer's rows have landed
+        if (bar_any(1, kProducers, bad)) {
             if (ptid == 0) raise_flag(c.flags, kFlagTimeout);
             break;
         }
-        uint8_t *V = c.Vs + vb * kVBytes;
-        if (!c.fp8) {
-            const uint8_t *raw = c.Raw + rb * kRawHalf;
-            for (int k = ptid; k < kTile * 16; k += 128) {
-                const int j = k & (kTile - 1), g = k >> 5;  // row j, channels 32g..32g+31
-                uint4 o[4];
-                if (M.rvalid[rb][j]) {
-                    const uint8_t *src = raw + j * kKvRow;
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(src + g * 16);
-                    const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(src + kKvCodes + 2 * g);
-                    const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(sc2 & 0xFFu)));
-                    const __half2 s1 = __half2half2(__float2half_rn(e4m3_value(sc2 >> 8)));
-                    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-                    uint32_t h[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint32_t bits = e2m1x2_half2_bits((w[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-                        const __half2 x = *reinterpret_cast<const __half2 *>(&bits);
-                        h[i] = pack_h2(__hmul2(x, i < 8 ? s0 : s1));
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(V + cm_off512(j, 32 * g + 8 * i)) = o[i];
-            }
-        } else {
-            for (int k = ptid; k < kTile * 32; k += 128) {
-                const int j = k & (kTile - 1), g = k >> 5;  // row j, channels 16g..16g+15
-                uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-                if (M.rvalid[0][j]) {
-                    const uint4 cw = *reinterpret_cast<const uint4 *>(c.Raw + j * kDim + g * 16);
-                    o0 = make_uint4(pack_h2(e4m3x2_half2(cw.x & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.x >> 16)),
-                                    pack_h2(e4m3x2_half2(cw.y & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.y >> 16)));
-                    o1 = make_uint4(pack_h2(e4m3x2_half2(cw.z & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.z >> 16)),
-                                    pack_h2(e4m3x2_half2(cw.w & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.w >> 16)));
-                }
-                *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g)) = o0;
-                *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g + 8)) = o1;
-            }
-        }
-        if (ptid < kTile) {
-            M.mvalid[vb][ptid] = M.rvalid[rb][ptid];
-            M.mscale[vb][ptid] = M.rscale[rb][ptid];
+        store_row<FP8>(c.Vs + vb * kVBytes, j, w, cur);
+        if (w == 0) {
+            const uint32_t mask = __ballot_sync(0xFFFFFFFFu, cur.valid);
+            if (j == 0) M.vmask[vb] = mask;
+            M.mscale[vb][j] = FP8 ? __uint_as_float(cur.s[0]) : 1.0f;
         }
         tc::fence_async_smem();
         tc::mbar_arrive(&M.full_v[vb]);
-        tc::named_sync(1, 128);  // raw[rb] may be refilled after this
+        cur = nxt;
     }
-    tc::cp_async_wait_all();
 }
 
-// ---- MMA issuer (warp 8, lane 0) -----------------------------------------------------
+// ---- MMA issuer (one thread) ---------------------------------------------------------
+// QK^T of tile t is issued in groups of 8 MMAs; between groups (and while
+// waiting for the next tile) the issuer polls for a finished P and issues its
+// PV at once, so PV never queues behind a whole QK^T.
 __device__ __forceinline__ void issue_mmas(const Ctx &c)
 {
     AttnMisc &M = *c.M;
@@ -299,49 +303,86 @@ __device__ __forceinline__ void issue_mmas(const Ctx &c)
                      kQRowsBytes, &M.q_bar);
     bool ok = tc::mbar_wait(&M.q_bar, 0);
     if (!ok) tc::mbar_wait(&M.q_bar, 0);  // let copies in flight land before giving up
+    // descriptors; a K step of 16 adds 256 B (16 in the 16-byte address field) to the
+    // K-major operands and 16,384 B (1,024) to V read MN-major
+    const uint64_t qd = tc::sdesc(tc::smem_u32(c.Qs), 128, 8192);
+    const uint32_t va0 = tc::smem_u32(c.Vs), va1 = tc::smem_u32(c.Vs + kVBytes);
+    const uint64_t vd0 = tc::sdesc(va0, 128, 8192), vd1 = tc::sdesc(va1, 128, 8192);
+    const uint64_t vm0 = tc::sdesc(va0 + c.half * (256 / 8) * 128, 8192, 128);
+    const uint64_t vm1 = tc::sdesc(va1 + c.half * (256 / 8) * 128, 8192, 128);
+    const uint64_t pd0 = tc::sdesc(tc::smem_u32(c.Ps), 128, 512);
+    const uint64_t pd1 = tc::sdesc(tc::smem_u32(c.Ps + kPBytes), 128, 512);
+    int qk_done = 0;  // tiles whose QK^T has been issued
+    int pv_next = 0;  // next tile whose PV is due
     uint64_t *last_bar = nullptr;
     uint32_t last_par = 0;
-    const uint32_t qa = tc::smem_u32(c.Qs), pa = tc::smem_u32(c.Ps);
     auto issue_pv = [&](int t) {
-        if (!tc::mbar_wait(&M.p_full, t & 1)) {
-            ok = false;
-            return;
-        }
+        const int pb = t & 1;
         tc::fence_after_sync();
-        // B = V[t&1] read MN-major: N = this CTA's 256 channels (8-channel groups 128 B apart),
-        // K = 32 keys (8-key groups 8,192 B apart)
-        const uint32_t vb = tc::smem_u32(c.Vs + (t & 1) * kVBytes) + c.half * (256 / 8) * 128;
-        for (int ks = 0; ks < kTile / 16; ++ks)
-            tc::mma_f16(c.tmem + kColO, tc::sdesc(pa + ks * 256, 128, 512), tc::sdesc(vb + ks * 2 * 8192, 8192, 128),
-                        kIdescPV, (t > 0 || ks > 0) ? 1u : 0u);
-        tc::mma_commit(&M.pv_done[t & 1]);
-        last_bar = &M.pv_done[t & 1];
+        const uint64_t pdb = pb ? pd1 : pd0, vmb = pb ? vm1 : vm0;
+        tc::mma_f16(c.tmem + kColO, pdb, vmb, kIdescPV, t > 0 ? 1u : 0u);
+        tc::mma_f16(c.tmem + kColO, pdb + 16, vmb + 1024, kIdescPV, 1u);
+        tc::mma_commit(&M.pv_done[pb]);
+        last_bar = &M.pv_done[pb];
         last_par = (t >> 1) & 1;
+    };
+    // issue every PV whose P is ready (non-blocking)
+    auto poll_pv = [&]() {
+        while (pv_next < qk_done && tc::mbar_try_wait(&M.p_full[pv_next & 1], (pv_next >> 1) & 1)) {
+            issue_pv(pv_next);
+            ++pv_next;
+        }
+    };
+    // bounded wait on (bar, parity) that keeps issuing ready PVs meanwhile
+    auto wait_polling = [&](uint64_t *bar, uint32_t par) {
+        for (uint32_t i = 0; i < tc::kWaitLimit; ++i) {
+            if (tc::mbar_try_wait(bar, par)) return true;
+            poll_pv();
+        }
+        return false;
     };
     for (int t = 0; t < c.n_tiles && ok; ++t) {
         const int vb = t & 1;
-        if (!tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) ||
-            (t >= 2 && !tc::mbar_wait(&M.s_free[vb], ((t - 2) >> 1) & 1))) {
+        if (!wait_polling(&M.full_v[vb], (t >> 1) & 1) ||
+            (t >= 2 && !wait_polling(&M.s_free[vb], ((t - 2) >> 1) & 1))) {
             ok = false;
             break;
         }
         tc::fence_after_sync();
-        const uint32_t va = tc::smem_u32(c.Vs + vb * kVBytes);
-        for (int ks = 0; ks < kDim / 16; ++ks)
-            tc::mma_f16(c.tmem + 32 * vb, tc::sdesc(qa + ks * 256, 128, 8192), tc::sdesc(va + ks * 256, 128, 8192),
-                        kIdescQK, ks > 0 ? 1u : 0u);
-        tc::mma_commit(&M.s_full[vb]);
-        last_bar = &M.s_full[vb];
-        last_par = (t >> 1) & 1;
-        if (t >= 1) issue_pv(t - 1);
+        const uint32_t d = c.tmem + 32 * vb;
+        const uint64_t vdb = vb ? vd1 : vd0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int ks = 8 * g + k;
+                tc::mma_f16(d, qd + 16 * ks, vdb + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+            }
+            if (g == 3) {
+                tc::mma_commit(&M.s_full[vb]);
+                last_bar = &M.s_full[vb];
+                last_par = (t >> 1) & 1;
+                qk_done = t + 1;
+            }
+            poll_pv();
+        }
     }
-    if (ok && c.n_tiles > 0) issue_pv(c.n_tiles - 1);
+    // the remaining PVs, in order
+    while (ok && pv_next < qk_done) {
+        if (!tc::mbar_wait(&M.p_full[pv_next & 1], (pv_next >> 1) & 1)) {
+            ok = false;
+            break;
+        }
+        issue_pv(pv_next);
+        ++pv_next;
+    }
     if (!ok) raise_flag(c.flags, kFlagTimeout);
     // every issued MMA must have finished before the tensor memory is released
     if (last_bar) tc::mbar_wait(last_bar, last_par);
 }
 
 // ---- softmax rows (warps 0-3, thread = tensor-memory lane = query row) ----------------
+template <bool FP8>
 __device__ __forceinline__ void softmax_rows(const Ctx &c)
 {
     AttnMisc &M = *c.M;
@@ -364,24 +405,25 @@ __device__ __forceinline__ void softmax_rows(const Ctx &c)
         tc::tmem_ld32(tc::taddr(c.tmem, lane_base, 32 * vb), s);
         tc::fence_before_sync();
         tc::mbar_arrive(&M.s_free[vb]);
+        const uint32_t vmask = M.vmask[vb];
         float mt = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kTile; ++j) {
-            s[j] = M.mvalid[vb][j] ? s[j] * M.mscale[vb][j] : -INFINITY;
+            const float z = FP8 ? s[j] * M.mscale[vb][j] : s[j];
+            s[j] = ((vmask >> j) & 1u) ? z : -INFINITY;
             mt = fmaxf(mt, s[j]);
         }
-        // PV(t-1) must be done: O is then current and the P buffer free
-        w_ok = (t == 0) || tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
-            ok = false;
-            break;
-        }
-        tc::fence_after_sync();
         const float m_new = active ? fmaxf(m_used, mt) : m_used;
         // lazy rescale, warp-uniform: every lane of the warp joins the tensor-memory traffic
         if (__any_sync(0xFFFFFFFFu, active && m_new > m_used + kRescaleGap)) {
-            const float alpha = (active && m_used != -INFINITY) ? __expf(m_used - m_new) : (active ? 0.0f : 1.0f);
             if (t >= 1) {
+                w_ok = tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);  // O is current
+                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const float alpha = (active && m_used != -INFINITY) ? __expf(m_used - m_new) : (active ? 0.0f : 1.0f);
 #pragma unroll 1
                 for (int c0 = 0; c0 < 256; c0 += 32) {
                     float o[32];
@@ -390,32 +432,41 @@ __device__ __forceinline__ void softmax_rows(const Ctx &c)
                     for (int i = 0; i < 32; ++i) o[i] *= alpha;
                     tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
                 }
+                if (active) l_sum *= alpha;
             }
-            if (active) {
-                l_sum *= alpha;
-                m_used = m_new;
-            }
+            if (active) m_used = m_new;
         }
+        // P[vb] is free once PV(t-2) has finished
+        w_ok = (t < 2) || tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+            ok = false;
+            break;
+        }
+        const float mb = m_used * kLog2e;
+        float p[kTile];
+        float ls = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kTile; ++j) {
+            p[j] = (active && s[j] != -INFINITY) ? exp2f(fmaf(s[j], kLog2e, -mb)) : 0.0f;
+            ls += p[j];
+        }
+        l_sum += ls;
         uint32_t ph[kTile / 2];
 #pragma unroll
         for (int j = 0; j < kTile; j += 2) {
-            float p0 = 0.0f, p1 = 0.0f;
-            if (active) {
-                p0 = (s[j] == -INFINITY) ? 0.0f : __expf(s[j] - m_used);
-                p1 = (s[j + 1] == -INFINITY) ? 0.0f : __expf(s[j + 1] - m_used);
-                l_sum += p0 + p1;
-            }
-            // window rows hold raw E4M3 codes: their per-token scale joins the weight
-            ph[j >> 1] = pack_h2(__floats2half2_rn(p0 * M.mscale[vb][j], p1 * M.mscale[vb][j + 1]));
+            const float a = FP8 ? p[j] * M.mscale[vb][j] : p[j];      // window rows hold raw E4M3 codes:
+            const float d = FP8 ? p[j + 1] * M.mscale[vb][j + 1] : p[j + 1];  // their scale joins the weight
+            ph[j >> 1] = pack_h2(__floats2half2_rn(a, d));
         }
         // P row into its K-major core-matrix layout: 4 groups of 8 keys, 512 B per 8-row group
+        uint8_t *Pb = c.Ps + vb * kPBytes;
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-            *reinterpret_cast<uint4 *>(c.Ps + (tid >> 3) * 512 + g * 128 + (tid & 7) * 16) =
+            *reinterpret_cast<uint4 *>(Pb + (tid >> 3) * 512 + g * 128 + (tid & 7) * 16) =
                 make_uint4(ph[4 * g], ph[4 * g + 1], ph[4 * g + 2], ph[4 * g + 3]);
         tc::fence_async_smem();
         tc::fence_before_sync();
-        tc::mbar_arrive(&M.p_full);
+        tc::mbar_arrive(&M.p_full[vb]);
     }
     if (ok && c.n_tiles > 0) {
         const int last = c.n_tiles - 1;
@@ -516,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     c.Qs = smem;
     c.Vs = smem + kOffV;
     c.Ps = smem + kOffP;
-    c.Raw = smem + kOffRaw;
+    c.sidx = reinterpret_cast<int32_t *>(smem + kOffIdx);
     c.flags = flags;
     c.b = blockIdx.y;
     int u = 0;
@@ -541,31 +592,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     if (tid == 0) {
         tc::mbar_init(&M.q_bar, 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&M.full_v[i], 128);
+            tc::mbar_init(&M.full_v[i], kProducers);
             tc::mbar_init(&M.s_full[i], 1);
             tc::mbar_init(&M.s_free[i], 128);
             tc::mbar_init(&M.pv_done[i], 1);
+            tc::mbar_init(&M.p_full[i], 128);
         }
-        tc::mbar_init(&M.p_full, 128);
         tc::mbar_init_fence();
     }
-    if (warp == 8) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
+    if (warp == kMmaWarp) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     c.tmem = M.tmem_slot;
 
-    if (warp >= 4 && warp < 8) {
-        produce(c);
-    } else if (warp == 8) {
+    if (warp >= 4 && warp < kMmaWarp) {
+        if (c.fp8) produce<true>(c);
+        else produce<false>(c);
+    } else if (warp == kMmaWarp) {
         if (lane == 0) issue_mmas(c);
         __syncwarp();
     } else {
-        softmax_rows(c);
+        if (c.fp8) softmax_rows<true>(c);
+        else softmax_rows<false>(c);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(c.tmem, kTmemCols);
     }
@@ -609,15 +662,16 @@ UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
     return up;
 }
 
-// Rows per chunk of a row unit: 256 (8 tiles), doubled while the grid would
-// exceed 8 waves of one CTA per SM (large batches need no split).
+// Rows per chunk of a row unit: 256 (8 tiles), doubled (up to the 2,048 rows
+// whose positions a CTA stages) while the grid would exceed 8 waves of one
+// CTA per SM (large batches need no split).
 int rows_per_chunk(int n_row_units, int n_window_units, int batch, int topk)
 {
     int rpc = 256;
     auto ctas = [&](int r) {
         return (int64_t)batch * 2 * ((int64_t)n_row_units * ((topk + r - 1) / r) + n_window_units);
     };
-    while (rpc < topk && ctas(rpc) > 8 * 148) rpc *= 2;
+    while (rpc < topk && rpc < kMaxChunkRows && ctas(rpc) > 8 * 148) rpc *= 2;
     return rpc;
 }
 
