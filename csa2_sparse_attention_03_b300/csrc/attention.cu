@@ -12,28 +12,40 @@
 // of up to 8 layers: their 8 x 16 = 128 query rows share every gathered row,
 // so a row is read and dequantised once for all of them and QK^T and PV are
 // 128-row tensor-core products.  Each layer's own window rows form a *window
-// unit*.  A CTA takes one (unit, chunk of rows, half of the output channels,
-// sequence) and produces a partial (running max, sum, unnormalised output);
-// the last CTA to finish a (layer, sequence, half) merges its partials.
+// unit*.  A *CTA pair* (a cluster of two) takes one (unit, chunk of rows,
+// sequence); CTA h of the pair owns channels 256h..256h+255 of the queries,
+// of every gathered row and of the output.  QK^T is split along channels:
+// each CTA forms the partial scores of its half, the two swap partials with
+// one bulk shared-memory copy each way and both add them (fp32 addition
+// commutes, so both hold bit-identical scores and run the identical softmax).
+// PV then touches only the CTA's own channels.  Each CTA leaves a partial
+// (running max, sum, unnormalised output of its half) per consumer layer; a
+// second kernel merges each (layer, sequence, half)'s partials in parallel.
 //
-// One CTA, 9 warps:
-//   warps 4-7  producers: each thread owns one row of a 32-row tile and a
-//              quarter of its bytes; it loads the next tile's bytes into
+// Tensor memory (512 columns): the 128 query rows of the CTA's half as fp16
+// pairs (128 columns, the A operand of QK^T), S double-buffered (2 x 64), and
+// O (256 columns).
+//
+// One CTA, 13 warps:
+//   warps 0-7  softmax: warp w serves query rows 32(w%4)..+31 (its tensor-
+//              memory lanes) and keys 32(w/4)..+31 of each 64-row tile; it
+//              first writes its rows' queries into tensor memory;
+//   warps 8-11 producers: per 64-row tile each thread owns one row and half
+//              of the CTA's channels; it loads the next tile's bytes into
 //              registers while it dequantises the current one (E2M1 x E4M3
 //              and E4M3 are exact in fp16) into the core-matrix layout;
-//   warp 8     tensor-memory allocation and tcgen05.mma issue, descriptors
-//              precomputed: S[b] = Q V^T (M 128, N 32, K 512) into tensor
-//              memory, then O += P V (M 128, N 256, K 32), O resident in
-//              tensor memory;
-//   warps 0-3  one thread per query row: S from tensor memory, fp32 online
-//              softmax with lazy rescaling of O (only when the running max
-//              grows by more than e^8), P to shared memory as fp16.
+//   warp 12    tensor-memory allocation and tcgen05.mma issue: S[b] = Q_h V_h^T
+//              (M 128, N 64, K 256; A from tensor memory), then O_h += P V_h
+//              (M 128, N 256, K 64), O_h resident in tensor memory.
 // V, S and P are double-buffered, so the softmax of tile t+1 does not wait
-// for PV(t) unless O must be rescaled.  Every hand-off is an mbarrier with a
-// bounded wait (a wait that gives up raises the timeout flag and the CTA
-// drains and exits).
+// for PV(t) unless O must be rescaled (lazy: only when a row's running max
+// grows by more than e^8).  Every hand-off is an mbarrier with a bounded wait
+// (a wait that gives up raises the timeout flag and the CTA drains); both
+// CTAs of a pair meet at a cluster barrier before either exits, so neither
+// touches the shared memory of a CTA that has finished.
 #include <algorithm>
 #include <cstring>
+#include <queue>
 #include <utility>
 #include <vector>
 
@@ -43,35 +55,45 @@
 namespace csa2 {
 namespace {
 
-constexpr int kTile = 32;                  // rows per tile
-constexpr int kProducers = 256;            // producer threads (warps 4-11)
+constexpr int kTile = 64;                  // rows per tile
+constexpr int kHalf = 256;                 // channels per CTA of a pair
+constexpr int kSoftThreads = 256;          // warps 0-7
+constexpr int kProducers = 128;            // warps 8-11
 constexpr int kMmaWarp = 12;
 constexpr int kThreads = 416;              // 13 warps
-constexpr int kMaxChunkRows = 2048;        // rows per chunk of a row unit (indices staged in smem)
-constexpr int kQRowsBytes = kHeads * kDim * 2;  // 16 KB: one layer's 16 query rows in fp16
-constexpr int kQBytes = 8 * kQRowsBytes;   // 131,072: 128 query rows
-constexpr int kVBytes = kTile * kDim * 2;  // 32,768 per buffer
-constexpr int kPBytes = 128 * kTile * 2;   // 8,192 per buffer
-constexpr int kOffV = kQBytes;
+constexpr int kMaxChunkRows = 2048;        // rows per chunk of a row unit
+constexpr int kVBytes = kTile * kHalf * 2; // 32,768 per buffer
+constexpr int kPBytes = 128 * kTile * 2;   // 16,384 per buffer
+constexpr int kXBytes = 128 * kTile * 4;   // 32,768: partial scores of one tile
+constexpr int kOffV = 0;
 constexpr int kOffP = kOffV + 2 * kVBytes;
-constexpr int kOffIdx = kOffP + 2 * kPBytes;
-constexpr int kOffMisc = kOffIdx + kMaxChunkRows * 4;
+constexpr int kOffXin = kOffP + 2 * kPBytes;   // the peer's partial lands here
+constexpr int kOffXout = kOffXin + kXBytes;    // ours, staged for the copy to the peer
+constexpr int kOffMisc = kOffXout + kXBytes;
 constexpr int kPartFloats = 64 + kHeads * kDim;  // m[2][16], l[2][16], O[16][512]
 constexpr int kMaxUnits = 2 * kMaxAttnEntries;
+constexpr int kMaxParts = 64;              // partials per layer: at most 63 row chunks and the window
 constexpr float kRescaleGap = 8.0f;        // lazy O rescale threshold (natural log)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kTmemCols = 512;        // S[0] cols 0-31, S[1] cols 32-63, O cols 256-511
-constexpr uint32_t kColO = 256;
-// Instruction descriptors: QK^T (both operands K-major), PV (B = V read MN-major).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0;              // 128 columns: query rows, fp16 pairs
+constexpr uint32_t kColS = 128;            // 2 x 64 columns
+constexpr uint32_t kColO = 256;            // 256 columns
+// Instruction descriptors: QK^T (A from tensor memory, B K-major), PV (A K-major, B = V read MN-major).
 constexpr uint32_t kIdescQK = tc::idesc_f16(128, kTile, false, false);
-constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, false, true);
+constexpr uint32_t kIdescPV = tc::idesc_f16(128, kHalf, false, true);
+// named barriers: 1 producers, 2 softmax (all 256)
+constexpr uint32_t kBarProd = 1, kBarSoft = 2;
 
 struct AttnMisc {
     float mscale[2][kTile];   // per V buffer: per-row scale (FP8 window rows)
-    uint32_t vmask[2];        // per V buffer: valid rows
+    uint32_t vmask[2][2];     // per V buffer: valid rows (bit j of word j/32)
+    float xmax[2][2][128];    // per tile parity and key half: tile max of each query row
+    float lpart[128];         // running sum of the second key half, for the final combine
     uint64_t q_bar, full_v[2], s_full[2], s_free[2], p_full[2], pv_done[2];
+    uint64_t x_full;          // the peer's partial scores have landed in Xin (bulk copy)
+    uint64_t x_free;          // the peer has consumed the partial this CTA sent it
     uint32_t tmem_slot;
-    int32_t last[8];
 };
 static_assert(kOffMisc + (int)sizeof(AttnMisc) <= 232448, "attention shared memory over the 227 KB limit");
 
@@ -81,10 +103,11 @@ struct UnitDev {
     int32_t is_window;
     int32_t n_layers;       // consumer layers (1..8)
     int32_t entry[8];
-    int32_t cta_begin;      // first flat CTA (x) index of this unit
+    int32_t cta_begin;      // first flat CTA (x) index of this unit (even)
 };
 
 struct EntryDev {
+    const float *q;         // [B][16][512]
     float *out;             // [B][16][512]
     float *lse;             // [B][16] or null
     int32_t n_parts;        // partials of this layer: row chunks + window
@@ -97,40 +120,26 @@ struct AttnParams {
     int32_t n_units;
     int32_t batch, topk, window, rows_per_chunk, max_parts;
     const int32_t *seq_lens;
-    const uint8_t *q16;     // [entry][B][16 KB] fp16 query rows in core-matrix layout
     float *partials;        // [entry][B][max_parts][kPartFloats]
-    uint32_t *counters;     // [entry][B][2]
 };
 
-struct QList {
-    const float *q[kMaxAttnEntries];
-};
-
-// Byte offset of fp16 element (row r, channel c) of an operand with 512-channel
-// rows in the no-swizzle core-matrix layout: 8-row groups 8,192 B apart,
+// Byte offset of fp16 element (row r, channel c) of an operand with 256-channel
+// rows in the no-swizzle core-matrix layout: 8-row groups 4,096 B apart,
 // 8-channel groups 128 B apart.
-__host__ __device__ __forceinline__ uint32_t cm_off512(uint32_t r, uint32_t c)
+__host__ __device__ __forceinline__ uint32_t cm_off256(uint32_t r, uint32_t c)
 {
-    return (r >> 3) * 8192u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
+    return (r >> 3) * 4096u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
+}
+
+// Partial scores of one tile: row r holds 16 float4 (64 keys), chunk k at
+// position k ^ (r & 7), so a quarter-warp's 16-byte accesses (8 consecutive
+// rows, same k) fall in distinct banks.
+__host__ __device__ __forceinline__ uint32_t x_off(uint32_t r, uint32_t k)
+{
+    return r * (kTile * 4) + ((k ^ (r & 7u)) * 16u);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
-
-// q (fp32 [B][16][512]) -> fp16 core-matrix rows, 16 KB per layer and sequence.
-__global__ void __launch_bounds__(256) pack_q_kernel(const __grid_constant__ QList qs, uint8_t *q16, int batch)
-{
-    const int e = blockIdx.x, b = blockIdx.y;
-    const float *q = qs.q[e] + (int64_t)b * kHeads * kDim;
-    uint8_t *dst = q16 + ((int64_t)e * batch + b) * kQRowsBytes;
-    for (int it = threadIdx.x; it < kHeads * kDim / 8; it += blockDim.x) {
-        const int r = it / (kDim / 8), c = (it % (kDim / 8)) * 8;
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(q + r * kDim + c));
-        const float4 d = __ldg(reinterpret_cast<const float4 *>(q + r * kDim + c + 4));
-        *reinterpret_cast<uint4 *>(dst + cm_off512(r, c)) =
-            make_uint4(pack_h2(__floats2half2_rn(a.x, a.y)), pack_h2(__floats2half2_rn(a.z, a.w)),
-                       pack_h2(__floats2half2_rn(d.x, d.y)), pack_h2(__floats2half2_rn(d.z, d.w)));
-    }
-}
 
 // OR-reduction of a predicate over the `count` threads of named barrier `id`
 // (also a barrier); every participant gets the same result.
@@ -150,28 +159,33 @@ struct Ctx {
     const AttnParams *P;
     const UnitDev *U;
     AttnMisc *M;
-    uint8_t *Qs, *Vs, *Ps;
-    int32_t *sidx;      // the chunk's row positions (row units)
+    uint8_t *Vs, *Ps, *Xin, *Xout;
     int *flags;
     uint32_t tmem;
     int b, L, W, row0, n_rows, n_tiles, chunk, half;
-    bool fp8;
 };
 
-// ---- producers (warps 4-11): gather + dequantise 32-row tiles ------------------------
-// Thread ptid owns row j = ptid % 32 of every tile and the eighth w = ptid / 32
-// of its 16-byte granules (FP4 rows: 16 granules of 32 channels, g = w, w + 8;
-// FP8 rows: 32 granules of 16 channels, g = w + 8i).
-constexpr int kPW = kProducers / 32;  // producer warps
+// ---- producers (warps 8-11): gather + dequantise 64-row tiles -------------------------
+// Thread ptid owns row j = ptid % 64 of every tile and the half w = ptid / 64
+// of the CTA's 256 channels: channels 256h + 128w .. +127 (FP4 rows: four
+// 16-byte granules of 32 channels and eight E4M3 scales; FP8 rows: eight
+// granules of 16).
 template <bool FP8>
 struct RowRegs {
-    uint4 g[FP8 ? 32 / kPW : 16 / kPW];
-    uint32_t s[FP8 ? 1 : 16 / kPW];  // FP4: two E4M3 scales per granule; FP8: the row's fp32 scale bits
+    uint4 g[FP8 ? 8 : 4];
+    uint32_t s[FP8 ? 1 : 2];  // FP4: the eight E4M3 scales; FP8: the row's fp32 scale bits
     bool valid;
 };
 
+// Position of row j of tile t of the chunk (row units; -1 past the chunk's end).
+__device__ __forceinline__ int32_t row_pos(const Ctx &c, int t, int j)
+{
+    const int v = t * kTile + j;
+    return v < c.n_rows ? __ldg(c.U->idx + (int64_t)c.b * c.P->topk + c.row0 + v) : -1;
+}
+
 template <bool FP8>
-__device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, RowRegs<FP8> &r)
+__device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, int32_t pos_fp4, RowRegs<FP8> &r)
 {
     const UnitDev &U = *c.U;
     const int v = t * kTile + j;  // row within this chunk
@@ -179,7 +193,7 @@ __device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, RowR
     uint32_t sc = 0u;
     if (v < c.n_rows) {
         if (!FP8) {
-            const int32_t pos = c.sidx[v];
+            const int32_t pos = pos_fp4;
             if (pos >= 0) {
                 const int64_t slot = pos < c.L ? slot_of(U.cache, c.b, pos) : -1;
                 if (slot < 0) {
@@ -204,16 +218,19 @@ __device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, RowR
     r.valid = ptr != nullptr;
     if (FP8) {
         r.s[0] = sc;
+        const uint8_t *base = ptr ? ptr + c.half * 256 + 128 * w : nullptr;
 #pragma unroll
-        for (int i = 0; i < 32 / kPW; ++i)
-            r.g[i] = ptr ? __ldg(reinterpret_cast<const uint4 *>(ptr + 16 * (w + kPW * i))) : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 8; ++i)
+            r.g[i] = base ? __ldg(reinterpret_cast<const uint4 *>(base + 16 * i)) : make_uint4(0u, 0u, 0u, 0u);
     } else {
+        const uint8_t *base = ptr ? ptr + c.half * 128 + 64 * w : nullptr;
 #pragma unroll
-        for (int i = 0; i < 16 / kPW; ++i) {
-            r.g[i] = ptr ? __ldg(reinterpret_cast<const uint4 *>(ptr + 16 * (w + kPW * i))) : make_uint4(0u, 0u, 0u, 0u);
-            r.s[i] = ptr ? (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(ptr + kKvCodes + 2 * (w + kPW * i)))
-                         : 0u;
-        }
+        for (int i = 0; i < 4; ++i)
+            r.g[i] = base ? __ldg(reinterpret_cast<const uint4 *>(base + 16 * i)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint2 sc2 = ptr ? __ldg(reinterpret_cast<const uint2 *>(ptr + kKvCodes + c.half * 16 + 8 * w))
+                              : make_uint2(0u, 0u);
+        r.s[0] = sc2.x;
+        r.s[1] = sc2.y;
     }
 }
 
@@ -222,22 +239,23 @@ __device__ __forceinline__ void store_row(uint8_t *V, int j, int w, const RowReg
 {
     if (FP8) {
 #pragma unroll
-        for (int i = 0; i < 32 / kPW; ++i) {
-            const int g = w + kPW * i;  // channels 16g..16g+15
+        for (int i = 0; i < 8; ++i) {
+            const int ch = 128 * w + 16 * i;  // channels ch..ch+15 of the half
             const uint4 cw = r.g[i];
-            *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g)) =
+            *reinterpret_cast<uint4 *>(V + cm_off256(j, ch)) =
                 make_uint4(pack_h2(e4m3x2_half2(cw.x & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.x >> 16)),
                            pack_h2(e4m3x2_half2(cw.y & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.y >> 16)));
-            *reinterpret_cast<uint4 *>(V + cm_off512(j, 16 * g + 8)) =
+            *reinterpret_cast<uint4 *>(V + cm_off256(j, ch + 8)) =
                 make_uint4(pack_h2(e4m3x2_half2(cw.z & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.z >> 16)),
                            pack_h2(e4m3x2_half2(cw.w & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.w >> 16)));
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 16 / kPW; ++i) {
-            const int g = w + kPW * i;  // channels 32g..32g+31, scales 2g (first 16) and 2g+1
-            const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(r.s[i] & 0xFFu)));
-            const __half2 s1 = __half2half2(__float2half_rn(e4m3_value((r.s[i] >> 8) & 0xFFu)));
+        for (int i = 0; i < 4; ++i) {
+            const int ch = 128 * w + 32 * i;  // channels ch..ch+31; scales of its two 16-channel blocks
+            const uint32_t sw = r.s[i >> 1] >> (16 * (i & 1));
+            const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(sw & 0xFFu)));
+            const __half2 s1 = __half2half2(__float2half_rn(e4m3_value((sw >> 8) & 0xFFu)));
             const uint32_t wd[4] = {r.g[i].x, r.g[i].y, r.g[i].z, r.g[i].w};
             uint32_t h[16];
 #pragma unroll
@@ -248,7 +266,7 @@ __device__ __forceinline__ void store_row(uint8_t *V, int j, int w, const RowReg
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(V + cm_off512(j, 32 * g + 8 * k)) =
+                *reinterpret_cast<uint4 *>(V + cm_off256(j, ch + 8 * k)) =
                     make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         }
     }
@@ -258,28 +276,26 @@ template <bool FP8>
 __device__ __forceinline__ void produce(const Ctx &c)
 {
     AttnMisc &M = *c.M;
-    const int ptid = threadIdx.x - 128;
-    const int j = ptid & (kTile - 1), w = ptid >> 5;
-    if (!FP8) {
-        for (int i = ptid; i < c.n_rows; i += kProducers)
-            c.sidx[i] = __ldg(c.U->idx + (int64_t)c.b * c.P->topk + c.row0 + i);
-        tc::named_sync(1, kProducers);
-    }
+    const int ptid = threadIdx.x - kSoftThreads;
+    const int j = ptid & (kTile - 1), w = ptid >> 6;
+    // row positions run two tiles ahead of the row bytes, so no load waits on another
+    int32_t pos_next = FP8 ? -1 : row_pos(c, 1, j);
     RowRegs<FP8> cur, nxt;
-    if (c.n_tiles > 0) load_row<FP8>(c, 0, j, w, cur);
+    if (c.n_tiles > 0) load_row<FP8>(c, 0, j, w, FP8 ? -1 : row_pos(c, 0, j), cur);
     for (int t = 0; t < c.n_tiles; ++t) {
         const int vb = t & 1;
-        if (t + 1 < c.n_tiles) load_row<FP8>(c, t + 1, j, w, nxt);  // in flight during this tile's work
+        if (t + 1 < c.n_tiles) load_row<FP8>(c, t + 1, j, w, pos_next, nxt);  // in flight during this tile's work
+        if (!FP8) pos_next = row_pos(c, t + 2, j);
         // V[vb] and its row metadata are free once PV(t-2) has finished
         const bool bad = (t >= 2) && !tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
-        if (bar_any(1, kProducers, bad)) {
+        if (bar_any(kBarProd, kProducers, bad)) {
             if (ptid == 0) raise_flag(c.flags, kFlagTimeout);
             break;
         }
         store_row<FP8>(c.Vs + vb * kVBytes, j, w, cur);
         if (w == 0) {
             const uint32_t mask = __ballot_sync(0xFFFFFFFFu, cur.valid);
-            if (j == 0) M.vmask[vb] = mask;
+            if ((j & 31) == 0) M.vmask[vb][j >> 5] = mask;
             M.mscale[vb][j] = FP8 ? __uint_as_float(cur.s[0]) : 1.0f;
         }
         tc::fence_async_smem();
@@ -289,29 +305,22 @@ __device__ __forceinline__ void produce(const Ctx &c)
 }
 
 // ---- MMA issuer (one thread) ---------------------------------------------------------
-// QK^T of tile t is issued in groups of 8 MMAs; between groups (and while
+// QK^T of tile t is issued in two groups of 8 MMAs; between groups (and while
 // waiting for the next tile) the issuer polls for a finished P and issues its
 // PV at once, so PV never queues behind a whole QK^T.
 __device__ __forceinline__ void issue_mmas(const Ctx &c)
 {
     AttnMisc &M = *c.M;
-    const UnitDev &U = *c.U;
-    // query rows of the consumer layers: layer slot j -> rows 16j..16j+15 (16 KB each)
-    tc::mbar_expect_tx(&M.q_bar, (uint32_t)U.n_layers * kQRowsBytes);
-    for (int j = 0; j < U.n_layers; ++j)
-        tc::bulk_g2s(c.Qs + j * kQRowsBytes, c.P->q16 + ((int64_t)U.entry[j] * c.P->batch + c.b) * kQRowsBytes,
-                     kQRowsBytes, &M.q_bar);
-    bool ok = tc::mbar_wait(&M.q_bar, 0);
-    if (!ok) tc::mbar_wait(&M.q_bar, 0);  // let copies in flight land before giving up
-    // descriptors; a K step of 16 adds 256 B (16 in the 16-byte address field) to the
-    // K-major operands and 16,384 B (1,024) to V read MN-major
-    const uint64_t qd = tc::sdesc(tc::smem_u32(c.Qs), 128, 8192);
+    bool ok = tc::mbar_wait(&M.q_bar, 0);  // the queries are in tensor memory
+    // descriptors; a K step of 16 adds 8 columns to the tensor-memory A operand,
+    // 256 B (16 in the 16-byte address field) to K-major smem operands and
+    // 8,192 B (512) to V read MN-major
     const uint32_t va0 = tc::smem_u32(c.Vs), va1 = tc::smem_u32(c.Vs + kVBytes);
-    const uint64_t vd0 = tc::sdesc(va0, 128, 8192), vd1 = tc::sdesc(va1, 128, 8192);
-    const uint64_t vm0 = tc::sdesc(va0 + c.half * (256 / 8) * 128, 8192, 128);
-    const uint64_t vm1 = tc::sdesc(va1 + c.half * (256 / 8) * 128, 8192, 128);
-    const uint64_t pd0 = tc::sdesc(tc::smem_u32(c.Ps), 128, 512);
-    const uint64_t pd1 = tc::sdesc(tc::smem_u32(c.Ps + kPBytes), 128, 512);
+    const uint64_t vd0 = tc::sdesc(va0, 128, 4096), vd1 = tc::sdesc(va1, 128, 4096);
+    const uint64_t vm0 = tc::sdesc(va0, 4096, 128), vm1 = tc::sdesc(va1, 4096, 128);
+    const uint64_t pd0 = tc::sdesc(tc::smem_u32(c.Ps), 128, 1024);
+    const uint64_t pd1 = tc::sdesc(tc::smem_u32(c.Ps + kPBytes), 128, 1024);
+    const uint32_t qa = c.tmem + kColQ;
     int qk_done = 0;  // tiles whose QK^T has been issued
     int pv_next = 0;  // next tile whose PV is due
     uint64_t *last_bar = nullptr;
@@ -320,8 +329,9 @@ __device__ __forceinline__ void issue_mmas(const Ctx &c)
         const int pb = t & 1;
         tc::fence_after_sync();
         const uint64_t pdb = pb ? pd1 : pd0, vmb = pb ? vm1 : vm0;
-        tc::mma_f16(c.tmem + kColO, pdb, vmb, kIdescPV, t > 0 ? 1u : 0u);
-        tc::mma_f16(c.tmem + kColO, pdb + 16, vmb + 1024, kIdescPV, 1u);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+            tc::mma_f16(c.tmem + kColO, pdb + 16 * k, vmb + 512 * k, kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(&M.pv_done[pb]);
         last_bar = &M.pv_done[pb];
         last_par = (t >> 1) & 1;
@@ -349,16 +359,16 @@ __device__ __forceinline__ void issue_mmas(const Ctx &c)
             break;
         }
         tc::fence_after_sync();
-        const uint32_t d = c.tmem + 32 * vb;
+        const uint32_t d = c.tmem + kColS + kTile * vb;
         const uint64_t vdb = vb ? vd1 : vd0;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int ks = 8 * g + k;
-                tc::mma_f16(d, qd + 16 * ks, vdb + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+                tc::mma_f16_ta(d, qa + 8 * ks, vdb + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
             }
-            if (g == 3) {
+            if (g == 1) {
                 tc::mma_commit(&M.s_full[vb]);
                 last_bar = &M.s_full[vb];
                 last_par = (t >> 1) & 1;
@@ -381,115 +391,164 @@ __device__ __forceinline__ void issue_mmas(const Ctx &c)
     if (last_bar) tc::mbar_wait(last_bar, last_par);
 }
 
-// ---- softmax rows (warps 0-3, thread = tensor-memory lane = query row) ----------------
+// ---- softmax (warps 0-7) --------------------------------------------------------------
+// Thread (row r = 32(w%4) + lane, key half kh = w/4) holds the row's scores of
+// keys 32kh..32kh+31 of each tile and O columns 128kh..128kh+127.  A failed
+// wait clears `ok`; the loop leaves only at a reduction over all 256 threads,
+// so every softmax thread meets every named barrier the same number of times.
 template <bool FP8>
 __device__ __forceinline__ void softmax_rows(const Ctx &c)
 {
     AttnMisc &M = *c.M;
     const UnitDev &U = *c.U;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int slot_layer = tid >> 4, head = tid & 15;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, kh = warp >> 2;
+    const int r = 32 * quad + lane;
+    const int slot_layer = r >> 4, head = r & 15;
     const bool active = slot_layer < U.n_layers;
-    const uint32_t lane_base = (uint32_t)(32 * warp);
-    float m_used = -INFINITY, l_sum = 0.0f;
+    const uint32_t lane_base = (uint32_t)(32 * quad);
+    const uint32_t peer = (uint32_t)(c.half ^ 1);
+    const uint32_t xin_peer = tc::mapa(tc::smem_u32(c.Xin), peer);
+    const uint32_t xfull_peer = tc::mapa(tc::smem_u32(&M.x_full), peer);
+    const uint32_t xfree_peer = tc::mapa(tc::smem_u32(&M.x_free), peer);
+
+    // this row's queries (channels 128kh..+127 of the half) into tensor memory as fp16 pairs
+    {
+        const float *q = active ? c.P->entries[U.entry[slot_layer]].q + ((int64_t)c.b * kHeads + head) * kDim +
+                                      c.half * kHalf + 128 * kh
+                                : nullptr;
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 a = q ? __ldg(reinterpret_cast<const float4 *>(q + 64 * cc + 4 * i))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                h[2 * i] = __uint_as_float(pack_h2(__floats2half2_rn(a.x, a.y)));
+                h[2 * i + 1] = __uint_as_float(pack_h2(__floats2half2_rn(a.z, a.w)));
+            }
+            tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColQ + 64 * kh + 32 * cc), h);
+        }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&M.q_bar);
+    }
+
+    float m_used = -INFINITY, l_half = 0.0f;
     bool ok = true;
     for (int t = 0; t < c.n_tiles; ++t) {
         const int vb = t & 1;
-        bool w_ok = tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) && tc::mbar_wait(&M.s_full[vb], (t >> 1) & 1);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
-            ok = false;
-            break;
-        }
+        ok = ok && tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) && tc::mbar_wait(&M.s_full[vb], (t >> 1) & 1);
         tc::fence_after_sync();
-        float s[kTile];
-        tc::tmem_ld32(tc::taddr(c.tmem, lane_base, 32 * vb), s);
+        float s[32];
+        tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColS + kTile * vb + 32 * kh), s);
         tc::fence_before_sync();
         tc::mbar_arrive(&M.s_free[vb]);
-        const uint32_t vmask = M.vmask[vb];
-        float mt = -INFINITY;
+        // our partial scores to the peer, once it has consumed the previous ones
+        ok = ok && (t < 1 || tc::mbar_wait_cluster(&M.x_free, (t - 1) & 1));
 #pragma unroll
-        for (int j = 0; j < kTile; ++j) {
-            const float z = FP8 ? s[j] * M.mscale[vb][j] : s[j];
-            s[j] = ((vmask >> j) & 1u) ? z : -INFINITY;
-            mt = fmaxf(mt, s[j]);
+        for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4 *>(c.Xout + x_off(r, 8 * kh + k)) =
+                make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+        tc::fence_async_smem();
+        if (bar_any(kBarSoft, kSoftThreads, !ok)) break;
+        if (tid == 0) tc::bulk_s2peer(xin_peer, c.Xout, kXBytes, xfull_peer);
+        // full scores = ours + the peer's, masked and scaled; this key half's tile max
+        ok = tc::mbar_wait_cluster(&M.x_full, t & 1);
+        if (tid == 0 && ok && t + 1 < c.n_tiles) tc::mbar_expect_tx(&M.x_full, kXBytes);  // arm the next tile
+        const uint32_t vm = M.vmask[vb][kh];
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 v = *reinterpret_cast<const float4 *>(c.Xin + x_off(r, 8 * kh + k));
+            const float pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * k + i;
+                const float z = s[j] + pv[i];
+                const float zs = FP8 ? z * M.mscale[vb][32 * kh + j] : z;
+                s[j] = ((vm >> j) & 1u) ? zs : -INFINITY;
+                mx[i] = fmaxf(mx[i], s[j]);
+            }
         }
-        const float m_new = active ? fmaxf(m_used, mt) : m_used;
-        // lazy rescale, warp-uniform: every lane of the warp joins the tensor-memory traffic
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        M.xmax[vb][kh][r] = mt;
+        if (bar_any(kBarSoft, kSoftThreads, !ok)) break;  // also: every Xin read and xmax write is done
+        if (tid == 32) tc::mbar_arrive_cluster(xfree_peer);  // not the copy issuer: its release would wait on the copy
+        const float m_tile = fmaxf(mt, M.xmax[vb][kh ^ 1][r]);
+        const float m_new = active ? fmaxf(m_used, m_tile) : m_used;
+        // lazy rescale of this warp's O columns, warp-uniform (both key halves decide alike)
         if (__any_sync(0xFFFFFFFFu, active && m_new > m_used + kRescaleGap)) {
             if (t >= 1) {
-                w_ok = tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);  // O is current
-                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
-                    ok = false;
-                    break;
-                }
+                ok = ok && tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);  // O is current
                 tc::fence_after_sync();
                 const float alpha = (active && m_used != -INFINITY) ? __expf(m_used - m_new) : (active ? 0.0f : 1.0f);
 #pragma unroll 1
-                for (int c0 = 0; c0 < 256; c0 += 32) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     float o[32];
-                    tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+                    tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+                    tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
                 }
-                if (active) l_sum *= alpha;
+                if (active) l_half *= alpha;
             }
             if (active) m_used = m_new;
         }
         // P[vb] is free once PV(t-2) has finished
-        w_ok = (t < 2) || tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
-        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
-            ok = false;
-            break;
-        }
+        ok = ok && (t < 2 || tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1));
+        // P = exp(S - m) as fp16, K-major core-matrix layout (8 groups of 8 keys, 1,024 B
+        // per 8-row group); window rows hold raw E4M3 codes, so their scale joins the weight
         const float mb = m_used * kLog2e;
-        float p[kTile];
-        float ls = 0.0f;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < kTile; ++j) {
-            p[j] = (active && s[j] != -INFINITY) ? exp2f(fmaf(s[j], kLog2e, -mb)) : 0.0f;
-            ls += p[j];
+        for (int j = 0; j < 32; ++j) {
+            s[j] = (active && s[j] != -INFINITY) ? exp2f(fmaf(s[j], kLog2e, -mb)) : 0.0f;
+            ls[j & 3] += s[j];
         }
-        l_sum += ls;
-        uint32_t ph[kTile / 2];
+        l_half += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        uint8_t *Pb = c.Ps + vb * kPBytes + (r >> 3) * 1024 + (r & 7) * 16;
 #pragma unroll
-        for (int j = 0; j < kTile; j += 2) {
-            const float a = FP8 ? p[j] * M.mscale[vb][j] : p[j];      // window rows hold raw E4M3 codes:
-            const float d = FP8 ? p[j + 1] * M.mscale[vb][j + 1] : p[j + 1];  // their scale joins the weight
-            ph[j >> 1] = pack_h2(__floats2half2_rn(a, d));
+        for (int g = 0; g < 4; ++g) {
+            uint32_t ph[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 8 * g + 2 * i;
+                const float a = FP8 ? s[j] * M.mscale[vb][32 * kh + j] : s[j];
+                const float d = FP8 ? s[j + 1] * M.mscale[vb][32 * kh + j + 1] : s[j + 1];
+                ph[i] = pack_h2(__floats2half2_rn(a, d));
+            }
+            *reinterpret_cast<uint4 *>(Pb + (4 * kh + g) * 128) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
         }
-        // P row into its K-major core-matrix layout: 4 groups of 8 keys, 512 B per 8-row group
-        uint8_t *Pb = c.Ps + vb * kPBytes;
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-            *reinterpret_cast<uint4 *>(Pb + (tid >> 3) * 512 + g * 128 + (tid & 7) * 16) =
-                make_uint4(ph[4 * g], ph[4 * g + 1], ph[4 * g + 2], ph[4 * g + 3]);
         tc::fence_async_smem();
         tc::fence_before_sync();
         tc::mbar_arrive(&M.p_full[vb]);
     }
-    if (ok && c.n_tiles > 0) {
+    if (c.n_tiles > 0) {
         const int last = c.n_tiles - 1;
-        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait(&M.pv_done[last & 1], (last >> 1) & 1));
+        ok = ok && tc::mbar_wait(&M.pv_done[last & 1], (last >> 1) & 1);
     }
-    if (!ok && (tid & 31) == 0) raise_flag(c.flags, kFlagTimeout);
+    if (!ok) raise_flag(c.flags, kFlagTimeout);
+    // both key halves' sums, then this chunk's partial for the channel half: (m, l, unnormalised O)
+    if (kh == 1) M.lpart[r] = l_half;
+    const bool have = !bar_any(kBarSoft, kSoftThreads, !ok) && c.n_tiles > 0;
     tc::fence_after_sync();
-    // this chunk's partial for its channel half: (m, l, unnormalised O)
-    const bool have = ok && c.n_tiles > 0;
     float *orow = nullptr;
     if (active) {
         const int e = U.entry[slot_layer];
         const EntryDev &E = c.P->entries[e];
         const int part = U.is_window ? E.part_win : c.chunk;
         float *rec = c.P->partials + (((int64_t)e * c.P->batch + c.b) * c.P->max_parts + part) * kPartFloats;
-        const bool any = have && l_sum > 0.0f;
-        rec[c.half * 16 + head] = any ? m_used : -INFINITY;
-        rec[32 + c.half * 16 + head] = any ? l_sum : 0.0f;
-        orow = rec + 64 + head * kDim + c.half * 256;
+        if (kh == 0) {
+            const float l_sum = l_half + M.lpart[r];
+            const bool any = have && l_sum > 0.0f;
+            rec[c.half * 16 + head] = any ? m_used : -INFINITY;
+            rec[32 + c.half * 16 + head] = any ? l_sum : 0.0f;
+        }
+        orow = rec + 64 + head * kDim + c.half * kHalf + 128 * kh;
     }
-    for (int c0 = 0; c0 < 256; c0 += 32) {
+    for (int c0 = 0; c0 < 128; c0 += 32) {
         float o[32];
-        if (have) tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+        if (have) tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
         if (active) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
@@ -500,74 +559,81 @@ __device__ __forceinline__ void softmax_rows(const Ctx &c)
     tc::fence_before_sync();
 }
 
-// ---- merge: the last CTA to finish a (layer, sequence, half) combines its partials ----
-__device__ __forceinline__ void merge_if_last(const Ctx &c)
+// ---- merge: one CTA per (layer, sequence, channel half) combines the partials ----------
+// 256 threads.  The (m, l) of every part are staged in shared memory in one
+// round of independent loads; 16 threads then turn them into per-part weights
+// exp(m_p - max) (one head each), and every thread accumulates 16 output
+// channels of one head over the parts.  A layer with no parts writes zeros.
+struct MergeParams {
+    EntryDev entries[kMaxAttnEntries];
+    int32_t batch, max_parts;
+    const float *partials;  // [entry][B][max_parts][kPartFloats]
+};
+
+__global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__ MergeParams P)
 {
-    AttnMisc &M = *c.M;
-    const UnitDev &U = *c.U;
-    const AttnParams &P = *c.P;
-    const int tid = threadIdx.x;
-    tc::named_sync(2, 128);  // every row of this CTA has written its partial
-    if (tid < U.n_layers) {
-        const int e = U.entry[tid];
-        __threadfence();
-        const uint32_t old = atomicAdd(P.counters + ((int64_t)e * P.batch + c.b) * 2 + c.half, 1u);
-        M.last[tid] = (old + 1 == (uint32_t)P.entries[e].n_parts) ? 1 : 0;
+    __shared__ float m_sh[kMaxParts][kHeads], l_sh[kMaxParts][kHeads];
+    __shared__ float inv_sh[kHeads];
+    const int e = blockIdx.x, b = blockIdx.y, half = blockIdx.z, tid = threadIdx.x;
+    const EntryDev &E = P.entries[e];
+    const int np = min(E.n_parts, kMaxParts);
+    const float *recs = P.partials + ((int64_t)e * P.batch + b) * P.max_parts * kPartFloats;
+    for (int i = tid; i < np * kHeads; i += 256) {
+        const float *rp = recs + (int64_t)(i / kHeads) * kPartFloats;
+        m_sh[i / kHeads][i % kHeads] = __ldcg(rp + half * 16 + i % kHeads);
+        l_sh[i / kHeads][i % kHeads] = __ldcg(rp + 32 + half * 16 + i % kHeads);
     }
-    tc::named_sync(2, 128);
-    for (int j = 0; j < U.n_layers; ++j) {
-        if (!M.last[j]) continue;
-        __threadfence();
-        const int e = U.entry[j];
-        const EntryDev &E = P.entries[e];
-        const float *recs = P.partials + ((int64_t)e * P.batch + c.b) * P.max_parts * kPartFloats;
-        const int h = tid >> 3, c0 = c.half * 256 + (tid & 7) * 32;  // head, 32 output channels
+    __syncthreads();
+    if (tid < kHeads) {
         float mx = -INFINITY;
-        for (int p = 0; p < E.n_parts; ++p) {
-            const float *rp = recs + (int64_t)p * kPartFloats;
-            if (__ldcg(rp + 32 + c.half * 16 + h) > 0.0f) mx = fmaxf(mx, __ldcg(rp + c.half * 16 + h));
-        }
-        float acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+        for (int p = 0; p < np; ++p)
+            if (l_sh[p][tid] > 0.0f) mx = fmaxf(mx, m_sh[p][tid]);
         float ls = 0.0f;
-        for (int p = 0; p < E.n_parts; ++p) {
-            const float *rp = recs + (int64_t)p * kPartFloats;
-            const float lp = __ldcg(rp + 32 + c.half * 16 + h);
-            if (!(lp > 0.0f)) continue;
-            const float wp = __expf(__ldcg(rp + c.half * 16 + h) - mx);
-            ls += wp * lp;
-            const float4 *op = reinterpret_cast<const float4 *>(rp + 64 + h * kDim + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldcg(op + i);
-                acc[4 * i] += wp * v.x;
-                acc[4 * i + 1] += wp * v.y;
-                acc[4 * i + 2] += wp * v.z;
-                acc[4 * i + 3] += wp * v.w;
-            }
+        for (int p = 0; p < np; ++p) {
+            const float wp = l_sh[p][tid] > 0.0f ? __expf(m_sh[p][tid] - mx) : 0.0f;
+            ls += wp * l_sh[p][tid];
+            m_sh[p][tid] = wp;  // m becomes the part's weight
         }
-        const float inv = ls > 0.0f ? 1.0f / ls : 0.0f;
-        float4 *out = reinterpret_cast<float4 *>(E.out + ((int64_t)c.b * kHeads + h) * kDim + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            out[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
-        if (c.half == 0 && E.lse && (tid & 7) == 0)
-            E.lse[(int64_t)c.b * kHeads + h] = ls > 0.0f ? mx + logf(ls) : -INFINITY;
+        inv_sh[tid] = ls > 0.0f ? 1.0f / ls : 0.0f;
+        if (half == 0 && E.lse) E.lse[(int64_t)b * kHeads + tid] = ls > 0.0f ? mx + logf(ls) : -INFINITY;
     }
+    __syncthreads();
+    const int h = tid >> 4, c0 = half * kHalf + (tid & 15) * 16;
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll 4
+    for (int p = 0; p < np; ++p) {
+        const float wp = m_sh[p][h];
+        const float4 *op = reinterpret_cast<const float4 *>(recs + (int64_t)p * kPartFloats + 64 + h * kDim + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = __ldcg(op + i);
+            acc[4 * i] += wp * v.x;
+            acc[4 * i + 1] += wp * v.y;
+            acc[4 * i + 2] += wp * v.z;
+            acc[4 * i + 3] += wp * v.w;
+        }
+    }
+    const float inv = inv_sh[h];
+    float4 *out = reinterpret_cast<float4 *>(E.out + ((int64_t)b * kHeads + h) * kDim + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams P, int *flags)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnParams P, int *flags)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Ctx c;
     c.P = &P;
     c.M = reinterpret_cast<AttnMisc *>(smem + kOffMisc);
-    c.Qs = smem;
     c.Vs = smem + kOffV;
     c.Ps = smem + kOffP;
-    c.sidx = reinterpret_cast<int32_t *>(smem + kOffIdx);
+    c.Xin = smem + kOffXin;
+    c.Xout = smem + kOffXout;
     c.flags = flags;
     c.b = blockIdx.y;
     int u = 0;
@@ -575,11 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     c.U = &P.units[u];
     const int local = (int)blockIdx.x - c.U->cta_begin;
     c.chunk = local >> 1;
-    c.half = local & 1;
+    c.half = (int)tc::cluster_rank();  // = local & 1: a pair is one cluster
     c.L = max(0, __ldg(P.seq_lens + c.b));
     c.W = P.window;
-    c.fp8 = c.U->is_window != 0;
-    if (c.fp8) {
+    const bool fp8 = c.U->is_window != 0;
+    if (fp8) {
         c.row0 = 0;
         c.n_rows = c.W;
     } else {
@@ -590,43 +656,44 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     AttnMisc &M = *c.M;
 
     if (tid == 0) {
-        tc::mbar_init(&M.q_bar, 1);
+        tc::mbar_init(&M.q_bar, kSoftThreads);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&M.full_v[i], kProducers);
             tc::mbar_init(&M.s_full[i], 1);
-            tc::mbar_init(&M.s_free[i], 128);
+            tc::mbar_init(&M.s_free[i], kSoftThreads);
             tc::mbar_init(&M.pv_done[i], 1);
-            tc::mbar_init(&M.p_full[i], 128);
+            tc::mbar_init(&M.p_full[i], kSoftThreads);
         }
+        tc::mbar_init(&M.x_full, 1);
+        tc::mbar_init(&M.x_free, 1);
         tc::mbar_init_fence();
+        if (c.n_tiles > 0) tc::mbar_expect_tx(&M.x_full, kXBytes);  // armed for the first tile's partial
     }
     if (warp == kMmaWarp) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
     tc::fence_before_sync();
-    __syncthreads();
+    tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc::fence_after_sync();
     c.tmem = M.tmem_slot;
 
-    if (warp >= 4 && warp < kMmaWarp) {
-        if (c.fp8) produce<true>(c);
+    if (warp < 8) {
+        if (fp8) softmax_rows<true>(c);
+        else softmax_rows<false>(c);
+    } else if (warp < kMmaWarp) {
+        if (fp8) produce<true>(c);
         else produce<false>(c);
-    } else if (warp == kMmaWarp) {
+    } else {
         if (lane == 0) issue_mmas(c);
         __syncwarp();
-    } else {
-        if (c.fp8) softmax_rows<true>(c);
-        else softmax_rows<false>(c);
     }
     tc::fence_before_sync();
-    __syncthreads();
+    tc::cluster_sync();  // no remote shared-memory access after this point
     if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(c.tmem, kTmemCols);
     }
-    if (warp < 4) merge_if_last(c);
 }
 
 }  // namespace
-
 // ---- host planning ---------------------------------------------------------------------
 namespace {
 
@@ -662,35 +729,67 @@ UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
     return up;
 }
 
-// Rows per chunk of a row unit: 256 (8 tiles), doubled (up to the 2,048 rows
-// whose positions a CTA stages) while the grid would exceed 8 waves of one
-// CTA per SM (large batches need no split).
-int rows_per_chunk(int n_row_units, int n_window_units, int batch, int topk)
+// Rows per chunk of a row unit (a multiple of the 64-row tile, at most the
+// 2,048 rows whose positions a CTA stages).  Each candidate is scored by
+// dispatching the pairs in launch order onto 74 pair slots (148 SMs, one CTA
+// per SM), a pair costing, in tile units, its tiles plus a fixed set-up and
+// half a tile per consumer layer (its queries in, its partial out), and by the
+// merge tail, which reads one partial per chunk; the lowest score wins, ties
+// going to longer chunks.
+int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
 {
-    int rpc = 256;
-    auto ctas = [&](int r) {
-        return (int64_t)batch * 2 * ((int64_t)n_row_units * ((topk + r - 1) / r) + n_window_units);
-    };
-    while (rpc < topk && rpc < kMaxChunkRows && ctas(rpc) > 8 * 148) rpc *= 2;
-    return rpc;
+    if (up.row_units.empty() || topk <= 0) return kMaxChunkRows;
+    constexpr int kPairSlots = 74;
+    constexpr double kPairSetup = 1.0, kPerLayer = 0.5, kMergePerPart = 0.02;
+    const int rmax = std::min(kMaxChunkRows, (topk + kTile - 1) / kTile * kTile);
+    int rmin = kTile;  // at most kMaxParts - 1 chunks
+    while (rmin < rmax && (topk + rmin - 1) / rmin > kMaxParts - 1) rmin *= 2;
+    const int win_tiles = (window + kTile - 1) / kTile;
+    size_t max_layers = 1;
+    for (const auto &g : up.row_units) max_layers = std::max(max_layers, g.size());
+    int best = rmax;
+    double best_score = 1e300;
+    for (int r = rmin; r <= rmax; r *= 2) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> slots;
+        for (int i = 0; i < kPairSlots; ++i) slots.push(0.0);
+        double span = 0.0;
+        auto dispatch = [&](double cost) {
+            const double t0 = slots.top();
+            slots.pop();
+            slots.push(t0 + cost);
+            span = std::max(span, t0 + cost);
+        };
+        const int chunks = (topk + r - 1) / r;
+        for (int b = 0; b < batch; ++b) {
+            for (const auto &g : up.row_units)
+                for (int ch = 0; ch < chunks; ++ch)
+                    dispatch(kPairSetup + kPerLayer * (double)g.size() + (std::min(r, topk - ch * r) + kTile - 1) / kTile);
+            for (size_t u = 0; u < up.window_units.size(); ++u) dispatch(kPairSetup + kPerLayer + win_tiles);
+        }
+        const double score = span + kMergePerPart * (double)(chunks + 1) * (double)max_layers;
+        if (score <= best_score) {
+            best_score = score;
+            best = r;
+        }
+        if (r >= rmax) break;
+    }
+    return best;
 }
 
 struct WsLayout {
-    size_t counters = 0, q16 = 0, partials = 0, total = 0;
-    int rpc = 256, chunks = 0, max_parts = 1;
+    size_t partials = 0, total = 0;
+    int rpc = kMaxChunkRows, chunks = 0, max_parts = 1;
 };
 
 WsLayout ws_layout(const UnitPlan &up, int n_entries, int batch, int topk, int window)
 {
     WsLayout w;
-    w.rpc = rows_per_chunk((int)up.row_units.size(), (int)up.window_units.size(), batch, topk);
+    w.rpc = rows_per_chunk(up, batch, topk, window);
     w.chunks = (topk > 0 && !up.row_units.empty()) ? (topk + w.rpc - 1) / w.rpc : 0;
     w.max_parts = std::max(1, w.chunks + (window > 0 ? 1 : 0));
     auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
-    w.counters = r256((size_t)n_entries * batch * 2 * 4);
-    w.q16 = r256((size_t)n_entries * batch * kQRowsBytes);
     w.partials = r256((size_t)n_entries * batch * w.max_parts * kPartFloats * 4);
-    w.total = w.counters + w.q16 + w.partials;
+    w.total = w.partials;
     return w;
 }
 
@@ -719,10 +818,9 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
     p.rows_per_chunk = wl.rpc;
     p.max_parts = wl.max_parts;
     p.seq_lens = plan.seq_lens;
-    p.counters = reinterpret_cast<uint32_t *>(ws);
-    p.q16 = ws + wl.counters;
-    p.partials = reinterpret_cast<float *>(ws + wl.counters + wl.q16);
+    p.partials = reinterpret_cast<float *>(ws);
     for (int e = 0; e < plan.n_entries; ++e) {
+        p.entries[e].q = plan.entries[e].q;
         p.entries[e].out = plan.entries[e].out;
         p.entries[e].lse = plan.entries[e].lse;
         p.entries[e].n_parts = 0;
@@ -757,21 +855,7 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
     p.n_units = nu;
 
     cudaError_t err = cudaSuccess;
-    // a layer with neither selected rows nor a window attends over nothing
-    for (int e = 0; e < plan.n_entries && err == cudaSuccess; ++e)
-        if (p.entries[e].n_parts == 0)
-            err = cudaMemsetAsync(plan.entries[e].out, 0, (size_t)plan.batch * kHeads * kDim * 4, stream);
-    if (err == cudaSuccess) err = cudaMemsetAsync(ws, 0, wl.counters, stream);
-    if (err == cudaSuccess && cta > 0) {
-        QList qs;
-        std::memset(&qs, 0, sizeof(qs));
-        for (int e = 0; e < plan.n_entries; ++e) qs.q[e] = plan.entries[e].q;
-        pack_q_kernel<<<dim3((unsigned)plan.n_entries, (unsigned)plan.batch), 256, 0, stream>>>(
-            qs, const_cast<uint8_t *>(p.q16), plan.batch);
-        count_launches(1);
-        err = cudaGetLastError();
-    }
-    if (err == cudaSuccess && cta > 0) {
+    if (cta > 0) {
         const size_t smem = kOffMisc + sizeof(AttnMisc);
         int dev = 0;
         err = cudaGetDevice(&dev);
@@ -787,6 +871,18 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
         }
     }
     if (err == cudaSuccess && mid_event) err = record_event(mid_event, stream);
+    // merge (a layer with neither selected rows nor a window gets zeros)
+    if (err == cudaSuccess) {
+        MergeParams mp;
+        std::memset(&mp, 0, sizeof(mp));
+        std::memcpy(mp.entries, p.entries, sizeof(mp.entries));
+        mp.batch = plan.batch;
+        mp.max_parts = wl.max_parts;
+        mp.partials = p.partials;
+        attn_merge_kernel<<<dim3((unsigned)plan.n_entries, (unsigned)plan.batch, 2u), 256, 0, stream>>>(mp);
+        count_launches(1);
+        err = cudaGetLastError();
+    }
     return err;
 }
 

@@ -43,7 +43,6 @@ namespace {
 constexpr int kScanWarps = 8;
 constexpr int kScanKeys = 1024;                 // candidates per scan CTA
 constexpr int kScanTiles = kScanKeys / kIdxTile;  // 16 key tiles
-constexpr int kSelCluster = 8;
 constexpr int kSelThreads = 512;
 constexpr uint32_t kWaitLimit = 1u << 24;       // mbarrier polls before giving up
 
@@ -157,10 +156,11 @@ struct __align__(128) ScanSmem {
     __half qpre[2][kIdxHeads][kIdxDim];
     float wq[2][kIdxHeads];
     int32_t tile_ok[kScanTiles];
+    float sk_lut[256];  // E4M3 code -> value
     uint64_t bar;
 };
 
-__global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_constant__ ScanBatch sb,
+__global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_constant__ ScanBatch sb,
                                                                  SelectBufs bufs, const int32_t *seq_lens,
                                                                  int batch, int max_len, int *flags)
 {
@@ -210,30 +210,29 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
     }
 
     for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&S.hist[0][0])[i] = 0u;
-    // quantise the queries (FP4 rule) and pre-scale: qpre = scale * E2M1(code), exact in fp16
-    if (tid < 32) {
-        const int qi = tid >> 4, h = (tid >> 2) & 3, blk = tid & 3;
-        float v[16];
-        if (qi < job.n_q) {
-            const float *src = job.q_idx[qi] + ((int64_t)b * kIdxHeads + h) * kIdxDim + blk * 16;
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v[i] = __ldg(src + i);
-                amax = fmaxf(amax, fabsf(v[i]));
-            }
-            const float s = e4m3_value(e4m3_code(__fdiv_rn(amax, 6.0f)));
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float e = (s != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v[i], s))] : 0.0f;
-                S.qpre[qi][h][blk * 16 + i] = __float2half_rn(e * s);
-            }
-            if (blk == 0) S.wq[qi][h] = __ldg(job.w[qi] + (int64_t)b * kIdxHeads + h);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) S.qpre[qi][h][blk * 16 + i] = __float2half_rn(0.0f);
-            if (blk == 0) S.wq[qi][h] = 0.0f;
+    S.sk_lut[tid] = e4m3_value((uint32_t)tid);  // 256 threads
+    // quantise the queries (FP4 rule) and pre-scale: qpre = scale * E2M1(code), exact in fp16.
+    // 8 threads per 16-value block, two values each; the block max by shuffles.
+    {
+        const int bi = tid >> 3, pr = tid & 7;  // block (query, head, 16 channels), pair in block
+        const int qi = bi >> 4, h = (bi >> 2) & 3, blk = bi & 3;
+        const bool have = qi < job.n_q;
+        float v0 = 0.0f, v1 = 0.0f;
+        if (have) {
+            const float *src = job.q_idx[qi] + ((int64_t)b * kIdxHeads + h) * kIdxDim + blk * 16 + 2 * pr;
+            v0 = __ldg(src);
+            v1 = __ldg(src + 1);
         }
+        float amax = fmaxf(fabsf(v0), fabsf(v1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        const float sq = have ? e4m3_value(e4m3_code(__fdiv_rn(amax, 6.0f))) : 0.0f;
+        const float e0 = (sq != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v0, sq))] : 0.0f;
+        const float e1 = (sq != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v1, sq))] : 0.0f;
+        S.qpre[qi][h][blk * 16 + 2 * pr] = __float2half_rn(e0 * sq);
+        S.qpre[qi][h][blk * 16 + 2 * pr + 1] = __float2half_rn(e1 * sq);
+        if (blk == 0 && pr == 0) S.wq[qi][h] = have ? __ldg(job.w[qi] + (int64_t)b * kIdxHeads + h) : 0.0f;
     }
     __syncthreads();
 
@@ -268,84 +267,69 @@ __global__ void __launch_bounds__(kScanWarps * 32) scan_kernel(const __grid_cons
         }
     }
 
-    for (int grp = warp; grp < kScanKeys / 16; grp += kScanWarps) {
-        const int64_t c0 = base + grp * 16;
-        if (c0 >= n_cand) break;
-        const int64_t cA = c0 + g, cB = c0 + g + 8;
-        KeyLoad kA, kB;
-        if (direct) {
-            const int ti = grp >> 2;  // 4 groups of 16 keys per 64-key tile
-            const bool ok = have_tiles && S.tile_ok[ti];
-            const int r0 = (grp & 3) * 16;
-            kA = key_from_tile(S.tiles[ti], r0 + g, t);
-            kB = key_from_tile(S.tiles[ti], r0 + g + 8, t);
-            kA.ok = ok && cA < n_cand;
-            kB.ok = ok && cB < n_cand;
-            if (!kA.ok) kA.w[0] = kA.w[1] = kA.w[2] = kA.w[3] = kA.sc = 0u;
-            if (!kB.ok) kB.w[0] = kB.w[1] = kB.w[2] = kB.w[3] = kB.sc = 0u;
-        } else {
-            int64_t pA = -1, pB = -1;
-            if (cA < n_cand) pA = (int64_t)__ldg(pool + cA);
-            if (cB < n_cand) pB = (int64_t)__ldg(pool + cB);
-            if (pA >= L) pA = -1;
-            if (pB >= L) pB = -1;
-            kA = key_from_global(job.keys, b, pA, t, flags);
-            kB = key_from_global(job.keys, b, pB, t, flags);
-        }
-
-        float d[4][4];
+    // Each warp scores two 16-key groups per step (32 keys, 8 MMAs), so the two
+    // groups' load -> convert -> MMA -> epilogue chains overlap.
+    const bool scoring = finisher && my_q < job.n_q;
+#pragma unroll 1
+    for (int gA = warp; gA < kScanKeys / 16; gA += 2 * kScanWarps) {
+        KeyLoad k[4];
+        int64_t cc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t uA = (kA.w[j] >> (16 * (t & 1))) & 0xFFFFu;
-            const uint32_t uB = (kB.w[j] >> (16 * (t & 1))) & 0xFFFFu;
-            mma16816(d[j], e2m1x2_half2_bits(uA & 0xFFu), e2m1x2_half2_bits(uB & 0xFFu),
-                     e2m1x2_half2_bits(uA >> 8), e2m1x2_half2_bits(uB >> 8), bfrag[j][0], bfrag[j][1]);
+        for (int i = 0; i < 4; ++i) {
+            const int grp = gA + kScanWarps * (i >> 1);
+            cc[i] = base + grp * 16 + g + 8 * (i & 1);
+            if (direct) {
+                const int ti = grp >> 2;  // 4 groups of 16 keys per 64-key tile
+                k[i] = key_from_tile(S.tiles[ti], (grp & 3) * 16 + g + 8 * (i & 1), t);
+                k[i].ok = have_tiles && S.tile_ok[ti] && cc[i] < n_cand;
+                if (!k[i].ok) k[i].w[0] = k[i].w[1] = k[i].w[2] = k[i].w[3] = k[i].sc = 0u;
+            } else {
+                int64_t pos = -1;
+                if (cc[i] < n_cand) pos = (int64_t)__ldg(pool + cc[i]);
+                if (pos >= L) pos = -1;
+                k[i] = key_from_global(job.keys, b, pos, t, flags);
+            }
         }
-        // s = t0 + t1 + t2 + t3 in order; t_j = sk_j * (sq_j * P_j) is exact, so fma == add
-        float sA0, sA1, sB0, sB1;
-        {
-            float sk = e4m3_value(kA.sc & 0xFFu);
-            sA0 = sk * d[0][0];
-            sA1 = sk * d[0][1];
-            sk = e4m3_value(kB.sc & 0xFFu);
-            sB0 = sk * d[0][2];
-            sB1 = sk * d[0][3];
+        float d[2][4][4];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t uA = (k[2 * h2].w[j] >> (16 * (t & 1))) & 0xFFFFu;
+                const uint32_t uB = (k[2 * h2 + 1].w[j] >> (16 * (t & 1))) & 0xFFFFu;
+                mma16816(d[h2][j], e2m1x2_half2_bits(uA & 0xFFu), e2m1x2_half2_bits(uB & 0xFFu),
+                         e2m1x2_half2_bits(uA >> 8), e2m1x2_half2_bits(uB >> 8), bfrag[j][0], bfrag[j][1]);
+            }
+        float sc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // s = t0 + t1 + t2 + t3 in order; t_j = sk_j * (sq_j * P_j) is exact, so fma == add
+            const float *dd = &d[i >> 1][0][0];
+            const int e0 = 2 * (i & 1);  // accumulator pair of this key
+            float s0 = S.sk_lut[k[i].sc & 0xFFu] * dd[e0];
+            float s1 = S.sk_lut[k[i].sc & 0xFFu] * dd[e0 + 1];
 #pragma unroll
             for (int j = 1; j < 4; ++j) {
-                sk = e4m3_value((kA.sc >> (8 * j)) & 0xFFu);
-                sA0 = __fmaf_rn(sk, d[j][0], sA0);
-                sA1 = __fmaf_rn(sk, d[j][1], sA1);
-                sk = e4m3_value((kB.sc >> (8 * j)) & 0xFFu);
-                sB0 = __fmaf_rn(sk, d[j][2], sB0);
-                sB1 = __fmaf_rn(sk, d[j][3], sB1);
+                const float skj = S.sk_lut[(k[i].sc >> (8 * j)) & 0xFFu];
+                s0 = __fmaf_rn(skj, dd[4 * j + e0], s0);
+                s1 = __fmaf_rn(skj, dd[4 * j + e0 + 1], s1);
             }
+            const float r0 = s0 > 0.0f ? s0 : 0.0f, r1 = s1 > 0.0f ? s1 : 0.0f;
+            // heads 0,1 live on even t, heads 2,3 on odd t: chain w0*r0 -> +w1 r1 -> +w2 r2 -> +w3 r3
+            float acc = __fmaf_rn(w1, r1, __fmul_rn(w0, r0));
+            acc = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+            float v = __fmaf_rn(w3, r1, __fmaf_rn(w2, r0, acc));
+            sc[i] = (v == 0.0f) ? 0.0f : v;
         }
-        const float rA0 = sA0 > 0.0f ? sA0 : 0.0f, rA1 = sA1 > 0.0f ? sA1 : 0.0f;
-        const float rB0 = sB0 > 0.0f ? sB0 : 0.0f, rB1 = sB1 > 0.0f ? sB1 : 0.0f;
-        // heads 0,1 live on even t, heads 2,3 on odd t: chain w0*r0 -> +w1 r1 -> +w2 r2 -> +w3 r3
-        float accA = __fmaf_rn(w1, rA1, __fmul_rn(w0, rA0));
-        float accB = __fmaf_rn(w1, rB1, __fmul_rn(w0, rB0));
-        accA = __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-        accB = __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
-        if (finisher && my_q < job.n_q) {
-            float scA = __fmaf_rn(w3, rA1, __fmaf_rn(w2, rA0, accA));
-            float scB = __fmaf_rn(w3, rB1, __fmaf_rn(w2, rB0, accB));
-            if (scA == 0.0f) scA = 0.0f;
-            if (scB == 0.0f) scB = 0.0f;
-            if (cA < n_cand) {
-                const uint32_t key = kA.ok ? score_key(scA) : 0u;
-                key_out[cA] = key;
-                if (kA.ok) {
+        if (scoring) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (cc[i] >= n_cand) continue;
+                const uint32_t key = k[i].ok ? score_key(sc[i]) : 0u;
+                key_out[cc[i]] = key;
+                if (k[i].ok) {
                     atomicAdd(&S.hist[my_q][key >> (32 - kHistBits)], 1u);
-                    if (score_out) score_out[cA] = scA;
-                }
-            }
-            if (cB < n_cand) {
-                const uint32_t key = kB.ok ? score_key(scB) : 0u;
-                key_out[cB] = key;
-                if (kB.ok) {
-                    atomicAdd(&S.hist[my_q][key >> (32 - kHistBits)], 1u);
-                    if (score_out) score_out[cB] = scB;
+                    if (score_out) score_out[cc[i]] = sc[i];
                 }
             }
         }
@@ -469,13 +453,14 @@ __device__ __forceinline__ void for_range(const uint32_t *src, int64_t base, int
     }
 }
 
-// ---- select (one cluster of kSelCluster CTAs per row and target) ---------------
-// The row's candidates are split into kSelCluster contiguous slices (one per
+// ---- select (one cluster of CS CTAs per row and target) -------------------------
+// The row's candidates are split into CS contiguous slices (one per
 // CTA) and each slice into kSelWarps contiguous warp ranges, so position
 // order is (CTA rank, warp, lane).  Dynamic shared memory holds the CTA's
 // slice of keys when it fits (staged); otherwise the passes read it from
 // global memory (L2).
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+template <int CS>
+__global__ void __launch_bounds__(kSelThreads)
     select_kernel(SelectPlan plan, int max_len, int64_t stage_cap, int *flags)
 {
     __shared__ SelSmem S;
@@ -495,7 +480,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     const uint32_t *keys = plan.bufs.keys + row * plan.bufs.cand_cap;
     const int32_t *pool = R.pool ? R.pool + (int64_t)b * R.pool_len : nullptr;
     // slices of a multiple of 32 keys, so each starts 128-B aligned
-    const int64_t chunk = ceil_div(ceil_div(n_cand, kSelCluster), 32) * 32;
+    const int64_t chunk = ceil_div(ceil_div(n_cand, CS), 32) * 32;
     const int64_t s0 = min(n_cand, (int64_t)rank * chunk), s1 = min(n_cand, s0 + chunk);
     const int64_t span = ceil_div(s1 - s0, kSelWarps);
     const int64_t r0 = min(s1, s0 + warp * span), r1 = min(s1, r0 + span);
@@ -537,7 +522,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
         for (int i = tid; i < 2048; i += kSelThreads) {
             uint32_t v = 0;
 #pragma unroll
-            for (int r = 0; r < kSelCluster; ++r) v += cluster.map_shared_rank(S.h1, r)[i];
+            for (int r = 0; r < CS; ++r) v += cluster.map_shared_rank(S.h1, r)[i];
             S.red[i] = v;
         }
         __syncthreads();
@@ -552,7 +537,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
         for (int i = tid; i < 1024; i += kSelThreads) {
             uint32_t v = 0;
 #pragma unroll
-            for (int r = 0; r < kSelCluster; ++r) v += cluster.map_shared_rank(S.h2, r)[i];
+            for (int r = 0; r < CS; ++r) v += cluster.map_shared_rank(S.h2, r)[i];
             S.red[i] = v;
         }
         __syncthreads();
@@ -587,7 +572,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
     uint32_t tie_before = 0, sel_before = 0, total = 0;
     {
         uint32_t tb = 0;
-        for (int r = 0; r < kSelCluster; ++r) {
+        for (int r = 0; r < CS; ++r) {
             const uint32_t *c = cluster.map_shared_rank(S.cnt, r);
             const uint32_t ab = c[0], ti = c[1];
             const uint32_t q = (ties_needed > tb) ? min(ties_needed - tb, ti) : 0u;
@@ -628,7 +613,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
         written += __popc(sm);
         ties_seen += __popc(tm);
     });
-    for (uint32_t i = total + rank * kSelThreads + tid; i < K; i += kSelCluster * kSelThreads) out[i] = -1;
+    for (uint32_t i = total + rank * kSelThreads + tid; i < K; i += CS * kSelThreads) out[i] = -1;
 }
 
 }  // namespace
@@ -689,28 +674,48 @@ cudaError_t launch_scan(const ScanJob *jobs, int n_jobs, const SelectPlan &plan,
     return cudaSuccess;
 }
 
+// Launches select_kernel<CS> as clusters of CS CTAs along x.
+template <int CS>
+cudaError_t launch_select_cs(const SelectPlan &plan, int64_t cap, size_t smem, int *flags, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)CS, (unsigned)(plan.n_row_blocks * plan.batch), 2u);
+    cfg.blockDim = dim3(kSelThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_kernel<CS>, plan, plan.max_len, cap, flags);
+}
+
+// Stages up to 160 KB of keys per CTA.  Eight CTAs per row: 16-CTA clusters
+// were measured slower (the cross-rank histogram sums grow with the cluster).
 cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cudaStream_t stream,
                           cudaEvent_t mid_event)
 {
     (void)mid_event;
-    // stage each CTA's slice of keys in shared memory when it fits in 160 KB
+    constexpr int kCS = 8;
     constexpr int64_t kStageMax = 40960;
-    const int64_t slice = ceil_div(ceil_div(max_cand > 0 ? max_cand : 1, kSelCluster), 32) * 32;
-    const int64_t cap = slice <= kStageMax ? slice : 0;
-    const size_t smem = (size_t)cap * 4;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static bool attr_set[64] = {};
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kStageMax * 4));
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(select_kernel<kCS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kStageMax * 4));
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
+        attr_set[dev] = true;
     }
-    dim3 grid((unsigned)kSelCluster, (unsigned)(plan.n_row_blocks * plan.batch), 2u);
-    select_kernel<<<grid, kSelThreads, smem, stream>>>(plan, plan.max_len, cap, flags);
+    const int64_t slice = ceil_div(ceil_div(max_cand > 0 ? max_cand : 1, kCS), 32) * 32;
+    const int64_t cap = slice <= kStageMax ? slice : 0;
+    e = launch_select_cs<kCS>(plan, cap, (size_t)cap * 4, flags, stream);
     count_launches(1);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -114,8 +114,8 @@ struct AttnPlan {
     size_t workspace_bytes;
 };
 
-// Workspace of one launch_attention call: per-(layer, sequence, half) merge
-// counters (zeroed by the launch), fp16 query rows, and split partials.
+// Workspace of one launch_attention call: the split partials (per layer,
+// sequence and part: running max and sum per head and half, unnormalised output).
 size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window);
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
                              cudaEvent_t mid_event);

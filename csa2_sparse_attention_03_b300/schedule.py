@@ -83,6 +83,7 @@ class DecodeStep:
             self.swa[l] = ring
             self._build_swa(l, ring, append)
         self._alloc_layers()
+        self._pack_arenas()
         self.descs = self._descs()
         self.arr = layer_array(self.descs)
         self.ws_bytes = csa2_decode_layers_workspace(self.descs, B, Lmax, self.topk, self.pool_len, self.window)
@@ -170,6 +171,35 @@ class DecodeStep:
                 if ly.mode == synth.FULL and self.pool_len:
                     self.pool[l] = torch.full((B, self.pool_len), -7, dtype=torch.int32, device=dev)
 
+    def _pack_arenas(self):
+        """Place the per-step inputs (queries, indexer queries and weights, the
+        appended rows) in one contiguous device buffer and the per-step outputs
+        (out, lse, indices, pools) in another, so a caller moves each direction
+        with a single copy."""
+        import torch
+
+        def pack(groups):
+            tensors = [t for g in groups for t in g.values()]
+            offs, total = [], 0
+            for t in tensors:
+                offs.append(total)
+                total += (t.numel() * t.element_size() + 255) // 256 * 256
+            arena = torch.zeros(max(total, 256), dtype=torch.uint8, device=self.device)
+            k = 0
+            for g in groups:
+                for key in list(g.keys()):
+                    t = g[key]
+                    n = t.numel() * t.element_size()
+                    view = arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+                    view.copy_(t)
+                    g[key] = view
+                    k += 1
+            return arena
+
+        self.arena_in = pack([self.q, self.q_idx, self.wts, self.new_rows])
+        self.arena_out = pack([self.out, self.lse, self.idx, self.pool])
+        torch.cuda.synchronize(self.device)
+
     def _descs(self):
         descs = []
         P = lambda t: t.data_ptr() if t is not None else None
@@ -203,11 +233,10 @@ class DecodeStep:
 
     # ---- inputs/outputs moved per step in the end-to-end measurement ----
     def step_inputs(self):
-        """Tensors a caller supplies per decode step (queries, indexer queries,
-        weights and the appended token rows)."""
-        ts = list(self.q.values()) + list(self.q_idx.values()) + list(self.wts.values())
-        ts += list(self.new_rows.values())
-        return ts
+        """What a caller supplies per decode step (queries, indexer queries,
+        weights and the appended token rows), as one contiguous buffer."""
+        return [self.arena_in]
 
     def step_outputs(self):
-        return list(self.out.values()) + list(self.lse.values()) + list(self.idx.values())
+        """What a step returns (out, lse, indices, pools), as one contiguous buffer."""
+        return [self.arena_out]
