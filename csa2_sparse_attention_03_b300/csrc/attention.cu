@@ -13,36 +13,34 @@
 // so a row is read and dequantised once for all of them and QK^T and PV are
 // 128-row tensor-core products.  Each layer's own window rows form a *window
 // unit*.  A *CTA pair* (a cluster of two) takes one (unit, chunk of rows,
-// sequence); CTA h of the pair owns channels 256h..256h+255 of the queries,
-// of every gathered row and of the output.  QK^T is split along channels:
-// each CTA forms the partial scores of its half, the two swap partials with
-// one bulk shared-memory copy each way and both add them (fp32 addition
-// commutes, so both hold bit-identical scores and run the identical softmax).
-// PV then touches only the CTA's own channels.  Each CTA leaves a partial
-// (running max, sum, unnormalised output of its half) per consumer layer; a
-// second kernel merges each (layer, sequence, half)'s partials in parallel.
+// sequence) and splits the work by stage, not by data:
+//   rank 0 (scores)  S = Q K^T over all 512 channels (queries in tensor
+//                    memory, the A operand), fp32 online softmax, and P as
+//                    fp16 -- the PV operand's own precision -- sent to rank 1
+//                    with one bulk shared-memory copy per 64-row tile,
+//                    together with each row's rescale factor;
+//   rank 1 (output)  applies the rescale factors to O, then O += P V over all
+//                    512 channels (O is the whole of its tensor memory).
+// The hand-off runs one way, so the copy overlaps the next tile's scores; the
+// PV commit is multicast to both CTAs' barriers, which tells rank 0 that its
+// P buffer is free again.  Each pair leaves a partial (running max and sum
+// from rank 0, unnormalised output from rank 1) per consumer layer; a second
+// kernel merges each layer's partials.
 //
-// Tensor memory (512 columns): the 128 query rows of the CTA's half as fp16
-// pairs (128 columns, the A operand of QK^T), S double-buffered (2 x 64), and
-// O (256 columns).
-//
-// One CTA, 13 warps:
-//   warps 0-7  softmax: warp w serves query rows 32(w%4)..+31 (its tensor-
-//              memory lanes) and keys 32(w/4)..+31 of each 64-row tile; it
-//              first writes its rows' queries into tensor memory;
-//   warps 8-11 producers: per 64-row tile each thread owns one row and half
-//              of the CTA's channels; it loads the next tile's bytes into
-//              registers while it dequantises the current one (E2M1 x E4M3
-//              and E4M3 are exact in fp16) into the core-matrix layout;
-//   warp 12    tensor-memory allocation and tcgen05.mma issue: S[b] = Q_h V_h^T
-//              (M 128, N 64, K 256; A from tensor memory), then O_h += P V_h
-//              (M 128, N 256, K 64), O_h resident in tensor memory.
-// V, S and P are double-buffered, so the softmax of tile t+1 does not wait
-// for PV(t) unless O must be rescaled (lazy: only when a row's running max
-// grows by more than e^8).  Every hand-off is an mbarrier with a bounded wait
-// (a wait that gives up raises the timeout flag and the CTA drains); both
-// CTAs of a pair meet at a cluster barrier before either exits, so neither
-// touches the shared memory of a CTA that has finished.
+// One CTA, 17 warps:
+//   warps 8-15  producers (both ranks): per 64-row tile each thread owns one
+//               row and a quarter of its 512 channels, dequantises (E2M1 x
+//               E4M3 and E4M3 are exact in fp16) into the core-matrix layout;
+//   warp 16     tcgen05.mma issue: rank 0 QK^T (M 128, N 64, K 512), rank 1
+//               PV (M 128, N 2 x 256, K 64);
+//   warps 0-7   rank 0 softmax: warp w serves query rows 32(w%4)..+31 (its
+//               tensor-memory lanes) and keys 32(w/4)..+31 of each tile;
+//   warps 0-3   rank 1: O rescale when rank 0 asks for it, and the final
+//               read-out of O.
+// Tiles, S and P are double-buffered.  Every hand-off is an mbarrier with a
+// bounded wait (a wait that gives up raises the timeout flag and the CTA
+// drains); both CTAs of a pair meet at a cluster barrier before either exits,
+// so neither touches the shared memory of a CTA that has finished.
 #include <algorithm>
 #include <cstring>
 #include <queue>
@@ -56,43 +54,59 @@ namespace csa2 {
 namespace {
 
 constexpr int kTile = 64;                  // rows per tile
-constexpr int kHalf = 256;                 // channels per CTA of a pair
-constexpr int kSoftThreads = 256;          // warps 0-7
-constexpr int kProducers = 128;            // warps 8-11
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 416;              // 13 warps
+constexpr int kSoftThreads = 256;          // rank 0 warps 0-7
+constexpr int kWorkers = 128;              // rank 1 warps 0-3
+constexpr int kProdWarp0 = 8;
+constexpr int kProducers = 256;            // warps 8-15
+constexpr int kMmaWarp = 16;
+constexpr int kThreads = 544;              // 17 warps
 constexpr int kMaxChunkRows = 2048;        // rows per chunk of a row unit
-constexpr int kVBytes = kTile * kHalf * 2; // 32,768 per buffer
-constexpr int kPBytes = 128 * kTile * 2;   // 16,384 per buffer
-constexpr int kXBytes = 128 * kTile * 4;   // 32,768: partial scores of one tile
-constexpr int kOffV = 0;
-constexpr int kOffP = kOffV + 2 * kVBytes;
-constexpr int kOffXin = kOffP + 2 * kPBytes;   // the peer's partial lands here
-constexpr int kOffXout = kOffXin + kXBytes;    // ours, staged for the copy to the peer
-constexpr int kOffMisc = kOffXout + kXBytes;
+constexpr int kTileBytes = kTile * kDim * 2;   // 65,536: one 64-row tile, all channels, fp16
+constexpr int kPBytes = 128 * kTile * 2;       // 16,384: P of one tile, fp16
+constexpr int kMsgBytes = kPBytes + 128 * 4 + 16;  // P, per-row rescale factor, header
+constexpr int kOffTiles = 0;
+constexpr int kOffMsg = kOffTiles + 2 * kTileBytes;
+constexpr int kOffMisc = kOffMsg + 2 * kMsgBytes;
 constexpr int kPartFloats = 64 + kHeads * kDim;  // m[2][16], l[2][16], O[16][512]
 constexpr int kMaxUnits = 2 * kMaxAttnEntries;
 constexpr int kMaxParts = 64;              // partials per layer: at most 63 row chunks and the window
 constexpr float kRescaleGap = 8.0f;        // lazy O rescale threshold (natural log)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0;              // 128 columns: query rows, fp16 pairs
-constexpr uint32_t kColS = 128;            // 2 x 64 columns
-constexpr uint32_t kColO = 256;            // 256 columns
+constexpr uint32_t kColQ = 0;              // rank 0: 256 columns, query rows as fp16 pairs
+constexpr uint32_t kColS = 256;            // rank 0: 2 x 64 columns
+constexpr uint32_t kColO = 0;              // rank 1: 512 columns
 // Instruction descriptors: QK^T (A from tensor memory, B K-major), PV (A K-major, B = V read MN-major).
 constexpr uint32_t kIdescQK = tc::idesc_f16(128, kTile, false, false);
-constexpr uint32_t kIdescPV = tc::idesc_f16(128, kHalf, false, true);
-// named barriers: 1 producers, 2 softmax (all 256)
+constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, false, true);
+// named barriers: 1 producers, 2 rank-0 softmax
 constexpr uint32_t kBarProd = 1, kBarSoft = 2;
+static_assert(kMsgBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+constexpr int kStageRow = 256 * 4 + 16;    // rank 1 read-out: one row-half of O, padded
+static_assert(128 * kStageRow <= kOffMisc, "the read-out stage fits in the tile and message buffers");
+
+// The P message of one tile (rank 0 Pout / rank 1 Pin).
+struct PMsg {
+    uint8_t p[kPBytes];       // K-major core-matrix layout: 8 groups of 8 keys, 1,024 B per 8-row group
+    float alpha[128];         // per query row: factor to apply to O before this tile's PV
+    uint32_t rescale;         // nonzero: some alpha differs from 1
+    uint32_t pad[3];
+};
+static_assert(sizeof(PMsg) == kMsgBytes, "P message layout");
 
 struct AttnMisc {
-    float mscale[2][kTile];   // per V buffer: per-row scale (FP8 window rows)
-    uint32_t vmask[2][2];     // per V buffer: valid rows (bit j of word j/32)
+    float mscale[2][kTile];   // per tile buffer: per-row scale (FP8 window rows)
+    uint32_t vmask[2][2];     // per tile buffer: valid rows (bit j of word j/32)
     float xmax[2][2][128];    // per tile parity and key half: tile max of each query row
     float lpart[128];         // running sum of the second key half, for the final combine
-    uint64_t q_bar, full_v[2], s_full[2], s_free[2], p_full[2], pv_done[2];
-    uint64_t x_full;          // the peer's partial scores have landed in Xin (bulk copy)
-    uint64_t x_free;          // the peer has consumed the partial this CTA sent it
+    uint64_t q_bar;           // rank 0: queries in tensor memory
+    uint64_t full_t[2];       // tile dequantised
+    uint64_t s_full[2];       // rank 0: QK^T committed
+    uint64_t s_free[2];       // rank 0: S loaded by the softmax (QK^T of that tile had finished)
+    uint64_t sm_done[2];      // rank 0: the softmax of that tile is complete
+    uint64_t p_full[2];       // rank 1: a P message landed (bulk copy)
+    uint64_t o_ready[2];      // rank 1: O holds the rescale that tile asks for
+    uint64_t pv_evt[2];       // both: PV of that tile finished (multicast commit)
     uint32_t tmem_slot;
 };
 static_assert(kOffMisc + (int)sizeof(AttnMisc) <= 232448, "attention shared memory over the 227 KB limit");
@@ -120,23 +134,16 @@ struct AttnParams {
     int32_t n_units;
     int32_t batch, topk, window, rows_per_chunk, max_parts;
     const int32_t *seq_lens;
+    const uint8_t *q16;     // [entry][B][16][512] fp16 query rows
     float *partials;        // [entry][B][max_parts][kPartFloats]
 };
 
-// Byte offset of fp16 element (row r, channel c) of an operand with 256-channel
-// rows in the no-swizzle core-matrix layout: 8-row groups 4,096 B apart,
-// 8-channel groups 128 B apart.
-__host__ __device__ __forceinline__ uint32_t cm_off256(uint32_t r, uint32_t c)
+// Byte offset of fp16 element (row r, channel c) of a 512-channel operand in
+// the no-swizzle core-matrix layout: 8-row groups 8,192 B apart, 8-channel
+// groups 128 B apart.
+__host__ __device__ __forceinline__ uint32_t cm_off512(uint32_t r, uint32_t c)
 {
-    return (r >> 3) * 4096u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
-}
-
-// Partial scores of one tile: row r holds 16 float4 (64 keys), chunk k at
-// position k ^ (r & 7), so a quarter-warp's 16-byte accesses (8 consecutive
-// rows, same k) fall in distinct banks.
-__host__ __device__ __forceinline__ uint32_t x_off(uint32_t r, uint32_t k)
-{
-    return r * (kTile * 4) + ((k ^ (r & 7u)) * 16u);
+    return (r >> 3) * 8192u + (c >> 3) * 128u + (r & 7u) * 16u + (c & 7u) * 2u;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
@@ -159,17 +166,56 @@ struct Ctx {
     const AttnParams *P;
     const UnitDev *U;
     AttnMisc *M;
-    uint8_t *Vs, *Ps, *Xin, *Xout;
+    uint8_t *T;         // 2 tiles
+    PMsg *Msg;          // 2 P messages (rank 0: outgoing, rank 1: incoming)
     int *flags;
     uint32_t tmem;
-    int b, L, W, row0, n_rows, n_tiles, chunk, half;
+    int b, L, W, row0, n_rows, n_tiles, chunk, rank;
 };
 
-// ---- producers (warps 8-11): gather + dequantise 64-row tiles -------------------------
-// Thread ptid owns row j = ptid % 64 of every tile and the half w = ptid / 64
-// of the CTA's 256 channels: channels 256h + 128w .. +127 (FP4 rows: four
-// 16-byte granules of 32 channels and eight E4M3 scales; FP8 rows: eight
-// granules of 16).
+// ---- rank 0, warps 0-15: the queries into tensor memory ---------------------------------
+// Thread (row r = 32(w%4) + lane, part w/4) moves channels 128 part..+127 of
+// its row (fp16, packed by the step's first kernel; one round of 16-byte
+// loads) into tensor-memory columns 64 part..+63 as fp16 pairs.  The packed
+// layout of one (layer, sequence) is [part 4][granule 16][head 16][8 channels],
+// so the 16 heads of a layer read one contiguous 256-B run per load.
+__device__ __forceinline__ void load_q(const Ctx &c)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quad = warp & 3, part = warp >> 2;
+    const int r = 32 * quad + lane, slot_layer = r >> 4, head = r & 15;
+    const UnitDev &U = *c.U;
+    uint4 v[16];
+    if (slot_layer < U.n_layers) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+                               c.P->q16 + ((int64_t)U.entry[slot_layer] * c.P->batch + c.b) * (kHeads * kDim * 2)) +
+                           (part * 16) * kHeads + head;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __ldg(src + i * kHeads);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        float h[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            h[4 * i] = __uint_as_float(v[8 * cc + i].x);
+            h[4 * i + 1] = __uint_as_float(v[8 * cc + i].y);
+            h[4 * i + 2] = __uint_as_float(v[8 * cc + i].z);
+            h[4 * i + 3] = __uint_as_float(v[8 * cc + i].w);
+        }
+        tc::tmem_st32(tc::taddr(c.tmem, (uint32_t)(32 * quad), kColQ + 64 * part + 32 * cc), h);
+    }
+    tc::fence_before_sync();
+    tc::mbar_arrive(&c.M->q_bar);
+}
+
+// ---- producers (warps 8-15, both ranks): gather + dequantise 64-row tiles ------------
+// Thread ptid owns row j = ptid % 64 of every tile and the quarter w = ptid / 64
+// of its channels, 128w..128w+127 (FP4 rows: four 16-byte granules of 32
+// channels and eight E4M3 scales; FP8 rows: eight granules of 16 channels).
 template <bool FP8>
 struct RowRegs {
     uint4 g[FP8 ? 8 : 4];
@@ -218,17 +264,16 @@ __device__ __forceinline__ void load_row(const Ctx &c, int t, int j, int w, int3
     r.valid = ptr != nullptr;
     if (FP8) {
         r.s[0] = sc;
-        const uint8_t *base = ptr ? ptr + c.half * 256 + 128 * w : nullptr;
+        const uint8_t *base = ptr ? ptr + 128 * w : nullptr;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             r.g[i] = base ? __ldg(reinterpret_cast<const uint4 *>(base + 16 * i)) : make_uint4(0u, 0u, 0u, 0u);
     } else {
-        const uint8_t *base = ptr ? ptr + c.half * 128 + 64 * w : nullptr;
+        const uint8_t *base = ptr ? ptr + 64 * w : nullptr;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             r.g[i] = base ? __ldg(reinterpret_cast<const uint4 *>(base + 16 * i)) : make_uint4(0u, 0u, 0u, 0u);
-        const uint2 sc2 = ptr ? __ldg(reinterpret_cast<const uint2 *>(ptr + kKvCodes + c.half * 16 + 8 * w))
-                              : make_uint2(0u, 0u);
+        const uint2 sc2 = ptr ? __ldg(reinterpret_cast<const uint2 *>(ptr + kKvCodes + 8 * w)) : make_uint2(0u, 0u);
         r.s[0] = sc2.x;
         r.s[1] = sc2.y;
     }
@@ -240,12 +285,12 @@ __device__ __forceinline__ void store_row(uint8_t *V, int j, int w, const RowReg
     if (FP8) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int ch = 128 * w + 16 * i;  // channels ch..ch+15 of the half
+            const int ch = 128 * w + 16 * i;  // channels ch..ch+15
             const uint4 cw = r.g[i];
-            *reinterpret_cast<uint4 *>(V + cm_off256(j, ch)) =
+            *reinterpret_cast<uint4 *>(V + cm_off512(j, ch)) =
                 make_uint4(pack_h2(e4m3x2_half2(cw.x & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.x >> 16)),
                            pack_h2(e4m3x2_half2(cw.y & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.y >> 16)));
-            *reinterpret_cast<uint4 *>(V + cm_off256(j, ch + 8)) =
+            *reinterpret_cast<uint4 *>(V + cm_off512(j, ch + 8)) =
                 make_uint4(pack_h2(e4m3x2_half2(cw.z & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.z >> 16)),
                            pack_h2(e4m3x2_half2(cw.w & 0xFFFFu)), pack_h2(e4m3x2_half2(cw.w >> 16)));
         }
@@ -266,136 +311,100 @@ __device__ __forceinline__ void store_row(uint8_t *V, int j, int w, const RowReg
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(V + cm_off256(j, ch + 8 * k)) =
+                *reinterpret_cast<uint4 *>(V + cm_off512(j, ch + 8 * k)) =
                     make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]);
         }
     }
+}
+
+// Tile buffer b is free for tile t >= 2 once, on rank 0, the softmax has
+// loaded S(t-2) (so QK^T(t-2) is done; FP8 tiles also need the softmax of
+// t-2 complete, for the row scales) and, on rank 1, PV(t-2) has finished.
+template <bool FP8>
+__device__ __forceinline__ bool wait_tile_free(const Ctx &c, int t)
+{
+    AttnMisc &M = *c.M;
+    const int b = t & 1;
+    const uint32_t par = ((t - 2) >> 1) & 1;
+    if (c.rank == 0) return tc::mbar_wait(FP8 ? &M.sm_done[b] : &M.s_free[b], par);
+    return tc::mbar_wait(&M.pv_evt[b], par);
 }
 
 template <bool FP8>
 __device__ __forceinline__ void produce(const Ctx &c)
 {
     AttnMisc &M = *c.M;
-    const int ptid = threadIdx.x - kSoftThreads;
+    const int ptid = threadIdx.x - kProdWarp0 * 32;
     const int j = ptid & (kTile - 1), w = ptid >> 6;
-    // row positions run two tiles ahead of the row bytes, so no load waits on another
+    if (c.rank == 0) load_q(c);
+    // FP4: row positions run two tiles ahead and row bytes one tile ahead;
+    // FP8 window tiles (few) load in place
     int32_t pos_next = FP8 ? -1 : row_pos(c, 1, j);
     RowRegs<FP8> cur, nxt;
-    if (c.n_tiles > 0) load_row<FP8>(c, 0, j, w, FP8 ? -1 : row_pos(c, 0, j), cur);
+    if (!FP8 && c.n_tiles > 0) load_row<FP8>(c, 0, j, w, row_pos(c, 0, j), cur);
     for (int t = 0; t < c.n_tiles; ++t) {
-        const int vb = t & 1;
-        if (t + 1 < c.n_tiles) load_row<FP8>(c, t + 1, j, w, pos_next, nxt);  // in flight during this tile's work
-        if (!FP8) pos_next = row_pos(c, t + 2, j);
-        // V[vb] and its row metadata are free once PV(t-2) has finished
-        const bool bad = (t >= 2) && !tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1);
+        const int b = t & 1;
+        if (FP8) {
+            load_row<FP8>(c, t, j, w, -1, cur);
+        } else {
+            if (t + 1 < c.n_tiles) load_row<FP8>(c, t + 1, j, w, pos_next, nxt);  // in flight during this tile
+            pos_next = row_pos(c, t + 2, j);
+        }
+        const bool bad = (t >= 2) && !wait_tile_free<FP8>(c, t);
         if (bar_any(kBarProd, kProducers, bad)) {
             if (ptid == 0) raise_flag(c.flags, kFlagTimeout);
             break;
         }
-        store_row<FP8>(c.Vs + vb * kVBytes, j, w, cur);
+        store_row<FP8>(c.T + b * kTileBytes, j, w, cur);
         if (w == 0) {
             const uint32_t mask = __ballot_sync(0xFFFFFFFFu, cur.valid);
-            if ((j & 31) == 0) M.vmask[vb][j >> 5] = mask;
-            M.mscale[vb][j] = FP8 ? __uint_as_float(cur.s[0]) : 1.0f;
+            if ((j & 31) == 0) M.vmask[b][j >> 5] = mask;
+            M.mscale[b][j] = FP8 ? __uint_as_float(cur.s[0]) : 1.0f;
         }
         tc::fence_async_smem();
-        tc::mbar_arrive(&M.full_v[vb]);
-        cur = nxt;
+        tc::mbar_arrive(&M.full_t[b]);
+        if (!FP8) cur = nxt;
     }
 }
 
-// ---- MMA issuer (one thread) ---------------------------------------------------------
-// QK^T of tile t is issued in two groups of 8 MMAs; between groups (and while
-// waiting for the next tile) the issuer polls for a finished P and issues its
-// PV at once, so PV never queues behind a whole QK^T.
-__device__ __forceinline__ void issue_mmas(const Ctx &c)
+// ---- rank 0: QK^T issue (one thread) --------------------------------------------------
+// S(t) = Q K(t)^T: 32 MMAs of K 16 (A: queries in tensor memory, 8 columns per
+// K step; B: the tile, K-major, 256 B per K step).
+__device__ __forceinline__ void issue_qk(const Ctx &c)
 {
     AttnMisc &M = *c.M;
-    bool ok = tc::mbar_wait(&M.q_bar, 0);  // the queries are in tensor memory
-    // descriptors; a K step of 16 adds 8 columns to the tensor-memory A operand,
-    // 256 B (16 in the 16-byte address field) to K-major smem operands and
-    // 8,192 B (512) to V read MN-major
-    const uint32_t va0 = tc::smem_u32(c.Vs), va1 = tc::smem_u32(c.Vs + kVBytes);
-    const uint64_t vd0 = tc::sdesc(va0, 128, 4096), vd1 = tc::sdesc(va1, 128, 4096);
-    const uint64_t vm0 = tc::sdesc(va0, 4096, 128), vm1 = tc::sdesc(va1, 4096, 128);
-    const uint64_t pd0 = tc::sdesc(tc::smem_u32(c.Ps), 128, 1024);
-    const uint64_t pd1 = tc::sdesc(tc::smem_u32(c.Ps + kPBytes), 128, 1024);
-    const uint32_t qa = c.tmem + kColQ;
-    int qk_done = 0;  // tiles whose QK^T has been issued
-    int pv_next = 0;  // next tile whose PV is due
+    bool ok = tc::mbar_wait(&M.q_bar, 0);
+    const uint64_t kd0 = tc::sdesc(tc::smem_u32(c.T), 128, 8192);
+    const uint64_t kd1 = tc::sdesc(tc::smem_u32(c.T + kTileBytes), 128, 8192);
     uint64_t *last_bar = nullptr;
     uint32_t last_par = 0;
-    auto issue_pv = [&](int t) {
-        const int pb = t & 1;
-        tc::fence_after_sync();
-        const uint64_t pdb = pb ? pd1 : pd0, vmb = pb ? vm1 : vm0;
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-            tc::mma_f16(c.tmem + kColO, pdb + 16 * k, vmb + 512 * k, kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(&M.pv_done[pb]);
-        last_bar = &M.pv_done[pb];
-        last_par = (t >> 1) & 1;
-    };
-    // issue every PV whose P is ready (non-blocking)
-    auto poll_pv = [&]() {
-        while (pv_next < qk_done && tc::mbar_try_wait(&M.p_full[pv_next & 1], (pv_next >> 1) & 1)) {
-            issue_pv(pv_next);
-            ++pv_next;
-        }
-    };
-    // bounded wait on (bar, parity) that keeps issuing ready PVs meanwhile
-    auto wait_polling = [&](uint64_t *bar, uint32_t par) {
-        for (uint32_t i = 0; i < tc::kWaitLimit; ++i) {
-            if (tc::mbar_try_wait(bar, par)) return true;
-            poll_pv();
-        }
-        return false;
-    };
     for (int t = 0; t < c.n_tiles && ok; ++t) {
-        const int vb = t & 1;
-        if (!wait_polling(&M.full_v[vb], (t >> 1) & 1) ||
-            (t >= 2 && !wait_polling(&M.s_free[vb], ((t - 2) >> 1) & 1))) {
-            ok = false;
-            break;
-        }
+        const int b = t & 1;
+        ok = tc::mbar_wait(&M.full_t[b], (t >> 1) & 1) && (t < 2 || tc::mbar_wait(&M.s_free[b], ((t - 2) >> 1) & 1));
+        if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t d = c.tmem + kColS + kTile * vb;
-        const uint64_t vdb = vb ? vd1 : vd0;
+        const uint32_t d = c.tmem + kColS + kTile * b;
+        const uint64_t kd = b ? kd1 : kd0;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int ks = 8 * g + k;
-                tc::mma_f16_ta(d, qa + 8 * ks, vdb + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
-            }
-            if (g == 1) {
-                tc::mma_commit(&M.s_full[vb]);
-                last_bar = &M.s_full[vb];
-                last_par = (t >> 1) & 1;
-                qk_done = t + 1;
-            }
-            poll_pv();
-        }
-    }
-    // the remaining PVs, in order
-    while (ok && pv_next < qk_done) {
-        if (!tc::mbar_wait(&M.p_full[pv_next & 1], (pv_next >> 1) & 1)) {
-            ok = false;
-            break;
-        }
-        issue_pv(pv_next);
-        ++pv_next;
+        for (int ks = 0; ks < kDim / 16; ++ks)
+            tc::mma_f16_ta(d, c.tmem + kColQ + 8 * ks, kd + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+        tc::mma_commit(&M.s_full[b]);
+        last_bar = &M.s_full[b];
+        last_par = (t >> 1) & 1;
     }
     if (!ok) raise_flag(c.flags, kFlagTimeout);
-    // every issued MMA must have finished before the tensor memory is released
-    if (last_bar) tc::mbar_wait(last_bar, last_par);
+    if (last_bar) tc::mbar_wait(last_bar, last_par);  // every MMA done before tensor memory is released
 }
 
-// ---- softmax (warps 0-7) --------------------------------------------------------------
+// ---- rank 0: softmax (warps 0-7) ------------------------------------------------------
 // Thread (row r = 32(w%4) + lane, key half kh = w/4) holds the row's scores of
-// keys 32kh..32kh+31 of each tile and O columns 128kh..128kh+127.  A failed
-// wait clears `ok`; the loop leaves only at a reduction over all 256 threads,
-// so every softmax thread meets every named barrier the same number of times.
+// keys 32kh..32kh+31 of each tile.  Per tile: S from tensor memory, mask and
+// scale, the row's tile max (both key halves), the lazy rescale decision (a
+// row moves its reference max only when the tile max exceeds it by more than
+// e^8; the factor for O travels to rank 1), then P = exp(S - m) as fp16 into
+// the outgoing message, which thread 0 copies to rank 1.  A failed wait clears
+// `ok`; the loop leaves only at a reduction over all 256 threads, so every
+// softmax thread meets every named barrier the same number of times.
 template <bool FP8>
 __device__ __forceinline__ void softmax_rows(const Ctx &c)
 {
@@ -407,163 +416,295 @@ __device__ __forceinline__ void softmax_rows(const Ctx &c)
     const int slot_layer = r >> 4, head = r & 15;
     const bool active = slot_layer < U.n_layers;
     const uint32_t lane_base = (uint32_t)(32 * quad);
-    const uint32_t peer = (uint32_t)(c.half ^ 1);
-    const uint32_t xin_peer = tc::mapa(tc::smem_u32(c.Xin), peer);
-    const uint32_t xfull_peer = tc::mapa(tc::smem_u32(&M.x_full), peer);
-    const uint32_t xfree_peer = tc::mapa(tc::smem_u32(&M.x_free), peer);
+    const uint32_t pin_peer = tc::mapa(tc::smem_u32(c.Msg), 1);
+    const uint32_t pfull_peer = tc::mapa(tc::smem_u32(&M.p_full[0]), 1);
 
-    // this row's queries (channels 128kh..+127 of the half) into tensor memory as fp16 pairs
-    {
-        const float *q = active ? c.P->entries[U.entry[slot_layer]].q + ((int64_t)c.b * kHeads + head) * kDim +
-                                      c.half * kHalf + 128 * kh
-                                : nullptr;
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-            float h[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 a = q ? __ldg(reinterpret_cast<const float4 *>(q + 64 * cc + 4 * i))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                h[2 * i] = __uint_as_float(pack_h2(__floats2half2_rn(a.x, a.y)));
-                h[2 * i + 1] = __uint_as_float(pack_h2(__floats2half2_rn(a.z, a.w)));
-            }
-            tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColQ + 64 * kh + 32 * cc), h);
-        }
-        tc::fence_before_sync();
-        tc::mbar_arrive(&M.q_bar);
-    }
+    load_q(c);
 
     float m_used = -INFINITY, l_half = 0.0f;
     bool ok = true;
     for (int t = 0; t < c.n_tiles; ++t) {
-        const int vb = t & 1;
-        ok = ok && tc::mbar_wait(&M.full_v[vb], (t >> 1) & 1) && tc::mbar_wait(&M.s_full[vb], (t >> 1) & 1);
+        const int b = t & 1;
+        ok = ok && tc::mbar_wait(&M.full_t[b], (t >> 1) & 1) && tc::mbar_wait(&M.s_full[b], (t >> 1) & 1);
         tc::fence_after_sync();
         float s[32];
-        tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColS + kTile * vb + 32 * kh), s);
+        tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColS + kTile * b + 32 * kh), s);
+        const uint32_t vm = M.vmask[b][kh];  // read before S is released: the tile buffer may refill after
         tc::fence_before_sync();
-        tc::mbar_arrive(&M.s_free[vb]);
-        // our partial scores to the peer, once it has consumed the previous ones
-        ok = ok && (t < 1 || tc::mbar_wait_cluster(&M.x_free, (t - 1) & 1));
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4 *>(c.Xout + x_off(r, 8 * kh + k)) =
-                make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-        tc::fence_async_smem();
-        if (bar_any(kBarSoft, kSoftThreads, !ok)) break;
-        if (tid == 0) tc::bulk_s2peer(xin_peer, c.Xout, kXBytes, xfull_peer);
-        // full scores = ours + the peer's, masked and scaled; this key half's tile max
-        ok = tc::mbar_wait_cluster(&M.x_full, t & 1);
-        if (tid == 0 && ok && t + 1 < c.n_tiles) tc::mbar_expect_tx(&M.x_full, kXBytes);  // arm the next tile
-        const uint32_t vm = M.vmask[vb][kh];
+        tc::mbar_arrive(&M.s_free[b]);
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 v = *reinterpret_cast<const float4 *>(c.Xin + x_off(r, 8 * kh + k));
-            const float pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = 4 * k + i;
-                const float z = s[j] + pv[i];
-                const float zs = FP8 ? z * M.mscale[vb][32 * kh + j] : z;
-                s[j] = ((vm >> j) & 1u) ? zs : -INFINITY;
-                mx[i] = fmaxf(mx[i], s[j]);
-            }
+        for (int j = 0; j < 32; ++j) {
+            const float z = FP8 ? s[j] * M.mscale[b][32 * kh + j] : s[j];
+            s[j] = ((vm >> j) & 1u) ? z : -INFINITY;
+            mx[j & 3] = fmaxf(mx[j & 3], s[j]);
         }
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        M.xmax[vb][kh][r] = mt;
-        if (bar_any(kBarSoft, kSoftThreads, !ok)) break;  // also: every Xin read and xmax write is done
-        if (tid == 32) tc::mbar_arrive_cluster(xfree_peer);  // not the copy issuer: its release would wait on the copy
-        const float m_tile = fmaxf(mt, M.xmax[vb][kh ^ 1][r]);
+        M.xmax[b][kh][r] = mt;
+        if (bar_any(kBarSoft, kSoftThreads, !ok)) break;  // also: both key halves' maxima are written
+        const float m_tile = fmaxf(mt, M.xmax[b][kh ^ 1][r]);
         const float m_new = active ? fmaxf(m_used, m_tile) : m_used;
-        // lazy rescale of this warp's O columns, warp-uniform (both key halves decide alike)
-        if (__any_sync(0xFFFFFFFFu, active && m_new > m_used + kRescaleGap)) {
-            if (t >= 1) {
-                ok = ok && tc::mbar_wait(&M.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1);  // O is current
-                tc::fence_after_sync();
-                const float alpha = (active && m_used != -INFINITY) ? __expf(m_used - m_new) : (active ? 0.0f : 1.0f);
-#pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    float o[32];
-                    tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
-                }
-                if (active) l_half *= alpha;
-            }
-            if (active) m_used = m_new;
+        const bool resc = active && m_new > m_used + kRescaleGap;
+        const float alpha = resc ? (m_used == -INFINITY ? 0.0f : __expf(m_used - m_new)) : 1.0f;
+        if (resc) {
+            l_half *= alpha;
+            m_used = m_new;
         }
-        // P[vb] is free once PV(t-2) has finished
-        ok = ok && (t < 2 || tc::mbar_wait(&M.pv_done[vb], ((t - 2) >> 1) & 1));
-        // P = exp(S - m) as fp16, K-major core-matrix layout (8 groups of 8 keys, 1,024 B
-        // per 8-row group); window rows hold raw E4M3 codes, so their scale joins the weight
+        // the outgoing message of this parity is free once rank 1 finished PV(t-2)
+        ok = ok && (t < 2 || tc::mbar_wait_cluster(&M.pv_evt[b], ((t - 2) >> 1) & 1));
+        PMsg &msg = c.Msg[b];
+        // P = exp(S - m) as fp16; window rows hold raw E4M3 codes, so their scale joins the weight
         const float mb = m_used * kLog2e;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            s[j] = (active && s[j] != -INFINITY) ? exp2f(fmaf(s[j], kLog2e, -mb)) : 0.0f;
+            s[j] = (active && s[j] != -INFINITY) ? tc::exp2_fast(fmaf(s[j], kLog2e, -mb)) : 0.0f;
             ls[j & 3] += s[j];
         }
         l_half += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        uint8_t *Pb = c.Ps + vb * kPBytes + (r >> 3) * 1024 + (r & 7) * 16;
+        uint8_t *Pb = msg.p + (r >> 3) * 1024 + (r & 7) * 16;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             uint32_t ph[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int j = 8 * g + 2 * i;
-                const float a = FP8 ? s[j] * M.mscale[vb][32 * kh + j] : s[j];
-                const float d = FP8 ? s[j + 1] * M.mscale[vb][32 * kh + j + 1] : s[j + 1];
+                const float a = FP8 ? s[j] * M.mscale[b][32 * kh + j] : s[j];
+                const float d = FP8 ? s[j + 1] * M.mscale[b][32 * kh + j + 1] : s[j + 1];
                 ph[i] = pack_h2(__floats2half2_rn(a, d));
             }
             *reinterpret_cast<uint4 *>(Pb + (4 * kh + g) * 128) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
         }
+        if (kh == 0) msg.alpha[r] = alpha;
         tc::fence_async_smem();
-        tc::fence_before_sync();
-        tc::mbar_arrive(&M.p_full[vb]);
+        const bool any_resc = bar_any(kBarSoft, kSoftThreads, resc);  // also: the whole message is written
+        tc::mbar_arrive(&M.sm_done[b]);
+        if (tid == 0) {
+            msg.rescale = any_resc ? 1u : 0u;
+            tc::fence_async_smem();
+            tc::bulk_s2peer(pin_peer + b * kMsgBytes, &msg, kMsgBytes, pfull_peer + b * 8);
+        }
     }
     if (c.n_tiles > 0) {
+        // rank 1 has consumed the last message (and its multicast arrival has landed here)
         const int last = c.n_tiles - 1;
-        ok = ok && tc::mbar_wait(&M.pv_done[last & 1], (last >> 1) & 1);
+        ok = ok && tc::mbar_wait_cluster(&M.pv_evt[last & 1], (last >> 1) & 1);
     }
     if (!ok) raise_flag(c.flags, kFlagTimeout);
-    // both key halves' sums, then this chunk's partial for the channel half: (m, l, unnormalised O)
+    // both key halves' sums; the partial's (m, l), the same for both channel halves
     if (kh == 1) M.lpart[r] = l_half;
     const bool have = !bar_any(kBarSoft, kSoftThreads, !ok) && c.n_tiles > 0;
+    if (active && kh == 0) {
+        const int e = U.entry[slot_layer];
+        const EntryDev &E = c.P->entries[e];
+        const int part = U.is_window ? E.part_win : c.chunk;
+        float *rec = c.P->partials + (((int64_t)e * c.P->batch + c.b) * c.P->max_parts + part) * kPartFloats;
+        const float l_sum = l_half + M.lpart[r];
+        const bool any = have && l_sum > 0.0f;
+        rec[head] = rec[16 + head] = any ? m_used : -INFINITY;
+        rec[32 + head] = rec[48 + head] = any ? l_sum : 0.0f;
+    }
+}
+
+// ---- rank 1: PV issue (one thread) ----------------------------------------------------
+// O += P(t) V(t): 4 K steps of 16 keys x 2 channel halves of N 256 (A: P from
+// the landed message, K-major, 256 B per K step; B: the tile read MN-major,
+// 16,384 B per K step, channel half n at +4,096 B).  The commit is multicast
+// to both CTAs' pv_evt: here it frees the tile buffer and (with o_ready) lets
+// the workers rescale O; on rank 0 it frees the outgoing message.
+__device__ __forceinline__ void issue_pv(const Ctx &c)
+{
+    AttnMisc &M = *c.M;
+    bool ok = true;
+    bool issued = false;
+    int last = -1;
+    for (int t = 0; t < c.n_tiles; ++t) {
+        const int b = t & 1;
+        const uint32_t par = (t >> 1) & 1;
+        ok = tc::mbar_wait(&M.full_t[b], par) && tc::mbar_wait_cluster(&M.p_full[b], par) &&
+             tc::mbar_wait(&M.o_ready[b], par);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t va = tc::smem_u32(c.T + b * kTileBytes);
+        const uint64_t pd = tc::sdesc(tc::smem_u32(c.Msg[b].p), 128, 1024);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+                tc::mma_f16(c.tmem + kColO + 256 * n, pd + 16 * k, tc::sdesc(va + 4096 * n + 16384 * k, 8192, 128),
+                            kIdescPV, (t > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit_multicast(&M.pv_evt[b], 0x3);
+        issued = true;
+        last = t;
+    }
+    if (!ok) raise_flag(c.flags, kFlagTimeout);
+    if (issued) tc::mbar_wait(&M.pv_evt[last & 1], (last >> 1) & 1);  // every MMA done before tensor memory is released
+}
+
+// ---- rank 1: O rescale and read-out (warps 0-3, thread = tensor-memory lane = query row) ----
+__device__ __forceinline__ void o_workers(const Ctx &c)
+{
+    AttnMisc &M = *c.M;
+    const UnitDev &U = *c.U;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int r = tid, slot_layer = r >> 4, head = r & 15;
+    const bool active = slot_layer < U.n_layers;
+    const uint32_t lane_base = (uint32_t)(32 * warp);
+    bool ok = true;
+    for (int t = 0; t < c.n_tiles; ++t) {
+        const int b = t & 1;
+        const bool landed = tc::mbar_wait_cluster(&M.p_full[b], (t >> 1) & 1);
+        if (tid == 0 && landed && t + 2 < c.n_tiles) tc::mbar_expect_tx(&M.p_full[b], kMsgBytes);  // tile t+2
+        ok = __all_sync(0xFFFFFFFFu, landed);
+        if (!ok) break;
+        const PMsg &msg = c.Msg[b];
+        if (msg.rescale && t >= 1) {
+            // O must hold PV(t-1) before it is scaled
+            ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait(&M.pv_evt[(t - 1) & 1], ((t - 1) >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after_sync();
+            const float a = msg.alpha[r];
+            if (__any_sync(0xFFFFFFFFu, a != 1.0f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < kDim; c0 += 32) {
+                    float o[32];
+                    tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= a;
+                    tc::tmem_st32(tc::taddr(c.tmem, lane_base, kColO + c0), o);
+                }
+            }
+            tc::fence_before_sync();
+        }
+        tc::mbar_arrive(&M.o_ready[b]);
+    }
+    if (ok && c.n_tiles > 0) {
+        const int last = c.n_tiles - 1;
+        ok = __all_sync(0xFFFFFFFFu, tc::mbar_wait(&M.pv_evt[last & 1], (last >> 1) & 1));
+    }
+    if (!ok && (tid & 31) == 0) raise_flag(c.flags, kFlagTimeout);
     tc::fence_after_sync();
+    // this chunk's unnormalised output, all 512 channels, in two channel halves:
+    // each thread puts its row-half in shared memory (the tile buffers are idle
+    // now; rows 1,040 B apart, so a quarter-warp's 16-byte stores of 8
+    // consecutive rows fall in distinct banks) and sends it with one bulk copy
+    const bool have = ok && c.n_tiles > 0;
     float *orow = nullptr;
     if (active) {
         const int e = U.entry[slot_layer];
         const EntryDev &E = c.P->entries[e];
         const int part = U.is_window ? E.part_win : c.chunk;
-        float *rec = c.P->partials + (((int64_t)e * c.P->batch + c.b) * c.P->max_parts + part) * kPartFloats;
-        if (kh == 0) {
-            const float l_sum = l_half + M.lpart[r];
-            const bool any = have && l_sum > 0.0f;
-            rec[c.half * 16 + head] = any ? m_used : -INFINITY;
-            rec[32 + c.half * 16 + head] = any ? l_sum : 0.0f;
-        }
-        orow = rec + 64 + head * kDim + c.half * kHalf + 128 * kh;
+        orow = c.P->partials + (((int64_t)e * c.P->batch + c.b) * c.P->max_parts + part) * kPartFloats + 64 +
+               head * kDim;
     }
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-        float o[32];
-        if (have) tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + 128 * kh + c0), o);
-        if (active) {
+    float *srow = reinterpret_cast<float *>(c.T + r * kStageRow);
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1 && active) tc::bulk_wait_read0();  // the first copy has read this row
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+            float o[32];
+            if (have) {
+                tc::tmem_ld32(tc::taddr(c.tmem, lane_base, kColO + 256 * hh + c0), o);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+            }
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4 *>(orow + c0 + i) =
-                    have ? make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(srow + c0 + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+        }
+        if (active) {
+            tc::fence_async_smem();
+            tc::bulk_s2g(orow + 256 * hh, srow, 1024);
+            tc::bulk_commit();
         }
     }
+    if (active) tc::bulk_wait0();
     tc::fence_before_sync();
 }
 
-// ---- merge: one CTA per (layer, sequence, channel half) combines the partials ----------
-// 256 threads.  The (m, l) of every part are staged in shared memory in one
-// round of independent loads; 16 threads then turn them into per-part weights
-// exp(m_p - max) (one head each), and every thread accumulates 16 output
-// channels of one head over the parts.  A layer with no parts writes zeros.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnParams P, int *flags)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx c;
+    c.P = &P;
+    c.M = reinterpret_cast<AttnMisc *>(smem + kOffMisc);
+    c.T = smem + kOffTiles;
+    c.Msg = reinterpret_cast<PMsg *>(smem + kOffMsg);
+    c.flags = flags;
+    c.b = blockIdx.y;
+    int u = 0;
+    while (u + 1 < P.n_units && (int)blockIdx.x >= P.units[u + 1].cta_begin) ++u;
+    c.U = &P.units[u];
+    const int local = (int)blockIdx.x - c.U->cta_begin;
+    c.chunk = local >> 1;
+    c.rank = (int)tc::cluster_rank();  // = local & 1: a pair is one cluster
+    c.L = max(0, __ldg(P.seq_lens + c.b));
+    c.W = P.window;
+    const bool fp8 = c.U->is_window != 0;
+    if (fp8) {
+        c.row0 = 0;
+        c.n_rows = c.W;
+    } else {
+        c.row0 = c.chunk * P.rows_per_chunk;
+        c.n_rows = max(0, min(P.rows_per_chunk, P.topk - c.row0));
+    }
+    c.n_tiles = (c.n_rows + kTile - 1) / kTile;
+    AttnMisc &M = *c.M;
+
+    if (tid == 0) {
+        tc::mbar_init(&M.q_bar, kSoftThreads + kProducers);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&M.full_t[i], kProducers);
+            tc::mbar_init(&M.s_full[i], 1);
+            tc::mbar_init(&M.s_free[i], kSoftThreads);
+            tc::mbar_init(&M.sm_done[i], kSoftThreads);
+            tc::mbar_init(&M.p_full[i], 1);
+            tc::mbar_init(&M.o_ready[i], kWorkers);
+            tc::mbar_init(&M.pv_evt[i], 1);
+        }
+        tc::mbar_init_fence();
+        if (c.rank == 1)  // armed for the first two tiles' messages
+            for (int i = 0; i < 2 && i < c.n_tiles; ++i) tc::mbar_expect_tx(&M.p_full[i], kMsgBytes);
+    }
+    if (warp == kMmaWarp) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
+    tc::fence_before_sync();
+    tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
+    tc::fence_after_sync();
+    c.tmem = M.tmem_slot;
+
+    if (warp >= kProdWarp0 && warp < kMmaWarp) {
+        if (fp8) produce<true>(c);
+        else produce<false>(c);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            if (c.rank == 0) issue_qk(c);
+            else issue_pv(c);
+        }
+        __syncwarp();
+    } else if (c.rank == 0) {
+        if (fp8) softmax_rows<true>(c);
+        else softmax_rows<false>(c);
+    } else if (warp < 4) {
+        o_workers(c);
+    }
+    tc::fence_before_sync();
+    tc::cluster_sync();  // no remote shared-memory access after this point
+    if (warp == kMmaWarp) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(c.tmem, kTmemCols);
+    }
+}
+
+// ---- merge: the partials of one (layer, sequence) -> out, lse -------------------------
+// Grid (layer, sequence, eighth of the channels); 256 threads, thread = (head
+// tid/16, 4 channels).  The (m, l) of every part are staged in shared memory
+// in one round of independent loads; 16 threads turn them into per-part
+// weights exp(m_p - max); every thread then sums one float4 per part.  A
+// layer with no parts writes zeros.
 struct MergeParams {
     EntryDev entries[kMaxAttnEntries];
     int32_t batch, max_parts;
@@ -574,7 +715,8 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
 {
     __shared__ float m_sh[kMaxParts][kHeads], l_sh[kMaxParts][kHeads];
     __shared__ float inv_sh[kHeads];
-    const int e = blockIdx.x, b = blockIdx.y, half = blockIdx.z, tid = threadIdx.x;
+    const int e = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int c_base = blockIdx.z * (kDim / 8), half = c_base / 256;
     const EntryDev &E = P.entries[e];
     const int np = min(E.n_parts, kMaxParts);
     const float *recs = P.partials + ((int64_t)e * P.batch + b) * P.max_parts * kPartFloats;
@@ -595,105 +737,27 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const __grid_constant__
             m_sh[p][tid] = wp;  // m becomes the part's weight
         }
         inv_sh[tid] = ls > 0.0f ? 1.0f / ls : 0.0f;
-        if (half == 0 && E.lse) E.lse[(int64_t)b * kHeads + tid] = ls > 0.0f ? mx + logf(ls) : -INFINITY;
+        if (blockIdx.z == 0 && E.lse) E.lse[(int64_t)b * kHeads + tid] = ls > 0.0f ? mx + logf(ls) : -INFINITY;
     }
     __syncthreads();
-    const int h = tid >> 4, c0 = half * kHalf + (tid & 15) * 16;
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#pragma unroll 4
+    const int h = tid >> 4, c0 = c_base + (tid & 15) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int p = 0; p < np; ++p) {
         const float wp = m_sh[p][h];
-        const float4 *op = reinterpret_cast<const float4 *>(recs + (int64_t)p * kPartFloats + 64 + h * kDim + c0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 v = __ldcg(op + i);
-            acc[4 * i] += wp * v.x;
-            acc[4 * i + 1] += wp * v.y;
-            acc[4 * i + 2] += wp * v.z;
-            acc[4 * i + 3] += wp * v.w;
-        }
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(recs + (int64_t)p * kPartFloats + 64 + h * kDim + c0));
+        acc.x += wp * v.x;
+        acc.y += wp * v.y;
+        acc.z += wp * v.z;
+        acc.w += wp * v.w;
     }
     const float inv = inv_sh[h];
-    float4 *out = reinterpret_cast<float4 *>(E.out + ((int64_t)b * kHeads + h) * kDim + c0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        out[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ AttnParams P, int *flags)
-{
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Ctx c;
-    c.P = &P;
-    c.M = reinterpret_cast<AttnMisc *>(smem + kOffMisc);
-    c.Vs = smem + kOffV;
-    c.Ps = smem + kOffP;
-    c.Xin = smem + kOffXin;
-    c.Xout = smem + kOffXout;
-    c.flags = flags;
-    c.b = blockIdx.y;
-    int u = 0;
-    while (u + 1 < P.n_units && (int)blockIdx.x >= P.units[u + 1].cta_begin) ++u;
-    c.U = &P.units[u];
-    const int local = (int)blockIdx.x - c.U->cta_begin;
-    c.chunk = local >> 1;
-    c.half = (int)tc::cluster_rank();  // = local & 1: a pair is one cluster
-    c.L = max(0, __ldg(P.seq_lens + c.b));
-    c.W = P.window;
-    const bool fp8 = c.U->is_window != 0;
-    if (fp8) {
-        c.row0 = 0;
-        c.n_rows = c.W;
-    } else {
-        c.row0 = c.chunk * P.rows_per_chunk;
-        c.n_rows = max(0, min(P.rows_per_chunk, P.topk - c.row0));
-    }
-    c.n_tiles = (c.n_rows + kTile - 1) / kTile;
-    AttnMisc &M = *c.M;
-
-    if (tid == 0) {
-        tc::mbar_init(&M.q_bar, kSoftThreads);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&M.full_v[i], kProducers);
-            tc::mbar_init(&M.s_full[i], 1);
-            tc::mbar_init(&M.s_free[i], kSoftThreads);
-            tc::mbar_init(&M.pv_done[i], 1);
-            tc::mbar_init(&M.p_full[i], kSoftThreads);
-        }
-        tc::mbar_init(&M.x_full, 1);
-        tc::mbar_init(&M.x_free, 1);
-        tc::mbar_init_fence();
-        if (c.n_tiles > 0) tc::mbar_expect_tx(&M.x_full, kXBytes);  // armed for the first tile's partial
-    }
-    if (warp == kMmaWarp) tc::tmem_alloc(&M.tmem_slot, kTmemCols);
-    tc::fence_before_sync();
-    tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
-    tc::fence_after_sync();
-    c.tmem = M.tmem_slot;
-
-    if (warp < 8) {
-        if (fp8) softmax_rows<true>(c);
-        else softmax_rows<false>(c);
-    } else if (warp < kMmaWarp) {
-        if (fp8) produce<true>(c);
-        else produce<false>(c);
-    } else {
-        if (lane == 0) issue_mmas(c);
-        __syncwarp();
-    }
-    tc::fence_before_sync();
-    tc::cluster_sync();  // no remote shared-memory access after this point
-    if (warp == kMmaWarp) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(c.tmem, kTmemCols);
-    }
+    *reinterpret_cast<float4 *>(E.out + ((int64_t)b * kHeads + h) * kDim + c0) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 }  // namespace
+
 // ---- host planning ---------------------------------------------------------------------
 namespace {
 
@@ -729,27 +793,33 @@ UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
     return up;
 }
 
-// Rows per chunk of a row unit (a multiple of the 64-row tile, at most the
-// 2,048 rows whose positions a CTA stages).  Each candidate is scored by
-// dispatching the pairs in launch order onto 74 pair slots (148 SMs, one CTA
-// per SM), a pair costing, in tile units, its tiles plus a fixed set-up and
-// half a tile per consumer layer (its queries in, its partial out), and by the
-// merge tail, which reads one partial per chunk; the lowest score wins, ties
-// going to longer chunks.
+// Rows per chunk of a row unit: a multiple of the 64-row tile, at most 2,048
+// and at most 63 chunks.  Candidates (the smallest tile multiple giving 1..8
+// chunks, and the powers of two) are scored by dispatching the pairs in launch
+// order onto 74 pair slots (148 SMs, one CTA per SM), a pair costing, in tile
+// units, its tiles plus a fixed set-up and a quarter tile per consumer layer
+// (its queries in, its partial out), plus the merge, which reads one partial
+// per chunk; the lowest score wins, ties going to longer chunks.
 int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
 {
     if (up.row_units.empty() || topk <= 0) return kMaxChunkRows;
     constexpr int kPairSlots = 74;
-    constexpr double kPairSetup = 1.0, kPerLayer = 0.5, kMergePerPart = 0.02;
+    constexpr double kPairSetup = 3.0, kPerLayer = 0.25, kMergePerPart = 0.02;
     const int rmax = std::min(kMaxChunkRows, (topk + kTile - 1) / kTile * kTile);
-    int rmin = kTile;  // at most kMaxParts - 1 chunks
-    while (rmin < rmax && (topk + rmin - 1) / rmin > kMaxParts - 1) rmin *= 2;
     const int win_tiles = (window + kTile - 1) / kTile;
     size_t max_layers = 1;
     for (const auto &g : up.row_units) max_layers = std::max(max_layers, g.size());
+    // candidates: the smallest tile multiple giving 1..8 chunks, and the powers of two
+    std::vector<int> cand;
+    for (int n = 1; n <= 8; ++n) cand.push_back(std::min(rmax, ((topk + n - 1) / n + kTile - 1) / kTile * kTile));
+    for (int r = kTile; r < rmax; r *= 2) cand.push_back(r);
+    std::sort(cand.begin(), cand.end());
+    cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
     int best = rmax;
     double best_score = 1e300;
-    for (int r = rmin; r <= rmax; r *= 2) {
+    for (const int r : cand) {
+        const int chunks = (topk + r - 1) / r;
+        if (chunks > kMaxParts - 1) continue;
         std::priority_queue<double, std::vector<double>, std::greater<double>> slots;
         for (int i = 0; i < kPairSlots; ++i) slots.push(0.0);
         double span = 0.0;
@@ -759,7 +829,6 @@ int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
             slots.push(t0 + cost);
             span = std::max(span, t0 + cost);
         };
-        const int chunks = (topk + r - 1) / r;
         for (int b = 0; b < batch; ++b) {
             for (const auto &g : up.row_units)
                 for (int ch = 0; ch < chunks; ++ch)
@@ -767,17 +836,16 @@ int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
             for (size_t u = 0; u < up.window_units.size(); ++u) dispatch(kPairSetup + kPerLayer + win_tiles);
         }
         const double score = span + kMergePerPart * (double)(chunks + 1) * (double)max_layers;
-        if (score <= best_score) {
+        if (score < best_score - 1e-9 || (score <= best_score + 1e-9 && r > best)) {
             best_score = score;
             best = r;
         }
-        if (r >= rmax) break;
     }
     return best;
 }
 
 struct WsLayout {
-    size_t partials = 0, total = 0;
+    size_t q16 = 0, partials = 0, total = 0;
     int rpc = kMaxChunkRows, chunks = 0, max_parts = 1;
 };
 
@@ -788,12 +856,30 @@ WsLayout ws_layout(const UnitPlan &up, int n_entries, int batch, int topk, int w
     w.chunks = (topk > 0 && !up.row_units.empty()) ? (topk + w.rpc - 1) / w.rpc : 0;
     w.max_parts = std::max(1, w.chunks + (window > 0 ? 1 : 0));
     auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    w.q16 = r256((size_t)n_entries * batch * kHeads * kDim * 2);
     w.partials = r256((size_t)n_entries * batch * w.max_parts * kPartFloats * 4);
-    w.total = w.partials;
+    w.total = w.q16 + w.partials;
     return w;
 }
 
 }  // namespace
+
+int attn_pack_jobs(const AttnPlan &plan, QuantJob *jobs, int cap)
+{
+    int n = 0;
+    uint8_t *q16 = static_cast<uint8_t *>(plan.workspace);
+    for (int e = 0; e < plan.n_entries && n < cap; ++e) {
+        QuantJob j;
+        std::memset(&j, 0, sizeof(j));
+        j.src = plan.entries[e].q;
+        j.dst.format = kFmtPackF16;
+        j.dst.data = q16 + (size_t)e * plan.batch * kHeads * kDim * 2;
+        j.rows_per_seq = kHeads;
+        j.n_seqs = plan.batch;
+        jobs[n++] = j;
+    }
+    return n;
+}
 
 size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window)
 {
@@ -818,7 +904,8 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
     p.rows_per_chunk = wl.rpc;
     p.max_parts = wl.max_parts;
     p.seq_lens = plan.seq_lens;
-    p.partials = reinterpret_cast<float *>(ws);
+    p.q16 = ws;
+    p.partials = reinterpret_cast<float *>(ws + wl.q16);
     for (int e = 0; e < plan.n_entries; ++e) {
         p.entries[e].q = plan.entries[e].q;
         p.entries[e].out = plan.entries[e].out;
@@ -855,7 +942,12 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
     p.n_units = nu;
 
     cudaError_t err = cudaSuccess;
-    if (cta > 0) {
+    if (cta > 0 && !plan.q_packed) {
+        std::vector<QuantJob> jobs((size_t)plan.n_entries);
+        const int n = attn_pack_jobs(plan, jobs.data(), plan.n_entries);
+        err = launch_quantize(jobs.data(), n, flags, stream);
+    }
+    if (err == cudaSuccess && cta > 0) {
         const size_t smem = kOffMisc + sizeof(AttnMisc);
         int dev = 0;
         err = cudaGetDevice(&dev);
@@ -879,7 +971,7 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
         mp.batch = plan.batch;
         mp.max_parts = wl.max_parts;
         mp.partials = p.partials;
-        attn_merge_kernel<<<dim3((unsigned)plan.n_entries, (unsigned)plan.batch, 2u), 256, 0, stream>>>(mp);
+        attn_merge_kernel<<<dim3((unsigned)plan.n_entries, (unsigned)plan.batch, 8u), 256, 0, stream>>>(mp);
         count_launches(1);
         err = cudaGetLastError();
     }

@@ -338,6 +338,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     plan.seq_lens = seq_lens;
     plan.workspace = workspace;
     plan.workspace_bytes = workspace_bytes;
+    plan.q_packed = 0;
     cudaError_t e = launch_attention(plan, fp, static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
 }
@@ -505,6 +506,23 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
         if (d.mode == CSA2_MODE_FULL && d.new_idx_key) add_append(d.new_idx_key, d.idx_keys);
         if (d.new_swa && swa_window > 0) add_append(d.new_swa, d.swa);
     }
+    // the attention's queries to fp16 ride in the same launch
+    std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
+    AttnPlan ap;
+    ap.entries = entries.data();
+    ap.n_entries = n_layers;
+    ap.batch = batch;
+    ap.topk = topk;
+    ap.window = swa_window;
+    ap.seq_lens = seq_lens;
+    ap.workspace = ws + P.part_off;
+    ap.workspace_bytes = P.part_size;
+    ap.q_packed = 1;
+    {
+        const size_t n0 = qjobs.size();
+        qjobs.resize(n0 + (size_t)n_layers);
+        qjobs.resize(n0 + (size_t)attn_pack_jobs(ap, qjobs.data() + n0, n_layers));
+    }
     if (P.n_idx) {
         e = cudaMemsetAsync(ws + P.select_off, 0, select_head_bytes(P.n_idx * batch), s);
         if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
@@ -590,16 +608,6 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "event");
 
     // attention of every layer
-    std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
-    AttnPlan ap;
-    ap.entries = entries.data();
-    ap.n_entries = n_layers;
-    ap.batch = batch;
-    ap.topk = topk;
-    ap.window = swa_window;
-    ap.seq_lens = seq_lens;
-    ap.workspace = ws + P.part_off;
-    ap.workspace_bytes = P.part_size;
     cudaEvent_t mid = (g_n_events > 4) ? static_cast<cudaEvent_t>(g_events[4]) : nullptr;
     e = launch_attention(ap, fp, s, mid);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");

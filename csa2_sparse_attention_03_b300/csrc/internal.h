@@ -33,7 +33,10 @@ struct QuantJob {
     int32_t n_seqs;
     int32_t append_last;      // 1: position = seq_lens[b] - 1 (decode append)
 };
-constexpr int kMaxQuantJobs = 64;
+constexpr int kMaxQuantJobs = 128;
+// Internal job format (not a cache format): rows of 512 fp32 channels to fp16,
+// dst.data = [n_seqs][rows_per_seq][512] fp16 (the attention's query rows).
+constexpr int32_t kFmtPackF16 = 0x7F;
 // Enqueue quantisation of every job (one launch per call).
 cudaError_t launch_quantize(const QuantJob *jobs, int n_jobs, int *flags, cudaStream_t stream);
 
@@ -112,11 +115,17 @@ struct AttnPlan {
     const int32_t *seq_lens;
     void *workspace;       // attn_workspace_bytes() bytes, 256-B aligned
     size_t workspace_bytes;
+    int q_packed;          // 1: the jobs of attn_pack_jobs() already ran on this stream
 };
 
-// Workspace of one launch_attention call: the split partials (per layer,
-// sequence and part: running max and sum per head and half, unnormalised output).
+// Workspace of one launch_attention call: every layer's query rows as fp16,
+// and the split partials (per layer, sequence and part: running max and sum
+// per head and half, unnormalised output).
 size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window);
+// The quantize jobs that pack the plan's queries to fp16 in its workspace (one
+// per entry; returns how many were written, at most `cap`).  A caller that
+// runs them in its own launch sets plan.q_packed.
+int attn_pack_jobs(const AttnPlan &plan, QuantJob *jobs, int cap);
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
                              cudaEvent_t mid_event);
 

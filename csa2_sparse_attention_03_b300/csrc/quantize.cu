@@ -18,11 +18,16 @@ struct QuantBatch {
     int32_t n_jobs;
 };
 
+// The job whose unit range holds `unit` (binary search over the range starts).
 __device__ __forceinline__ int find_job(const QuantBatch &qb, int64_t unit)
 {
-    int j = 0;
-    while (j + 1 < qb.n_jobs && unit >= qb.unit_begin[j + 1]) ++j;
-    return j;
+    int lo = 0, hi = qb.n_jobs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (unit >= qb.unit_begin[mid]) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
 }
 
 // Logical position of row i of sequence b, or -1 if the row is skipped.
@@ -82,7 +87,24 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
         const int64_t u = unit - qb.unit_begin[j];
         const int64_t n_rows = job.rows_per_seq * job.n_seqs;
         const int fmt = job.dst.format;
-        if (fmt == CSA2_FMT_FP4_KV) {
+        if (fmt == kFmtPackF16) {
+            // one 512-channel row (head h of sequence b), lane = 16 channels: fp32 -> fp16
+            // (round to nearest), stored as granules of 8 channels in the order
+            // [b][part 4][granule 16][head 16] that the attention's tensor-memory load reads
+            const int64_t r = u;
+            const int64_t b = r / job.rows_per_seq, hd = r % job.rows_per_seq;
+            float x[16];
+            load16(job.src + r * kDim + lane * 16, x);
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __half2 v = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+                h[i] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            uint4 *d = reinterpret_cast<uint4 *>(job.dst.data) + b * job.rows_per_seq * (kDim / 8) + hd;
+            d[(2 * lane) * job.rows_per_seq] = make_uint4(h[0], h[1], h[2], h[3]);
+            d[(2 * lane + 1) * job.rows_per_seq] = make_uint4(h[4], h[5], h[6], h[7]);
+        } else if (fmt == CSA2_FMT_FP4_KV) {
             const int64_t r = u;
             const int b = (int)(r / job.rows_per_seq);
             const int64_t pos = row_position(job, b, r % job.rows_per_seq);

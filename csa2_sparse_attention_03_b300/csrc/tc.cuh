@@ -141,6 +141,28 @@ __device__ __forceinline__ void bulk_s2peer(uint32_t dst_caddr, const void *src,
         : "memory");
 }
 
+// Bulk copy shared -> global in this thread's bulk async-group (16-B aligned
+// addresses, size a multiple of 16); commit, then wait for the group's source
+// reads (the shared memory may be rewritten) or for its completion.
+__device__ __forceinline__ void bulk_s2g(void *gdst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
+// 2^x by the special-function unit (ex2.approx.ftz: relative error about
+// 2^-22, results below the normal range flush to zero).
+__device__ __forceinline__ float exp2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // tensor core and bulk-copy engines (the async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -301,6 +323,17 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Arrive once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// (cluster ranks) when every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 }  // namespace tc

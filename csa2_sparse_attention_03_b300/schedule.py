@@ -231,6 +231,25 @@ class DecodeStep:
         csa2_decode_layers(self.descs, self.B, self.seq_lens, self.Lmax, self.topk, self.pool_len, self.window,
                            self.workspace, stream=stream, arr=self.arr)
 
+    def capture(self, stream, host_in=None, host_out=None):
+        """Capture one decode step in a CUDA graph on `stream` and return it.
+
+        With pinned host buffers `host_in` (the size of ``step_inputs()[0]``)
+        and `host_out` (the size of ``step_outputs()[0]``), the graph also
+        copies the step's inputs in from the host first and its outputs back
+        after, so one replay is a whole serving step.  The step's kernels are
+        captured as launched by ``csa2_decode_layers``."""
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if host_in is not None:
+                self.arena_in.copy_(host_in, non_blocking=True)
+            self.run(stream=stream)
+            if host_out is not None:
+                host_out.copy_(self.arena_out, non_blocking=True)
+        return g
+
     # ---- inputs/outputs moved per step in the end-to-end measurement ----
     def step_inputs(self):
         """What a caller supplies per decode step (queries, indexer queries,
