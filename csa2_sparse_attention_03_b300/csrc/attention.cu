@@ -793,6 +793,25 @@ UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
     return up;
 }
 
+struct WsLayout {
+    size_t q16 = 0, partials = 0, total = 0;
+    int rpc = kMaxChunkRows, chunks = 0, max_parts = 1;
+};
+
+// Workspace layout of a launch that splits row units into chunks of `rpc` rows.
+WsLayout layout_for(const UnitPlan &up, int n_entries, int batch, int topk, int window, int rpc)
+{
+    WsLayout w;
+    w.rpc = rpc;
+    w.chunks = (topk > 0 && !up.row_units.empty()) ? (topk + w.rpc - 1) / w.rpc : 0;
+    w.max_parts = std::max(1, w.chunks + (window > 0 ? 1 : 0));
+    auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    w.q16 = r256((size_t)n_entries * batch * kHeads * kDim * 2);
+    w.partials = r256((size_t)n_entries * batch * w.max_parts * kPartFloats * 4);
+    w.total = w.q16 + w.partials;
+    return w;
+}
+
 // Rows per chunk of a row unit: a multiple of the 64-row tile, at most 2,048
 // and at most 63 chunks.  Candidates (the smallest tile multiple giving 1..8
 // chunks, and the powers of two) are scored by dispatching the pairs in launch
@@ -800,7 +819,7 @@ UnitPlan group_units(const AttnEntry *entries, int n_entries, int window)
 // units, its tiles plus a fixed set-up and a quarter tile per consumer layer
 // (its queries in, its partial out), plus the merge, which reads one partial
 // per chunk; the lowest score wins, ties going to longer chunks.
-int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
+int rows_per_chunk(const UnitPlan &up, int n_entries, int batch, int topk, int window, size_t budget)
 {
     if (up.row_units.empty() || topk <= 0) return kMaxChunkRows;
     constexpr int kPairSlots = 74;
@@ -815,11 +834,12 @@ int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
     for (int r = kTile; r < rmax; r *= 2) cand.push_back(r);
     std::sort(cand.begin(), cand.end());
     cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
-    int best = rmax;
+    int best = -1, smallest = rmax;
     double best_score = 1e300;
     for (const int r : cand) {
         const int chunks = (topk + r - 1) / r;
         if (chunks > kMaxParts - 1) continue;
+        if (layout_for(up, n_entries, batch, topk, window, r).total > budget) continue;
         std::priority_queue<double, std::vector<double>, std::greater<double>> slots;
         for (int i = 0; i < kPairSlots; ++i) slots.push(0.0);
         double span = 0.0;
@@ -841,25 +861,13 @@ int rows_per_chunk(const UnitPlan &up, int batch, int topk, int window)
             best = r;
         }
     }
-    return best;
+    return best > 0 ? best : smallest;  // nothing fits the budget: the smallest workspace
 }
 
-struct WsLayout {
-    size_t q16 = 0, partials = 0, total = 0;
-    int rpc = kMaxChunkRows, chunks = 0, max_parts = 1;
-};
-
-WsLayout ws_layout(const UnitPlan &up, int n_entries, int batch, int topk, int window)
+// The launch's layout: the fastest chunking whose workspace fits `budget`.
+WsLayout ws_layout(const UnitPlan &up, int n_entries, int batch, int topk, int window, size_t budget)
 {
-    WsLayout w;
-    w.rpc = rows_per_chunk(up, batch, topk, window);
-    w.chunks = (topk > 0 && !up.row_units.empty()) ? (topk + w.rpc - 1) / w.rpc : 0;
-    w.max_parts = std::max(1, w.chunks + (window > 0 ? 1 : 0));
-    auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
-    w.q16 = r256((size_t)n_entries * batch * kHeads * kDim * 2);
-    w.partials = r256((size_t)n_entries * batch * w.max_parts * kPartFloats * 4);
-    w.total = w.q16 + w.partials;
-    return w;
+    return layout_for(up, n_entries, batch, topk, window, rows_per_chunk(up, n_entries, batch, topk, window, budget));
 }
 
 }  // namespace
@@ -881,17 +889,17 @@ int attn_pack_jobs(const AttnPlan &plan, QuantJob *jobs, int cap)
     return n;
 }
 
-size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window)
+size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window, size_t budget)
 {
     const UnitPlan up = group_units(entries, n_entries, window);
-    return ws_layout(up, n_entries, batch, topk, window).total;
+    return ws_layout(up, n_entries, batch, topk, window, budget).total;
 }
 
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream, cudaEvent_t mid_event)
 {
     if (plan.n_entries <= 0 || plan.n_entries > kMaxAttnEntries) return cudaErrorInvalidValue;
     const UnitPlan up = group_units(plan.entries, plan.n_entries, plan.window);
-    const WsLayout wl = ws_layout(up, plan.n_entries, plan.batch, plan.topk, plan.window);
+    const WsLayout wl = ws_layout(up, plan.n_entries, plan.batch, plan.topk, plan.window, plan.workspace_bytes);
     if (plan.workspace_bytes < wl.total || (int)(up.row_units.size() + up.window_units.size()) > kMaxUnits)
         return cudaErrorInvalidValue;
     uint8_t *ws = static_cast<uint8_t *>(plan.workspace);

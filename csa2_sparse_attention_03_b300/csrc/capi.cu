@@ -135,6 +135,22 @@ size_t select_head_bytes(int n_rows) { return select_hist_bytes(n_rows); }
 
 }  // namespace
 
+namespace csa2 {
+
+size_t sparse_attn_workspace_within(int32_t batch, int32_t topk, int32_t swa_window, size_t budget)
+{
+    if (batch <= 0 || topk < 0 || swa_window < 0) return 0;
+    static const int32_t any_index = 0;  // stands for "an index list is given"
+    AttnEntry en;
+    memset(&en, 0, sizeof(en));
+    en.has_kv = topk > 0 ? 1 : 0;
+    en.idx = topk > 0 ? &any_index : nullptr;
+    en.has_swa = swa_window > 0 ? 1 : 0;
+    return attn_workspace_bytes(&en, 1, batch, topk, swa_window, budget);
+}
+
+}  // namespace csa2
+
 extern "C" {
 
 int32_t csa2_version(void) { return 100; }
@@ -282,14 +298,7 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
 
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window)
 {
-    if (batch <= 0 || topk < 0 || swa_window < 0) return 0;
-    static const int32_t any_index = 0;  // stands for "an index list is given"
-    AttnEntry en;
-    memset(&en, 0, sizeof(en));
-    en.has_kv = topk > 0 ? 1 : 0;
-    en.idx = topk > 0 ? &any_index : nullptr;
-    en.has_swa = swa_window > 0 ? 1 : 0;
-    return attn_workspace_bytes(&en, 1, batch, topk, swa_window);
+    return csa2::sparse_attn_workspace_within(batch, topk, swa_window, SIZE_MAX);
 }
 
 csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const float *q, int32_t batch,
@@ -327,7 +336,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     en.lse = lse;
     en.has_kv = idx ? 1 : 0;
     en.has_swa = swa_window > 0 ? 1 : 0;
-    st = check_ws(workspace, workspace_bytes, attn_workspace_bytes(&en, 1, batch, eff_topk, swa_window));
+    st = check_ws(workspace, workspace_bytes, attn_workspace_bytes(&en, 1, batch, eff_topk, swa_window, workspace_bytes));
     if (st) return st;
     AttnPlan plan;
     plan.entries = &en;

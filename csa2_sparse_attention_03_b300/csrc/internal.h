@@ -113,15 +113,20 @@ struct AttnPlan {
     int topk;              // rows per index list (0 when no entry has one)
     int window;
     const int32_t *seq_lens;
-    void *workspace;       // attn_workspace_bytes() bytes, 256-B aligned
+    void *workspace;       // at least attn_workspace_bytes(..., workspace_bytes) bytes, 256-B aligned
     size_t workspace_bytes;
     int q_packed;          // 1: the jobs of attn_pack_jobs() already ran on this stream
 };
 
 // Workspace of one launch_attention call: every layer's query rows as fp16,
 // and the split partials (per layer, sequence and part: running max and sum
-// per head and half, unnormalised output).
-size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window);
+// per head and half, unnormalised output).  The size of the fastest chunking
+// whose workspace is at most `budget` (or of the smallest, when none is);
+// launch_attention plans within plan.workspace_bytes the same way.
+size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window,
+                            size_t budget = SIZE_MAX);
+// csa2_sparse_attn's workspace for one layer, planned within `budget`.
+size_t sparse_attn_workspace_within(int32_t batch, int32_t topk, int32_t swa_window, size_t budget);
 // The quantize jobs that pack the plan's queries to fp16 in its workspace (one
 // per entry; returns how many were written, at most `cap`).  A caller that
 // runs them in its own launch sets plan.q_packed.

@@ -45,7 +45,7 @@ extern "C" csa2_status csa2_sparse_attn_noalloc(const csa2_cache *kv, const csa2
                                                 int32_t topk, int32_t swa_window, float *out, float *lse,
                                                 void *stream)
 {
-    const size_t need = csa2_sparse_attn_workspace(batch, idx ? topk : 0, swa_window);
+    const size_t need = csa2::sparse_attn_workspace_within(batch, idx ? topk : 0, swa_window, kNoAllocScratchBytes);
     if (need > kNoAllocScratchBytes)
         return csa2::set_error(CSA2_ERR_UNSUPPORTED,
                                "csa2_sparse_attn_noalloc: this call needs %zu bytes of scratch, more than the "

@@ -167,7 +167,11 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
  *   swa_window  window length in tokens (0 = no window branch)
  *   out         device fp32 [batch][16][512];  lse: optional [batch][16]
  * Numerics: q and softmax weights enter the tensor cores as fp16 (the FP4 and
- * FP8 values are exact in fp16), accumulation and softmax in fp32. */
+ * FP8 values are exact in fp16), accumulation and softmax in fp32; the
+ * weights' exponential is the hardware ex2 (relative error about 2^-22).
+ * Workspace: csa2_sparse_attn_workspace() is the size of the fastest plan; a
+ * smaller workspace is accepted down to the smallest plan's size (the rows are
+ * then split into fewer, longer chunks), below it CSA2_ERR_WORKSPACE. */
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window);
 csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                              int32_t batch, int32_t n_heads, int32_t head_dim,
@@ -182,16 +186,17 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
  * a plugin living inside another runtime's allocator.  The paper has no
  * counterpart; this is a deployment convenience of this library.
  * Arguments, layouts, numerics and error codes are those of
- * csa2_sparse_attn minus the workspace.  The split partials go to a 4 MiB
- * array the library holds on every device that loads it, until exit; a call
- * whose partials need more than that (csa2_sparse_attn_workspace() > 4 MiB,
- * e.g. beyond about 24 sequences at topk 2048) returns CSA2_ERR_UNSUPPORTED
- * with a message.  It calls no allocator.  Every call on a device shares the
- * array, so calls that overlap on the GPU (other streams, other threads) race
- * and give wrong results: serialise them.  Each call rewrites every partial
- * it reads, so nothing needs clearing between calls.  The first call on each
- * device looks the array's device address up (with that device current);
- * make that first call before any stream capture. */
+ * csa2_sparse_attn minus the workspace.  The fp16 queries and the split
+ * partials go to a 4 MiB array the library holds on every device that loads
+ * it, until exit, planned to fit it (the fastest plan that fits); a call for
+ * which even the smallest plan needs more (beyond about 50 sequences)
+ * returns CSA2_ERR_UNSUPPORTED with a message.  It calls no allocator.  Every
+ * call on a device shares the array, so calls that overlap on the GPU (other
+ * streams, other threads) race and give wrong results: serialise them.  Each
+ * call rewrites everything it reads there, so nothing needs clearing between
+ * calls.  The first call on each device looks the array's device address up
+ * (with that device current); make that first call before any stream
+ * capture. */
 csa2_status csa2_sparse_attn_noalloc(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                                      int32_t batch, int32_t n_heads, int32_t head_dim,
                                      const int32_t *seq_lens, int32_t max_seq_len,
