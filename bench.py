@@ -319,6 +319,32 @@ def cpu_baseline(w, budget_s):
 
 
 # ---------------------------------------------------------------------------
+# ranks: one replica of the workload per GPU
+# ---------------------------------------------------------------------------
+
+def replica_seed(seed, rank):
+    """Workload seed of a rank's replica (independent draws per rank)."""
+    return seed + 100000 * rank
+
+
+def max_over_ranks(pg, values, device="cpu"):
+    """Element-wise max of this rank's floats over the process group (the
+    slowest rank's times); the values themselves without a group."""
+    if pg is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_value(world, batch, ms_per_step):
+    """Query tokens per second of all ranks together: every rank decodes
+    `batch` sequences per step, a step lasting the slowest rank's time."""
+    return world * batch / (ms_per_step * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle, timed
 # ---------------------------------------------------------------------------
 
@@ -392,8 +418,7 @@ def run_csa2(args):
 
     # each rank runs an independent replica of the workload (sequences are
     # independent units; nothing is exchanged on the data path)
-    if rank:
-        w.seed += 100000 * rank
+    w.seed = replica_seed(w.seed, rank)
     step = DecodeStep(w, device=dev, fill="device")
     stream = torch.cuda.Stream(device=dev)
     props = torch.cuda.get_device_properties(dev)
@@ -474,13 +499,9 @@ def run_csa2(args):
             phase_sum[i] += phases[i]
     if pg:
         pg.barrier()
-    ms_total = sum(times)
-    if pg:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(pg, [sum(times)], dev)[0]
     ms = ms_total / args.steps
-    value = world * w.batch / (ms * 1e-3)
+    value = whole_job_value(world, w.batch, ms)
 
     # dominant kernel: the phase with the largest share
     names = ["append (quantize)", "scan", "select", "level-1 scan+select", "attention", "merge"]
@@ -546,12 +567,8 @@ def run_csa2(args):
             e2e_step(False, direct=True)
         et = [e2e_step(True) for _ in range(args.e2e_steps)]
         dt = [e2e_step(True, direct=True) for _ in range(args.e2e_steps)]
-        e_ms, d_ms = sum(et) / len(et), sum(dt) / len(dt)
-        if pg:
-            t = torch.tensor([e_ms, d_ms], dtype=torch.float64, device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms, d_ms = float(t[0].item()), float(t[1].item())
-        e2e = {"value": world * w.batch / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
+        e_ms, d_ms = max_over_ranks(pg, [sum(et) / len(et), sum(dt) / len(dt)], dev)
+        e2e = {"value": whole_job_value(world, w.batch, e_ms), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e_ms,
                "how": "DecodeStep.capture: one CUDA graph per step that copies the pinned host input arena "
                       "in, runs csa2_decode_layers and copies the output arena (out, lse, indices) back; "
