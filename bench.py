@@ -504,6 +504,49 @@ def run_csa2(args):
         phased_tot += tot
         for i in range(n_ph):
             phase_sum[i] += phases[i]
+
+    # the layer-sequential order (per-layer entry points, as a model calls them),
+    # timed the same way from its own graph; one GPU only (a rank failing here
+    # must not leave the others in a collective)
+    st0, fl0 = csa2.csa2_check_device(stream)
+    if st0 != 0:
+        raise RuntimeError(f"device flags after the timed steps: status {st0}, bits {fl0}")
+    seq = None
+    if pg is None:
+        try:
+            with torch.cuda.stream(stream):
+                step.run_sequential(stream=stream)
+                stream.synchronize()
+                n0s = csa2.csa2_launch_count()
+                g_seq = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_seq, stream=stream):
+                    step.run_sequential(stream=stream)
+                seq_launches = csa2.csa2_launch_count() - n0s
+            torch.cuda.synchronize()
+
+            def seq_step():
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                    torch.sum(flush_rd, dim=0, out=flush_sink)
+                    t_start.record(stream)
+                    g_seq.replay()
+                    t_end.record(stream)
+                t_end.synchronize()
+                return t_start.elapsed_time(t_end)
+
+            for _ in range(3):
+                seq_step()
+            st_ms = [seq_step() for _ in range(max(1, min(args.steps, 100)))]
+            s_ms = sum(st_ms) / len(st_ms)
+            seq = {"ms_per_step": s_ms, "value": whole_job_value(world, w.batch, s_ms), "unit": UNIT,
+                   "launches_per_step": int(seq_launches),
+                   "how": "each layer in schedule order: its appends, its indexing, its attention, through "
+                          "csa2_quantize_kv / csa2_index_topk / csa2_sparse_attn, one CUDA graph per step"}
+            sst, sfl = csa2.csa2_check_device(stream)
+            if sst != 0:
+                seq = {"error": f"device flags after the layer-sequential steps: status {sst}, bits {sfl}"}
+        except Exception as exc:  # reported, never fatal to the main measurement
+            seq = {"error": repr(exc)[:300]}
     if pg:
         pg.barrier()
     ms_total = max_over_ranks(pg, [sum(times)], dev)[0]
@@ -603,6 +646,7 @@ def run_csa2(args):
                     "peak_source": f"{peak_kind} copy bandwidth"},
             "phases_ms": {names[i]: ph_ms[i] for i in range(n_ph)},
             "phased_ms_per_step": phased_tot / n_phased,
+            "layer_sequential": seq,
             "roofline": roof,
             "gpu_launches": int(launches_per_step) * args.steps,
             "launches_per_step": int(launches_per_step),

@@ -19,8 +19,8 @@ import numpy as np
 import torch
 
 from . import (FMT_FP4_IDX, FMT_FP4_KV, FMT_FP8_SWA, MODE_FULL, MODE_REINDEX, MODE_REUSE, MODE_SWA_ONLY,
-               Cache, csa2_cache, csa2_decode_layers, csa2_decode_layers_workspace, csa2_layer_desc,
-               csa2_quantize_kv, layer_array, synth)
+               Cache, csa2_cache, csa2_decode_layers, csa2_decode_layers_workspace, csa2_index_topk,
+               csa2_layer_desc, csa2_quantize_kv, csa2_sparse_attn, layer_array, load, synth)
 
 _MODE = {synth.FULL: MODE_FULL, synth.REINDEX: MODE_REINDEX, synth.REUSE: MODE_REUSE,
          synth.SWA_ONLY: MODE_SWA_ONLY}
@@ -249,6 +249,49 @@ class DecodeStep:
             if host_out is not None:
                 host_out.copy_(self.arena_out, non_blocking=True)
         return g
+
+    def run_sequential(self, stream=None):
+        """The same step in the layer-sequential order a model runs it in: for
+        each layer in schedule order its appends, then its indexing (Full, or
+        Reindex over its Full layer's keys or pool), then its attention, each
+        through the per-layer entry points (csa2_quantize_kv, csa2_index_topk,
+        csa2_sparse_attn).  Writes the same outputs as ``run``; the attention's
+        chunking is planned per layer, so outputs agree within the attention
+        tolerance rather than bit for bit.  Graph-capturable."""
+        if not hasattr(self, "_seq_ws"):
+            lib = load()
+            need = max(int(lib.csa2_index_topk_workspace(self.B, self.Lmax, self.pool_len, self.topk,
+                                                           self.pool_len)),
+                       int(lib.csa2_sparse_attn_workspace(self.B, self.topk, self.window)), 1)
+            self._seq_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+            self._seq_last = (self.seq_lens - 1).clamp(min=0)
+        ws, last = self._seq_ws, self._seq_last
+        for l, ly in enumerate(self.w.layers):
+            if ly.mode == synth.FULL and ("kv", l) in self.new_rows:
+                kv, ik = self.caches[l]
+                csa2_quantize_kv(self.new_rows[("kv", l)][:, None], kv, start_pos=last, seq_lens=self.seq_lens,
+                                 stream=stream)
+                csa2_quantize_kv(self.new_rows[("idxk", l)][:, None], ik, start_pos=last, seq_lens=self.seq_lens,
+                                 stream=stream)
+            if ("swa", l) in self.new_rows and self.window > 0:
+                csa2_quantize_kv(self.new_rows[("swa", l)][:, None], self.swa[l], start_pos=last,
+                                 seq_lens=self.seq_lens, stream=stream)
+            if ly.mode == synth.FULL:
+                csa2_index_topk(MODE_FULL, self.caches[l][1], self.q_idx[l], self.wts[l], self.seq_lens, self.Lmax,
+                                self.topk, out_idx=self.idx[l], out_pool=self.pool.get(l), workspace=ws,
+                                stream=stream)
+            elif ly.mode == synth.REINDEX:
+                pool = self.pool.get(ly.kv_src) if ly.use_pool else None
+                csa2_index_topk(MODE_REINDEX, self.caches[ly.kv_src][1], self.q_idx[l], self.wts[l], self.seq_lens,
+                                self.Lmax, self.topk, pool=pool, out_idx=self.idx[l], workspace=ws, stream=stream)
+            if ly.mode == synth.SWA_ONLY:
+                kv, idx, topk = None, None, 0
+            else:
+                kv = self.caches[ly.kv_src][0]
+                idx = self.idx[l] if ly.mode in (synth.FULL, synth.REINDEX) else self.idx[ly.idx_src]
+                topk = self.topk
+            csa2_sparse_attn(kv, self.swa[l], self.q[l], self.seq_lens, self.Lmax, idx, topk, self.window,
+                             out=self.out[l], lse=self.lse[l], workspace=ws, stream=stream)
 
     # ---- inputs/outputs moved per step in the end-to-end measurement ----
     def step_inputs(self):
