@@ -511,6 +511,40 @@ def run_csa2(args):
     st0, fl0 = csa2.csa2_check_device(stream)
     if st0 != 0:
         raise RuntimeError(f"device flags after the timed steps: status {st0}, bits {fl0}")
+
+    # the quantise step's cache build: one Full layer's main KV and indexer keys
+    # over the whole context (fp32 rows in, packed rows out), L2 flushed first
+    build = None
+    if pg is None:
+        try:
+            Lb = int(w.max_len)
+            build = {}
+            for kind, fmt, ch, row in (("main_kv", csa2.FMT_FP4_KV, 512, KV_ROW), ("indexer_keys", csa2.FMT_FP4_IDX, 64,
+                                                                                   IDX_ROW)):
+                src = torch.empty((1, Lb, ch), dtype=torch.float32, device=dev).normal_()
+                cache = csa2.Cache.contiguous(fmt, 1, (Lb + 63) // 64 * 64, dev)
+                b_ms = []
+                for it in range(6):
+                    with torch.cuda.stream(stream):
+                        flush.fill_(1)
+                        torch.sum(flush_rd, dim=0, out=flush_sink)
+                        t_start.record(stream)
+                        csa2.csa2_quantize_kv(src, cache, stream=stream)
+                        t_end.record(stream)
+                    t_end.synchronize()
+                    if it >= 3:
+                        b_ms.append(t_start.elapsed_time(t_end))
+                ms_b = sum(b_ms) / len(b_ms)
+                nbytes = Lb * (ch * 4 + row)
+                build[kind] = {"rows": Lb, "ms": ms_b, "algorithmic_bytes": nbytes,
+                               "achieved_gbs": nbytes / (ms_b * 1e-3) / 1e9,
+                               "frac": nbytes / (ms_b * 1e-3) / 1e9 / peaks()[0]}
+                del src, cache
+            bst, bfl = csa2.csa2_check_device(stream)
+            if bst != 0:
+                build = {"error": f"device flags after the cache builds: status {bst}, bits {bfl}"}
+        except Exception as exc:  # reported, never fatal to the main measurement
+            build = {"error": repr(exc)[:300]}
     seq = None
     if pg is None:
         try:
@@ -647,6 +681,7 @@ def run_csa2(args):
             "phases_ms": {names[i]: ph_ms[i] for i in range(n_ph)},
             "phased_ms_per_step": phased_tot / n_phased,
             "layer_sequential": seq,
+            "cache_build": build,
             "roofline": roof,
             "gpu_launches": int(launches_per_step) * args.steps,
             "launches_per_step": int(launches_per_step),
