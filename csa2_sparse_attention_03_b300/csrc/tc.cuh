@@ -85,20 +85,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v)
-{
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(caddr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier (remote) shared-memory writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_caddr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_caddr) : "memory");
-}
-
 // try_wait that acquires at cluster scope (the arrivals came from another CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
 {
@@ -119,7 +105,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return false;
 }
 
-// ---- bulk asynchronous copy (global -> shared), completing on an mbarrier ---
+// ---- bulk asynchronous copies ---------------------------------------------
+// global -> shared, completing on an mbarrier
 __device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
 {
     asm volatile(
@@ -166,21 +153,6 @@ __device__ __forceinline__ float exp2_fast(float x)
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // tensor core and bulk-copy engines (the async proxy).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-
-// ---- cp.async (16-byte granules) -------------------------------------------
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-
-// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
-{
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
-}
 
 // ---- tensor memory ---------------------------------------------------------
 // Allocation and release are warp-wide; the address lands in *slot.
@@ -239,35 +211,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const float v[32])
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-}
-
-// 16 consecutive 32-bit columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, float v[16])
-{
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(addr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t addr, const float v[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-            addr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
