@@ -7,24 +7,32 @@ FP8 window ring, indexer scoring and Top-K of the Full and Reindex layers,
 and the gather-attention (FP4 selected rows + FP8 window) of every layer,
 over the static 40-layer schedule (4 Full, 4 Reindex, 30 Reuse, 2 SWA-only)
 at batch 1, context 131,072 and Top-K 2,048 (the workload the headline
-metric is quoted on).  The step runs through ``csa2_decode_layers``, captured
-once in a CUDA graph and replayed.
+metric is quoted on; ``--config`` picks another).
+
+Headline: the *layer-sequential* step -- one ``csa2_decode_layer`` call per
+layer in schedule order, the order a model runs it in (layer l+1's queries
+do not exist before layer l is done) -- captured once in a CUDA graph and
+replayed.  The *phased* step (``csa2_decode_layers``: every layer's indexing,
+then every attention, valid only when all queries are known up front) is
+reported beside it under ``phased``.
 
 Timing: W untimed warm-up steps, then K timed steps.  Before every step a
-256 MB buffer is written to flush L2 (outside the timed events); each step is
-bracketed by CUDA events on the stream it runs on.  Phase events recorded by
-the library inside the graph give each kernel's duration.
+buffer of twice the L2 size is written and another read (outside the timed
+events); each step is bracketed by CUDA events on the stream it runs on.
+The attention and indexing kernels are also timed alone (every layer's
+attention, or every indexing layer, in one graph) for the roofline.
 
 Output: one JSON line (rank 0).  ``value`` = query-tokens/s (batch / step
 time); ``hbm`` gives the algorithmic bytes per step and the achieved GB/s
-against the measured copy bandwidth; ``roofline`` covers the dominant kernel;
-``e2e`` repeats the metric through the Python binding of the C interface with
-host buffers, copying the step's inputs in and outputs out every step;
-``cpu_baseline`` times the CPU oracle on a bounded sample of the workload.
+against the measured copy bandwidth; ``roofline`` covers the dominant
+kernel; ``e2e`` repeats the metric through the Python binding of the C
+interface with host buffers, copying the step's inputs in and outputs out
+every step; ``cpu_baseline`` times the CPU oracle on one whole decode step of
+the same workload (one thread and all host cores).
 
 ``--impl reference`` times the CPU oracle instead (there is no runnable
-reference implementation of this method): each step is one layer of each mode
-at the full context, composed into the 40-layer schedule.
+reference implementation of this method): each step is one whole decode step
+of the workload on the host cores.
 """
 from __future__ import annotations
 
@@ -35,6 +43,8 @@ import statistics
 import subprocess
 import sys
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -79,75 +89,94 @@ def peaks():
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
-def step_bytes(w):
-    """Algorithmic bytes of one decode step, by part.
-
-    scan:   36 B per (position, key pass).  A Full layer and the pool-free
-            Reindex layer over the same keys share one pass in this step
-            (their queries are both known when the step starts), so a
-            position of such a pair is counted once; pool-restricted
-            Reindex layers read 36 B (+4 B pool entry) per pool position.
-    gather: 288 B per selected row per non-SWA-only layer.
-    swa:    516 B per window row per layer.
-    io:     q and out (32 KiB each), lse, indexer q and weights, indices
-            written (4 B per Top-K / pool entry) and read by attention, and
-            the appended rows (fp32 read, packed write).
-    """
+def _layer_parts(w, ly):
+    """Bytes one layer moves in the layer-sequential order, by part: its key
+    pass (36 B per position scored, or 36 B + 4 B per pool entry), its
+    gathered rows (288 B per selected row), its window rows (516 B), and io
+    (q, out, lse, the indexer query and weights, indices written and read,
+    the appended rows: fp32 in, packed out)."""
     from csa2_sparse_attention_03_b300 import synth
     B = w.batch
     Ls = [int(x) for x in w.seq_lens]
+    p = dict(scan=0, gather=0, swa=0, io=0)
+    if ly.mode in (synth.FULL, synth.REINDEX):
+        if ly.mode == synth.REINDEX and ly.use_pool:
+            p["scan"] += B * w.pool_len * (IDX_ROW + 4)
+        else:
+            p["scan"] += IDX_ROW * sum(Ls)
+        p["io"] += B * (4 * 64 * 4 + 16) + B * w.topk * 4
+        if ly.mode == synth.FULL and w.pool_len:
+            p["io"] += B * w.pool_len * 4
+    if ly.mode != synth.SWA_ONLY:
+        p["gather"] += sum(min(w.topk, L) for L in Ls) * KV_ROW
+        p["io"] += B * w.topk * 4
+    p["swa"] += sum(min(w.window, L) for L in Ls) * SWA_ROW
+    p["io"] += B * (Q_BYTES + OUT_BYTES + LSE_BYTES)
+    if ly.mode == synth.FULL and w.append:
+        p["io"] += B * (512 * 4 + KV_ROW + 64 * 4 + IDX_ROW)
+    if w.append:
+        p["io"] += B * (512 * 4 + SWA_ROW)
+    return p
+
+
+def step_bytes(w):
+    """Algorithmic bytes of one decode step in the layer-sequential order, by
+    part: every Full and every Reindex layer reads its keys (each key pass is
+    counted), every non-SWA-only layer gathers its selected rows, every layer
+    reads its window, q, out, indices and appended rows."""
     parts = dict(scan=0, gather=0, swa=0, io=0)
-    layers = w.layers
-    paired = set()
-    for l, ly in enumerate(layers):
-        if ly.mode == synth.FULL:
-            partner = [r for r in range(len(layers)) if layers[r].mode == synth.REINDEX
-                       and layers[r].kv_src == l and not layers[r].use_pool]
-            n_pass = 1 + max(0, len(partner) - 1)
-            paired.update(partner[:1])
-            parts["scan"] += n_pass * IDX_ROW * sum(Ls)
-            parts["io"] += B * (4 * 64 * 4 + 16)       # q_idx + w
-            parts["io"] += B * w.topk * 4               # indices written
-            if w.pool_len:
-                parts["io"] += B * w.pool_len * 4
-        elif ly.mode == synth.REINDEX:
-            if ly.use_pool:
-                parts["scan"] += B * w.pool_len * (IDX_ROW + 4)
-            parts["io"] += B * (4 * 64 * 4 + 16) + B * w.topk * 4
-        if ly.mode != synth.SWA_ONLY:
-            sel = sum(min(w.topk, L) for L in Ls)
-            parts["gather"] += sel * KV_ROW
-            parts["io"] += B * w.topk * 4               # indices read
-        parts["swa"] += sum(min(w.window, L) for L in Ls) * SWA_ROW
-        parts["io"] += B * (Q_BYTES + OUT_BYTES + LSE_BYTES)
-        # appends: the new token's fp32 rows in, packed rows out
-        if ly.mode == synth.FULL and w.append:
-            parts["io"] += B * (512 * 4 + KV_ROW + 64 * 4 + IDX_ROW)
-        if w.append:
-            parts["io"] += B * (512 * 4 + SWA_ROW)
+    for ly in w.layers:
+        for k, v in _layer_parts(w, ly).items():
+            parts[k] += v
     parts["total"] = sum(parts.values())
     return parts
 
 
-def attention_bytes(w):
-    """Algorithmic bytes of the attention kernel (one launch covers every layer)."""
+def fused_step_bytes(w):
+    """The same step as the phased launch sequence reads it: a Full layer and
+    its pool-free Reindex partner score in one key pass, and two layers that
+    share a selection (the attention's unit) gather its rows once."""
     from csa2_sparse_attention_03_b300 import synth
-    Ls = [int(x) for x in w.seq_lens]
+    parts = step_bytes(w)
+    layers = w.layers
     B = w.batch
-    tot = 0
-    for ly in w.layers:
-        if ly.mode != synth.SWA_ONLY:
-            tot += sum(min(w.topk, L) for L in Ls) * KV_ROW + B * w.topk * 4
-        tot += sum(min(w.window, L) for L in Ls) * SWA_ROW
-        tot += B * (Q_BYTES + OUT_BYTES + LSE_BYTES)
-    return tot
+    Ls = [int(x) for x in w.seq_lens]
+    for l, ly in enumerate(layers):
+        if ly.mode == synth.REINDEX and not ly.use_pool:
+            parts["scan"] -= IDX_ROW * sum(Ls)  # shares its Full layer's pass
+    groups = {}
+    for l, ly in enumerate(layers):
+        if ly.mode == synth.SWA_ONLY:
+            continue
+        src = l if ly.mode in (synth.FULL, synth.REINDEX) else ly.idx_src
+        groups[src] = groups.get(src, 0) + 1
+    sel = sum(min(w.topk, L) for L in Ls) * KV_ROW
+    for n in groups.values():
+        parts["gather"] -= (n - (n + 1) // 2) * sel  # units of two layers
+    parts["total"] = parts["scan"] + parts["gather"] + parts["swa"] + parts["io"]
+    return parts
 
 
-def scan_bytes(w):
-    p = step_bytes(w)
+def attention_launch_bytes(w, ly):
+    """One layer's attention launch: selected rows, window rows, q/out/lse,
+    indices read, the appended window row."""
+    p = _layer_parts(w, ly)
     from csa2_sparse_attention_03_b300 import synth
-    n_idx = sum(1 for ly in w.layers if ly.mode in (synth.FULL, synth.REINDEX))
-    return p["scan"] + n_idx * w.batch * (4 * 64 * 4 + 16)
+    B = w.batch
+    io = B * (Q_BYTES + OUT_BYTES + LSE_BYTES) + (B * w.topk * 4 if ly.mode != synth.SWA_ONLY else 0)
+    return p["gather"] + p["swa"] + io
+
+
+def index_launch_bytes(w, ly):
+    """One indexing layer's launch: its key pass, indexer q and weights,
+    indices (and pool) written, a Full layer's appended row and key."""
+    from csa2_sparse_attention_03_b300 import synth
+    p = _layer_parts(w, ly)
+    B = w.batch
+    io = B * (4 * 64 * 4 + 16) + B * w.topk * 4
+    if ly.mode == synth.FULL:
+        io += (B * w.pool_len * 4 if w.pool_len else 0) + (B * (512 * 4 + KV_ROW + 64 * 4 + IDX_ROW) if w.append else 0)
+    return p["scan"] + io
 
 
 # ---------------------------------------------------------------------------
@@ -215,107 +244,98 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
 
-class OracleSample:
-    """One layer of each mode at the workload's full context, on the CPU oracle.
+class OracleStep:
+    """One whole decode step of a workload on the CPU oracle.
 
-    Set-up (not timed) draws the inputs from the seeded streams and quantises
-    them with the oracle; only what the sampled layers read is quantised (the
-    indexer keys of the whole context, the main-KV rows the selections and
-    windows touch).  ``run()`` times the oracle's per-layer decode work:
-    scoring + Top-K (Full, Reindex), gather-dequantise-attend (every mode).
-    """
+    Set-up (not timed) draws the inputs from the seeded host streams and
+    quantises the caches with the oracle, using every host core (the result
+    does not depend on the thread count).  ``run(threads)`` times the oracle's
+    decode step -- every layer's scoring, Top-K and gather-attention -- with
+    the given number of threads and returns (seconds, outputs).  Sequences
+    beyond ``max_seqs`` are left out (a bounded sample of the batch)."""
 
-    def __init__(self, w):
-        import numpy as np
+    def __init__(self, w, max_seqs=None):
+        import copy
+
         import oracle
         from csa2_sparse_attention_03_b300 import synth
-        self.np, self.orc, self.synth, self.w = np, oracle, synth, w
+        self.orc, self.synth = oracle, synth
         oracle.build()
-        b = 0
-        L = int(w.seq_lens[b])
-        self.L = L
-        f = next(i for i, ly in enumerate(w.layers) if ly.mode == synth.FULL)
-        r = next((i for i, ly in enumerate(w.layers) if ly.mode == synth.REINDEX), None)
-        u = next((i for i, ly in enumerate(w.layers) if ly.mode == synth.REUSE), None)
-        s = next((i for i, ly in enumerate(w.layers) if ly.mode == synth.SWA_ONLY), None)
-        self.sample_layers = {"F": f, "R": r, "U": u, "S": s}
-        self.counts = {"F": 0, "R": 0, "U": 0, "S": 0}
-        for ly in w.layers:
-            self.counts[synth.MODE_NAMES[ly.mode]] += 1
-        self.k_codes, self.k_scales = oracle.quant_fp4(synth.idx_key_values(w, f, b, 0, L))
-        self.q_idx = {m: synth.index_query(w, l)[b] for m, l in self.sample_layers.items()
-                      if l is not None and m in "FR"}
-        self.wts = {m: synth.index_weights(w, l)[b] for m, l in self.sample_layers.items()
-                    if l is not None and m in "FR"}
-        self.q = {m: synth.query(w, l)[b] for m, l in self.sample_layers.items() if l is not None}
-        self.swa = {}
-        for m, l in self.sample_layers.items():
-            if l is None:
+        w = copy.copy(w)
+        if max_seqs is not None and w.batch > max_seqs:
+            w.seq_lens = list(w.seq_lens)[:max_seqs]
+            w.batch = max_seqs
+        self.w = w
+        self.cores = os.cpu_count() or 1
+        oracle.set_threads(self.cores)
+        caches, per = {}, {}
+        for f, ly in enumerate(w.layers):
+            if ly.mode != synth.FULL:
                 continue
-            n = min(w.window, L)
-            self.swa[m] = oracle.quant_fp8(synth.swa_values(w, l, b)[w.window - n:])
-        # main-KV rows every sampled layer may touch: run the selections once untimed
-        self.cand = np.arange(L, dtype=np.int32)
-        sel = set()
-        for m in "FR":
-            if m in self.q_idx:
-                sc = oracle.index_scores(self.q_idx[m], self.wts[m], self.k_codes, self.k_scales)
-                sel.update(int(x) for x in oracle.topk(sc, self.cand, w.topk) if x >= 0)
-        rows = np.array(sorted(sel), dtype=np.int64)
-        self.kv_codes = np.zeros((L, 256), np.uint8)
-        self.kv_scales = np.zeros((L, 32), np.uint8)
-        lo = 0
-        while lo < rows.size:  # quantise the touched rows chunk by chunk of the value stream
-            c0 = int(rows[lo]) // synth.CHUNK_ROWS * synth.CHUNK_ROWS
-            hi = int(np.searchsorted(rows, c0 + synth.CHUNK_ROWS))
-            vals = synth.kv_values(w, f, b, c0, min(synth.CHUNK_ROWS, L - c0))
-            kc, ks = oracle.quant_fp4(vals[rows[lo:hi] - c0])
-            self.kv_codes[rows[lo:hi]] = kc
-            self.kv_scales[rows[lo:hi]] = ks
-            lo = hi
+            caches[f] = {}
+            for b, L in enumerate(w.seq_lens):
+                kc = np.empty((L, 256), np.uint8)
+                ks = np.empty((L, 32), np.uint8)
+                for r0 in range(0, L, synth.CHUNK_ROWS):
+                    n = min(synth.CHUNK_ROWS, L - r0)
+                    kc[r0:r0 + n], ks[r0:r0 + n] = oracle.quant_fp4(synth.kv_values(w, f, b, r0, n))
+                ic, isc = oracle.quant_fp4(synth.idx_key_values(w, f, b, 0, L))
+                caches[f][b] = dict(kv_codes=kc, kv_scales=ks, k_codes=ic, k_scales=isc)
+        for l, ly in enumerate(w.layers):
+            codes, scales = [], []
+            for b, L in enumerate(w.seq_lens):
+                n = min(w.window, L)
+                c, sc = oracle.quant_fp8(synth.swa_values(w, l, b)[w.window - n:])
+                codes.append(c)
+                scales.append(sc)
+            pl = dict(q=synth.query(w, l), swa_codes=codes, swa_scales=scales, q_idx=None, w=None)
+            if ly.mode in (synth.FULL, synth.REINDEX):
+                pl["q_idx"] = synth.index_query(w, l)
+                pl["w"] = synth.index_weights(w, l)
+            per[l] = pl
+        self.caches, self.per = caches, per
 
-    def layer(self, m, idx_in=None):
-        orc, w = self.orc, self.w
-        idx = idx_in
-        if m in "FR":
-            sc = orc.index_scores(self.q_idx[m], self.wts[m], self.k_codes, self.k_scales)
-            idx = orc.topk(sc, self.cand, w.topk)
-        if m == "S":
-            orc.sparse_attention(self.q[m], None, None, self.np.zeros((0,), self.np.int32), *self.swa[m])
-        else:
-            orc.sparse_attention(self.q[m], self.kv_codes, self.kv_scales, idx, *self.swa[m])
-        return idx
+    def run(self, threads):
+        self.orc.set_threads(threads)
+        t0 = time.perf_counter()
+        res = self.orc.decode_step(self.w.layers, list(self.w.seq_lens), self.w.topk, self.w.pool_len,
+                                   self.caches, self.per)
+        return time.perf_counter() - t0, res
 
-    def run(self):
-        """Times one layer per mode; returns (seconds of a composed 40-layer step, per-mode seconds)."""
-        t = {}
-        idx = None
-        for m in "FRUS":
-            if self.sample_layers[m] is None:
-                continue
-            t0 = time.perf_counter()
-            out = self.layer(m, idx)
-            t[m] = time.perf_counter() - t0
-            if m in "FR":
-                idx = out
-        step = sum(self.counts[m] * t.get(m, 0.0) for m in "FRUS")
-        return step, t, sum(t.values())
+    @staticmethod
+    def same(a, b):
+        """Byte-identical outputs of two runs (indices, outputs, lse)."""
+        for l in a:
+            for k in ("idx", "pool", "out", "lse"):
+                x, y = a[l][k], b[l][k]
+                if (x is None) != (y is None) or (x is not None and not np.array_equal(x, y)):
+                    return False
+        return True
 
 
 def cpu_baseline(w, budget_s):
-    samp = OracleSample(w)
-    steps, work = [], 0.0
-    while work < budget_s or not steps:
-        s, _, spent = samp.run()
-        steps.append(s)
-        work += spent
-    step_s = statistics.median(steps)
-    return {"value": w.batch / step_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"one layer of each mode (F, R, U, S) at B={w.batch}, L={samp.L}, K={w.topk}, "
-                       f"single-threaded C oracle, repeated {len(steps)}x ({work:.1f} s of CPU work); "
-                       f"step time composed as {samp.counts['F']}F+{samp.counts['R']}R+"
-                       f"{samp.counts['U']}U+{samp.counts['S']}S layer times (median)"),
-            "seconds_per_step": step_s}
+    """The oracle's whole decode step, single-threaded and on every host core
+    (checked byte-identical), on a bounded sample of the batch."""
+    max_seqs = 1 if w.batch > 1 else None
+    t0 = time.perf_counter()
+    st = OracleStep(w, max_seqs=max_seqs)
+    setup_s = time.perf_counter() - t0
+    t1, r1 = st.run(1)
+    tn, rn = st.run(st.cores)
+    ident = OracleStep.same(r1, rn)
+    runs = [tn]
+    while sum(runs) + t1 < budget_s and len(runs) < 5:
+        runs.append(st.run(st.cores)[0])
+    step_s = statistics.median(runs)
+    b = st.w.batch
+    return {"value": b / step_s, "unit": UNIT, "cores": st.cores, "kind": "oracle",
+            "sample": (f"whole decode step of the workload ({len(st.w.layers)} layers, K={st.w.topk}) on "
+                       f"{b} of its {w.batch} sequence(s), L={max(st.w.seq_lens)}: the C oracle on {st.cores} host "
+                       f"threads, median of {len(runs)} steps; set-up (input draws, cache quantisation) "
+                       f"{setup_s:.1f} s untimed"),
+            "seconds_per_step": step_s,
+            "single_thread": {"value": b / t1, "seconds_per_step": t1, "cores": 1},
+            "threads_identical": ident}
 
 
 # ---------------------------------------------------------------------------
@@ -354,35 +374,32 @@ def run_reference(args):
         return 0
     from csa2_sparse_attention_03_b300 import synth
     w = synth.workload(args.config)
-    samp = OracleSample(w)
-    # warm-up (at most 2 samples, untimed) also estimates one sample's cost; the
-    # timed steps are capped at about 90 s of oracle work so the arm ends in minutes
+    st = OracleStep(w, max_seqs=1 if w.batch > 1 else None)
+    cores = st.cores
     est = None
     for _ in range(max(1, min(args.warmup, 2))):
-        t = time.perf_counter()
-        samp.run()
-        est = time.perf_counter() - t
+        est = st.run(cores)[0]
+    # timed steps capped at about 90 s of oracle work so the arm ends in minutes
     n_timed = args.steps if args.steps * est <= 90.0 else max(3, int(90.0 / est))
     t0 = time.perf_counter()
     total = 0.0
     for _ in range(n_timed):
-        s, _, _ = samp.run()
-        total += s
+        total += st.run(cores)[0]
     wall = time.perf_counter() - t0
     ms = 1e3 * total / n_timed
-    value = w.batch / (total / n_timed)
+    b = st.w.batch
+    value = b / (total / n_timed)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "timed_steps": n_timed, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.max_len, "layers": len(w.layers),
                    "topk": w.topk, "window": w.window},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": (f"each step: one layer of each mode (F, R, U, S) at the full context on the "
-                                    f"single-threaded C oracle, composed as {samp.counts['F']}F+"
-                                    f"{samp.counts['R']}R+{samp.counts['U']}U+{samp.counts['S']}S; "
-                                    f"{n_timed} of the {args.steps} requested steps timed "
-                                    f"(capped near 90 s of oracle work), {wall:.1f} s wall")},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": (f"each step: the whole decode step of the workload on {b} of its {w.batch} "
+                                    f"sequence(s) by the C oracle on {cores} host threads; {n_timed} of the "
+                                    f"{args.steps} requested steps timed (capped near 90 s of oracle work), "
+                                    f"{wall:.1f} s wall")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -393,8 +410,52 @@ def run_reference(args):
 # the CUDA path
 # ---------------------------------------------------------------------------
 
+def _flush_buffers(torch, dev):
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(2 * max(props.L2_cache_size, 64 << 20), dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(flush.numel() // 8, dtype=torch.int64, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    return flush, flush_rd, flush_sink
+
+
+class GraphTimer:
+    """Replays a CUDA graph after an L2 flush (a write of twice the L2 size,
+    then a read of another buffer), CUDA events around the replay only."""
+
+    def __init__(self, torch, dev, stream):
+        self.torch, self.stream = torch, stream
+        self.flush, self.flush_rd, self.sink = _flush_buffers(torch, dev)
+        self.t0 = torch.cuda.Event(enable_timing=True)
+        self.t1 = torch.cuda.Event(enable_timing=True)
+
+    def capture(self, fn):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            fn()  # once outside the capture (planning, attribute set-up)
+            self.stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    def time(self, g, n, warm=3):
+        torch = self.torch
+        out = []
+        for i in range(warm + n):
+            with torch.cuda.stream(self.stream):
+                self.flush.fill_(1)
+                torch.sum(self.flush_rd, dim=0, out=self.sink)
+                self.t0.record(self.stream)
+                g.replay()
+                self.t1.record(self.stream)
+            self.t1.synchronize()
+            if i >= warm:
+                out.append(self.t0.elapsed_time(self.t1))
+        return out
+
+
 def run_csa2(args):
-    import numpy as np
     import torch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -428,89 +489,91 @@ def run_csa2(args):
     w.seed = replica_seed(w.seed, rank)
     step = DecodeStep(w, device=dev, fill="device")
     stream = torch.cuda.Stream(device=dev)
-    props = torch.cuda.get_device_properties(dev)
-    # L2 flush: write one buffer of twice the L2 size, then read another, so
-    # the step starts with L2 holding clean lines of neither its inputs nor
-    # the flush's own dirty data
-    flush = torch.empty(2 * max(props.L2_cache_size, 64 << 20), dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(flush.numel() // 8, dtype=torch.int64, device=dev)
-    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    timer = GraphTimer(torch, dev, stream)
 
-    # phase events inside the graph (recorded as external event nodes)
-    n_ph = 6
-    ph = [torch.cuda.Event(enable_timing=True) for _ in range(n_ph)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for e in ph:  # torch only times events it has seen recorded once
-            e.record(stream)
-    csa2.csa2_set_phase_events(ph)
-    with torch.cuda.stream(stream):
-        step.run(stream=stream)
-        stream.synchronize()
+    def check(what):
         st, flags = csa2.csa2_check_device(stream)
         if st != 0:
-            raise RuntimeError(f"device flags after the first step: status {st}, bits {flags}")
-        # the phase breakdown comes from a graph with event nodes between the
-        # kernels; the timed value from a second graph without them
-        g_phases = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_phases, stream=stream):
-            step.run(stream=stream)
-        csa2.csa2_set_phase_events([])
-        n0 = csa2.csa2_launch_count()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step.run(stream=stream)
-        launches_per_step = csa2.csa2_launch_count() - n0
-    torch.cuda.synchronize()
+            raise RuntimeError(f"device flags after {what}: status {st}, bits {flags}")
 
-    def one_step(timed, phased=False):
-        with torch.cuda.stream(stream):
-            flush.fill_(1)
-            torch.sum(flush_rd, dim=0, out=flush_sink)
-            t_start.record(stream)
-            (g_phases if phased else graph).replay()
-            t_end.record(stream)
-        t_end.synchronize()
-        if not timed:
-            return None
-        tot = t_start.elapsed_time(t_end)
-        if not phased:
-            return tot, None
-        marks = [t_start] + ph
-        phases = [marks[i].elapsed_time(marks[i + 1]) for i in range(n_ph)]
-        return tot, phases
-
+    # the headline: the layer-sequential step, one graph
+    n0 = csa2.csa2_launch_count()
+    g_seq = timer.capture(lambda: step.run_sequential(stream=stream))
+    seq_launches = (csa2.csa2_launch_count() - n0) // 2  # once eagerly, once captured
+    check("the layer-sequential step")
     for _ in range(max(args.warmup, 3)):
-        one_step(False)
+        timer.time(g_seq, 0, warm=1)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    times, phase_sum = [], [0.0] * n_ph
-    uuid = str(getattr(props, "uuid", "") or "")
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
     gpu_id = ("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or str(local))
     with ClockSampler(gpu_id) as clk:
-        for _ in range(args.steps):
-            tot, _ = one_step(True)
-            times.append(tot)
+        times = timer.time(g_seq, args.steps, warm=0)
     torch.cuda.synchronize()
-    # phase breakdown (separate replays of the graph with event nodes)
-    n_phased = max(1, min(args.steps, 100))
-    for _ in range(3):
-        one_step(False, phased=True)
-    phased_tot = 0.0
-    for _ in range(n_phased):
-        tot, phases = one_step(True, phased=True)
-        phased_tot += tot
-        for i in range(n_ph):
-            phase_sum[i] += phases[i]
+    check("the timed steps")
+    if pg:
+        pg.barrier()
+    ms_total = max_over_ranks(pg, [sum(times)], dev)[0]
+    ms = ms_total / args.steps
+    value = whole_job_value(world, w.batch, ms)
+    n_small = max(1, min(args.steps, 100))
 
-    # the layer-sequential order (per-layer entry points, as a model calls them),
-    # timed the same way from its own graph; one GPU only (a rank failing here
-    # must not leave the others in a collective)
-    st0, fl0 = csa2.csa2_check_device(stream)
-    if st0 != 0:
-        raise RuntimeError(f"device flags after the timed steps: status {st0}, bits {fl0}")
+    # the phased step (csa2_decode_layers), same timing
+    n0 = csa2.csa2_launch_count()
+    g_ph = timer.capture(lambda: step.run(stream=stream))
+    ph_launches = (csa2.csa2_launch_count() - n0) // 2
+    ph_ms = statistics.mean(timer.time(g_ph, n_small))
+    check("the phased step")
+    fsb = fused_step_bytes(w)
+    phased = {"ms_per_step": ph_ms, "value": whole_job_value(world, w.batch, ph_ms), "unit": UNIT,
+              "launches_per_step": int(ph_launches),
+              "hbm": {"algorithmic_bytes_per_step": fsb["total"],
+                      "parts": {k: v for k, v in fsb.items() if k != "total"},
+                      "achieved_gbs": fsb["total"] / (ph_ms * 1e-3) / 1e9},
+              "how": "csa2_decode_layers: every layer's indexing, then every layer's attention (valid only "
+                     "when every query is an input of the step); bytes counted as that launch sequence reads "
+                     "them (a Full layer and its Reindex partner in one key pass, two layers per gather)"}
+
+    # the dominant kernels alone: every layer's attention; every indexing layer
+    peak, peak_kind = peaks()
+    attn_layers = list(range(len(w.layers)))
+    idx_layers = [l for l, ly in enumerate(w.layers) if ly.mode in (synth.FULL, synth.REINDEX)]
+
+    def attn_only():
+        for l in attn_layers:
+            step.attention_only(l, stream=stream)
+
+    def index_only():
+        for l in idx_layers:
+            step.index_only(l, stream=stream)
+
+    kernels = {}
+    for name, fn, layers_, bytes_fn in (("attention (attn_kernel)", attn_only, attn_layers, attention_launch_bytes),
+                                        ("indexing (index_fused_kernel)", index_only, idx_layers, index_launch_bytes)):
+        if not layers_:
+            continue
+        n0 = csa2.csa2_launch_count()
+        g = timer.capture(fn)
+        nl = (csa2.csa2_launch_count() - n0) // 2
+        t = statistics.mean(timer.time(g, n_small))
+        by = sum(bytes_fn(w, w.layers[l]) for l in layers_)
+        kernels[name] = {"launches": int(nl), "ms_all_launches": t, "ms_per_launch": t / max(1, nl),
+                         "algorithmic_bytes_per_launch": by / max(1, nl),
+                         "achieved_gbs": by / (t * 1e-3) / 1e9, "frac": by / (t * 1e-3) / 1e9 / peak}
+        del g
+    check("the kernel timings")
+    # dominant kernel: the larger share of the step (its launches x their time)
+    top = max(kernels, key=lambda k: kernels[k]["ms_all_launches"]) if kernels else None
+    roof = None
+    if top:
+        kd = kernels[top]
+        roof = {"kernel": top, "bound": "hbm", "unit": "GB/s", "peak": peak,
+                "peak_source": f"{peak_kind} copy bandwidth", "achieved": kd["achieved_gbs"], "frac": kd["frac"],
+                "traffic": None, "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"],
+                "ms_per_launch": kd["ms_per_launch"],
+                "timing": "CUDA events around a graph of this kernel's launches for every layer of the step, "
+                          "L2 flushed before each replay"}
 
     # the quantise step's cache build: one Full layer's main KV and indexer keys
     # over the whole context (fp32 rows in, packed rows out), L2 flushed first
@@ -523,147 +586,55 @@ def run_csa2(args):
                                                                                    IDX_ROW)):
                 src = torch.empty((1, Lb, ch), dtype=torch.float32, device=dev).normal_()
                 cache = csa2.Cache.contiguous(fmt, 1, (Lb + 63) // 64 * 64, dev)
-                b_ms = []
-                for it in range(6):
-                    with torch.cuda.stream(stream):
-                        flush.fill_(1)
-                        torch.sum(flush_rd, dim=0, out=flush_sink)
-                        t_start.record(stream)
-                        csa2.csa2_quantize_kv(src, cache, stream=stream)
-                        t_end.record(stream)
-                    t_end.synchronize()
-                    if it >= 3:
-                        b_ms.append(t_start.elapsed_time(t_end))
-                ms_b = sum(b_ms) / len(b_ms)
+                g = timer.capture(lambda: csa2.csa2_quantize_kv(src, cache, stream=stream))
+                ms_b = statistics.mean(timer.time(g, 5))
                 nbytes = Lb * (ch * 4 + row)
                 build[kind] = {"rows": Lb, "ms": ms_b, "algorithmic_bytes": nbytes,
                                "achieved_gbs": nbytes / (ms_b * 1e-3) / 1e9,
-                               "frac": nbytes / (ms_b * 1e-3) / 1e9 / peaks()[0]}
-                del src, cache
-            bst, bfl = csa2.csa2_check_device(stream)
-            if bst != 0:
-                build = {"error": f"device flags after the cache builds: status {bst}, bits {bfl}"}
+                               "frac": nbytes / (ms_b * 1e-3) / 1e9 / peak}
+                del src, cache, g
+            check("the cache builds")
         except Exception as exc:  # reported, never fatal to the main measurement
             build = {"error": repr(exc)[:300]}
-    seq = None
-    if pg is None:
-        try:
-            with torch.cuda.stream(stream):
-                step.run_sequential(stream=stream)
-                stream.synchronize()
-                n0s = csa2.csa2_launch_count()
-                g_seq = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_seq, stream=stream):
-                    step.run_sequential(stream=stream)
-                seq_launches = csa2.csa2_launch_count() - n0s
-            torch.cuda.synchronize()
 
-            def seq_step():
-                with torch.cuda.stream(stream):
-                    flush.fill_(1)
-                    torch.sum(flush_rd, dim=0, out=flush_sink)
-                    t_start.record(stream)
-                    g_seq.replay()
-                    t_end.record(stream)
-                t_end.synchronize()
-                return t_start.elapsed_time(t_end)
-
-            for _ in range(3):
-                seq_step()
-            st_ms = [seq_step() for _ in range(max(1, min(args.steps, 100)))]
-            s_ms = sum(st_ms) / len(st_ms)
-            seq = {"ms_per_step": s_ms, "value": whole_job_value(world, w.batch, s_ms), "unit": UNIT,
-                   "launches_per_step": int(seq_launches),
-                   "how": "each layer in schedule order: its appends, its indexing, its attention, through "
-                          "csa2_quantize_kv / csa2_index_topk / csa2_sparse_attn, one CUDA graph per step"}
-            sst, sfl = csa2.csa2_check_device(stream)
-            if sst != 0:
-                seq = {"error": f"device flags after the layer-sequential steps: status {sst}, bits {sfl}"}
-        except Exception as exc:  # reported, never fatal to the main measurement
-            seq = {"error": repr(exc)[:300]}
-    if pg:
-        pg.barrier()
-    ms_total = max_over_ranks(pg, [sum(times)], dev)[0]
-    ms = ms_total / args.steps
-    value = whole_job_value(world, w.batch, ms)
-
-    # dominant kernel: the phase with the largest share
-    names = ["append (quantize)", "scan", "select", "level-1 scan+select", "attention", "merge"]
-    kern = ["quantize_kernel", "scan_kernel", "select_kernel", "scan_kernel+select_kernel (pool)",
-            "attn_tc_kernel + attn_merge_kernel", "attn_tc_kernel + attn_merge_kernel"]
-    ph_ms = [p / n_phased for p in phase_sum]
-    # attention is one unit: the gather/softmax kernel and the merge that writes the outputs
-    unit_ms = ph_ms[:4] + [ph_ms[4] + ph_ms[5]]
-    top = int(np.argmax(unit_ms))
-    peak, peak_kind = peaks()
-    sb = step_bytes(w)
-    if top == 4:
-        kbytes = attention_bytes(w)
-    elif top == 1:
-        kbytes = scan_bytes(w)
-    else:
-        kbytes = None
-    roof = {"kernel": kern[top], "bound": "hbm", "unit": "GB/s", "peak": peak,
-            "peak_source": f"{peak_kind} copy bandwidth", "traffic": None,
-            "ms_per_launch": unit_ms[top],
-            "timing": "phase events inside a separate graph replay of the same step"}
-    if kbytes is not None:
-        ach = kbytes / (unit_ms[top] * 1e-3) / 1e9
-        roof.update(achieved=ach, frac=ach / peak, algorithmic_bytes=kbytes)
-    else:
-        roof.update(achieved=None, frac=None, algorithmic_bytes=None)
-
-    # end to end: host inputs -> device -> step -> host outputs, as one graph replay
+    # end to end: host inputs -> device -> the layer-sequential step -> host outputs
     e2e = None
     if args.e2e_steps > 0:
-        ins = step.step_inputs()
-        outs = step.step_outputs()
-        h_in = [t.detach().cpu().pin_memory() for t in ins]
-        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-        bi = sum(t.numel() * t.element_size() for t in h_in)
-        bo = sum(t.numel() * t.element_size() for t in h_out)
-        csa2.csa2_set_phase_events([])
-        e_s = torch.cuda.Event(enable_timing=True)
-        e_e = torch.cuda.Event(enable_timing=True)
+        h_in = step.arena_in.detach().cpu().pin_memory()
+        h_out = torch.empty(step.arena_out.shape, dtype=step.arena_out.dtype, pin_memory=True)
+        bi = h_in.numel() * h_in.element_size()
+        bo = h_out.numel() * h_out.element_size()
 
-        # the serving step as one replay: host inputs in, the step, host outputs out
-        g_e2e = step.capture(stream, h_in[0], h_out[0])
+        def serve():
+            step.arena_in.copy_(h_in, non_blocking=True)
+            step.run_sequential(stream=stream)
+            h_out.copy_(step.arena_out, non_blocking=True)
 
-        def e2e_step(timed, direct=False):
+        g_e2e = timer.capture(serve)
+        et = timer.time(g_e2e, args.e2e_steps)
+
+        dt = []
+        for i in range(3 + args.e2e_steps):
             with torch.cuda.stream(stream):
-                flush.fill_(1)
-                torch.sum(flush_rd, dim=0, out=flush_sink)
-                e_s.record(stream)
-                if direct:
-                    for d, h in zip(ins, h_in):
-                        d.copy_(h, non_blocking=True)
-                    step.run(stream=stream)
-                    for h, d in zip(h_out, outs):
-                        h.copy_(d, non_blocking=True)
-                else:
-                    g_e2e.replay()
-                e_e.record(stream)
-            e_e.synchronize()
-            return e_s.elapsed_time(e_e) if timed else None
-
-        for _ in range(3):
-            e2e_step(False)
-            e2e_step(False, direct=True)
-        et = [e2e_step(True) for _ in range(args.e2e_steps)]
-        dt = [e2e_step(True, direct=True) for _ in range(args.e2e_steps)]
-        e_ms, d_ms = max_over_ranks(pg, [sum(et) / len(et), sum(dt) / len(dt)], dev)
+                timer.flush.fill_(1)
+                torch.sum(timer.flush_rd, dim=0, out=timer.sink)
+                timer.t0.record(stream)
+                serve()
+                timer.t1.record(stream)
+            timer.t1.synchronize()
+            if i >= 3:
+                dt.append(timer.t0.elapsed_time(timer.t1))
+        e_ms, d_ms = max_over_ranks(pg, [statistics.mean(et), statistics.mean(dt)], dev)
         e2e = {"value": whole_job_value(world, w.batch, e_ms), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e_ms,
-               "how": "DecodeStep.capture: one CUDA graph per step that copies the pinned host input arena "
-                      "in, runs csa2_decode_layers and copies the output arena (out, lse, indices) back; "
-                      "all inside the CUDA-event region",
+               "how": "one CUDA graph per step: the pinned host input arena (queries, indexer queries, "
+                      "weights, appended rows) copied in, the layer-sequential step (csa2_decode_layer per "
+                      "layer), the output arena (out, lse, indices) copied back; all inside the CUDA events",
                "direct_call_ms_per_step": d_ms}
-
-    st, flags = csa2.csa2_check_device(stream)
-    if st != 0:
-        raise RuntimeError(f"device flags after the timed steps: status {st}, bits {flags}")
+        check("the end-to-end steps")
 
     if rank == 0:
+        sb = step_bytes(w)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -671,20 +642,21 @@ def run_csa2(args):
             "config": {"workload": w.name, "batch": w.batch, "seq_len": w.max_len, "layers": len(w.layers),
                        "schedule": "".join(synth.MODE_NAMES[ly.mode] for ly in w.layers), "topk": w.topk,
                        "window": w.window, "pool": w.pool_len,
-                       "execution": "csa2_decode_layers captured in one CUDA graph, replayed",
-                       "l2": f"flushed before every timed step ({flush.numel() >> 20} MB write, then a {flush.numel() >> 20} MB read of another buffer)",
+                       "execution": "layer-sequential: csa2_decode_layer for each layer in schedule order, "
+                                    "captured in one CUDA graph, replayed",
+                       "l2": f"flushed before every timed step ({timer.flush.numel() >> 20} MB write, then a "
+                             f"{timer.flush.numel() >> 20} MB read of another buffer)",
                        "parallelism": f"replicas x{world}"},
             "hbm": {"algorithmic_bytes_per_step": sb["total"], "parts": {k: v for k, v in sb.items() if k != "total"},
                     "achieved_gbs": sb["total"] / (ms * 1e-3) / 1e9,
                     "frac": sb["total"] / (ms * 1e-3) / 1e9 / peak, "peak_gbs": peak,
                     "peak_source": f"{peak_kind} copy bandwidth"},
-            "phases_ms": {names[i]: ph_ms[i] for i in range(n_ph)},
-            "phased_ms_per_step": phased_tot / n_phased,
-            "layer_sequential": seq,
+            "phased": phased,
+            "kernels": kernels,
             "cache_build": build,
             "roofline": roof,
-            "gpu_launches": int(launches_per_step) * args.steps,
-            "launches_per_step": int(launches_per_step),
+            "gpu_launches": int(seq_launches) * args.steps,
+            "launches_per_step": int(seq_launches),
             "clocks": clk.summary(),
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -76,6 +76,13 @@ def load():
     L.csa2_decode_layers_workspace.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, i32, i32, i32, i32]
     L.csa2_decode_layers.restype = i32
     L.csa2_decode_layers.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, P, i32, i32, i32, i32, P, sz, P]
+    L.csa2_decode_layer_workspace.restype = sz
+    L.csa2_decode_layer_workspace.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, i32, i32, i32, i32]
+    L.csa2_decode_layer.restype = i32
+    L.csa2_decode_layer.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, i32, P, i32, i32, i32, i32, P, sz,
+                                    P]
+    L.csa2_test_set_wait_limit.restype = i32
+    L.csa2_test_set_wait_limit.argtypes = [i32]
     L.csa2_last_error.restype = ctypes.c_char_p
     L.csa2_last_error.argtypes = []
     L.csa2_check_device.restype = i32
@@ -175,7 +182,7 @@ def csa2_index_topk(mode, keys: Cache, q_idx, w, seq_lens, max_seq_len, topk, po
                             dtype=torch.float32, device=dev)
     need = L.csa2_index_topk_workspace(B, max_seq_len, pool_len, topk, P)
     if workspace is None:
-        workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=dev)
+        workspace = new_workspace(need, dev)
     _check(L.csa2_index_topk(mode, keys.ref, _ptr(q_idx), _ptr(w), B, q_idx.shape[1], q_idx.shape[2],
                              _ptr(seq_lens), max_seq_len, _ptr(pool), pool_len, topk, _ptr(out_idx),
                              _ptr(out_pool), P, _ptr(scores), _ptr(workspace), workspace.numel(),
@@ -193,13 +200,13 @@ def csa2_sparse_attn(kv, swa, q, seq_lens, max_seq_len, idx, topk, swa_window, o
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, q.shape[1]), dtype=torch.float32, device=q.device)
-    need = L.csa2_sparse_attn_workspace(B, topk if idx is not None else 0, swa_window)
-    if workspace is None:
-        workspace = torch.empty(max(int(need), 1), dtype=torch.uint8, device=q.device)
+    need = int(L.csa2_sparse_attn_workspace(B, topk if idx is not None else 0, swa_window))
+    if workspace is None and need > 0:
+        workspace = new_workspace(need, q.device)
     _check(L.csa2_sparse_attn(kv.ref if kv is not None else None, swa.ref if swa is not None else None,
                               _ptr(q), B, q.shape[1], q.shape[2], _ptr(seq_lens), max_seq_len, _ptr(idx),
-                              topk, swa_window, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-                              _stream(stream)))
+                              topk, swa_window, _ptr(out), _ptr(lse), _ptr(workspace),
+                              workspace.numel() if workspace is not None else 0, _stream(stream)))
     return out, lse
 
 
@@ -240,6 +247,32 @@ def csa2_decode_layers(descs, batch, seq_lens, max_seq_len, topk, pool_len, swa_
         arr = layer_array(descs)
     _check(load().csa2_decode_layers(arr, len(descs), batch, _ptr(seq_lens), max_seq_len, topk, pool_len,
                                      swa_window, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def csa2_decode_layer_workspace(descs, batch, max_seq_len, topk, pool_len, swa_window) -> int:
+    arr = layer_array(descs)
+    return int(load().csa2_decode_layer_workspace(arr, len(descs), batch, max_seq_len, topk, pool_len,
+                                                  swa_window))
+
+
+def csa2_decode_layer(descs, layer, batch, seq_lens, max_seq_len, topk, pool_len, swa_window, workspace,
+                      stream=None, arr=None):
+    """Layer ``layer`` of the schedule ``descs`` alone (appends, indexing, attention)."""
+    if arr is None:
+        arr = layer_array(descs)
+    _check(load().csa2_decode_layer(arr, len(descs), layer, batch, _ptr(seq_lens), max_seq_len, topk, pool_len,
+                                    swa_window, _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def csa2_test_set_wait_limit(polls: int):
+    """Test hook: polls of each fused indexing CTA's first tile wait (< 0: normal)."""
+    _check(load().csa2_test_set_wait_limit(int(polls)))
+
+
+def new_workspace(nbytes, device):
+    """A workspace as the C interface wants it: zero-filled before first use."""
+    import torch
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def csa2_check_device(stream=None):

@@ -6,8 +6,11 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
+#include <array>
 #include <cstring>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -130,8 +133,6 @@ csa2_status check_ws(void *ws, size_t have, size_t need)
 
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// bytes at the head of a select region that are zeroed per call (the histograms)
-size_t select_head_bytes(int n_rows) { return select_hist_bytes(n_rows); }
 
 }  // namespace
 
@@ -139,21 +140,173 @@ namespace csa2 {
 
 size_t sparse_attn_workspace_within(int32_t batch, int32_t topk, int32_t swa_window, size_t budget)
 {
-    if (batch <= 0 || topk < 0 || swa_window < 0) return 0;
-    static const int32_t any_index = 0;  // stands for "an index list is given"
-    AttnEntry en;
-    memset(&en, 0, sizeof(en));
-    en.has_kv = topk > 0 ? 1 : 0;
-    en.idx = topk > 0 ? &any_index : nullptr;
-    en.has_swa = swa_window > 0 ? 1 : 0;
-    return attn_workspace_bytes(&en, 1, batch, topk, swa_window, budget);
+    (void)batch;
+    (void)topk;
+    (void)swa_window;
+    (void)budget;
+    return 0;  // attention merges its partials inside each cluster
 }
 
 }  // namespace csa2
 
+namespace {
+
+// One indexing level: jobs over key caches, each scored by up to two query
+// rows (a Full layer and the pool-free Reindex layer over the same keys share
+// the pass).  Runs as one fused co-resident launch when it fits, otherwise as
+// the scan + select kernels (with the appends as a quantise launch first).
+struct IdxJob {
+    const csa2_cache *keys;
+    const int32_t *pool;     // [B][pool_len] or null
+    int32_t pool_len;
+    int32_t n_q;
+    const float *q_idx[2], *w[2];
+    int32_t *out_idx[2], *out_pool[2];
+    float *out_scores[2];
+    const csa2_cache *kv;    // appends of a Full layer
+    const float *new_kv, *new_key;
+};
+
+int64_t level_max_cand(const IdxJob *jobs, int n_jobs, int max_seq_len)
+{
+    int64_t m = 1;
+    for (int j = 0; j < n_jobs; ++j) m = std::max<int64_t>(m, jobs[j].pool ? jobs[j].pool_len : max_seq_len);
+    return m;
+}
+
+// Workspace of one level: the fused launch's group state, or the scan +
+// select buffers.
+struct LevelWs {
+    bool fused = false;
+    FusedPlan plan{};
+    size_t fused_bytes = 0, old_bytes = 0;
+};
+
+LevelWs level_ws(const IdxJob *jobs, int n_jobs, int batch, int max_seq_len)
+{
+    LevelWs w;
+    if (n_jobs <= 0) return w;
+    const int64_t mc = level_max_cand(jobs, n_jobs, max_seq_len);
+    int n_rows = 0;
+    for (int j = 0; j < n_jobs; ++j) n_rows += jobs[j].n_q;
+    if (n_jobs <= 8 && fused_plan(n_jobs, batch, mc, w.plan)) {
+        w.fused = true;
+        w.fused_bytes = round256(fused_state_bytes(n_jobs * batch));
+    } else {
+        w.old_bytes = round256(select_bytes(n_rows * batch, mc, max_seq_len));
+    }
+    return w;
+}
+
+cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int batch, const int32_t *seq_lens,
+                      int max_seq_len, int topk, int pool_out_len, int64_t scores_stride, uint8_t *fused_ws,
+                      uint8_t *old_ws, int *fp, cudaStream_t s)
+{
+    if (lw.fused) {
+        std::vector<FusedJobDesc> d((size_t)n_jobs);
+        for (int j = 0; j < n_jobs; ++j) {
+            const IdxJob &J = jobs[j];
+            FusedJobDesc &D = d[(size_t)j];
+            memset(&D, 0, sizeof(D));
+            D.keys = view_of(*J.keys);
+            D.pool = J.pool;
+            D.pool_len = J.pool ? J.pool_len : 0;
+            D.n_q = J.n_q;
+            for (int q = 0; q < 2; ++q) {
+                D.q_idx[q] = J.q_idx[q];
+                D.w[q] = J.w[q];
+                D.out_idx[q] = J.out_idx[q];
+                D.out_pool[q] = J.out_pool[q];
+                D.out_scores[q] = J.out_scores[q];
+            }
+            if (J.kv && J.new_kv) {
+                D.kv = view_of(*J.kv);
+                D.new_kv = J.new_kv;
+            }
+            D.new_key = J.new_key;
+        }
+        FusedLaunch L;
+        L.jobs = d.data();
+        L.n_jobs = n_jobs;
+        L.seq_lens = seq_lens;
+        L.state = fused_ws;
+        L.scores_stride = scores_stride;
+        L.batch = batch;
+        L.topk = topk;
+        L.pool_out = pool_out_len;
+        L.max_len = max_seq_len;
+        L.pdl = 1;
+        return launch_fused(L, lw.plan, fp, s);
+    }
+    // scan + select, the appends first
+    std::vector<QuantJob> qjobs;
+    for (int j = 0; j < n_jobs; ++j) {
+        const IdxJob &J = jobs[j];
+        const std::pair<const float *, const csa2_cache *> ap[2] = {{J.new_kv, J.kv}, {J.new_key, J.keys}};
+        for (const auto &a : ap) {
+            if (!a.first || !a.second) continue;
+            QuantJob q;
+            memset(&q, 0, sizeof(q));
+            q.src = a.first;
+            q.seq_lens = seq_lens;
+            q.dst = view_of(*a.second);
+            q.rows_per_seq = 1;
+            q.n_seqs = batch;
+            q.append_last = 1;
+            qjobs.push_back(q);
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    if (!qjobs.empty() && (e = launch_quantize(qjobs.data(), (int)qjobs.size(), fp, s)) != cudaSuccess) return e;
+    int n_rows = 0;
+    for (int j = 0; j < n_jobs; ++j) n_rows += jobs[j].n_q;
+    if (n_rows > kMaxSelectRows) return cudaErrorInvalidValue;
+    const int64_t mc = level_max_cand(jobs, n_jobs, max_seq_len);
+    SelectPlan plan;
+    memset(&plan, 0, sizeof(plan));
+    plan.bufs = carve_select(old_ws, n_rows * batch, mc, max_seq_len);
+    plan.n_row_blocks = n_rows;
+    plan.batch = batch;
+    plan.topk = topk;
+    plan.pool_out_len = pool_out_len;
+    plan.max_len = max_seq_len;
+    plan.seq_lens = seq_lens;
+    std::vector<ScanJob> sj((size_t)n_jobs);
+    std::vector<std::array<float *, 2>> sc((size_t)n_jobs);
+    int row = 0;
+    for (int j = 0; j < n_jobs; ++j) {
+        const IdxJob &J = jobs[j];
+        ScanJob &S = sj[(size_t)j];
+        memset(&S, 0, sizeof(S));
+        S.keys = view_of(*J.keys);
+        S.pool = J.pool;
+        S.pool_len = J.pool ? J.pool_len : 0;
+        S.n_q = J.n_q;
+        for (int q = 0; q < J.n_q; ++q) {
+            S.q_idx[q] = J.q_idx[q];
+            S.w[q] = J.w[q];
+            S.row[q] = row;
+            SelectRow &R = plan.rows[row++];
+            R.out_idx = J.out_idx[q];
+            R.out_pool = J.out_pool[q];
+            R.pool = J.pool;
+            R.pool_len = J.pool ? J.pool_len : 0;
+            sc[(size_t)j][(size_t)q] = J.out_scores[q];
+        }
+        if (J.n_q < 2) sc[(size_t)j][1] = nullptr;
+    }
+    if ((e = cudaMemsetAsync(old_ws, 0, select_hist_bytes(n_rows * batch), s)) != cudaSuccess) return e;
+    e = launch_scan(sj.data(), n_jobs, plan, (int)mc, reinterpret_cast<float *const (*)[2]>(sc.data()),
+                    scores_stride, fp, s);
+    if (e != cudaSuccess) return e;
+    return launch_select(plan, (int)mc, fp, s, nullptr);
+}
+
+}  // namespace
+
 extern "C" {
 
-int32_t csa2_version(void) { return 100; }
+int32_t csa2_version(void) { return 200; }
 
 int64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -230,9 +383,15 @@ size_t csa2_index_topk_workspace(int32_t batch, int32_t max_seq_len, int32_t poo
 {
     (void)topk;
     (void)pool_out_len;
-    if (batch <= 0 || max_seq_len < 0) return 0;
-    const int64_t cap = max_seq_len > pool_len ? max_seq_len : pool_len;
-    return select_bytes(batch, cap > 0 ? cap : 1, max_seq_len > 0 ? max_seq_len : 1);
+    if (batch <= 0 || max_seq_len < 1) return 0;
+    IdxJob j;
+    memset(&j, 0, sizeof(j));
+    j.n_q = 1;
+    static const int32_t any_pool = 0;
+    j.pool = pool_len > 0 ? &any_pool : nullptr;
+    j.pool_len = pool_len;
+    const LevelWs lw = level_ws(&j, 1, batch, max_seq_len);
+    return lw.fused_bytes + lw.old_bytes;
 }
 
 csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q_idx, const float *w,
@@ -254,46 +413,27 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
         return fail(CSA2_ERR_INVALID_ARG, "out_pool needs mode FULL and pool_out_len in [1, 65536]");
     csa2_status st = check_cache(keys, CSA2_FMT_FP4_IDX, batch, max_seq_len, "keys");
     if (st) return st;
-    const size_t need = csa2_index_topk_workspace(batch, max_seq_len, pool ? pool_len : 0, topk, pool_out_len);
-    st = check_ws(workspace, workspace_bytes, need);
+    IdxJob j;
+    memset(&j, 0, sizeof(j));
+    j.keys = keys;
+    j.pool = pool;
+    j.pool_len = pool ? pool_len : 0;
+    j.n_q = 1;
+    j.q_idx[0] = q_idx;
+    j.w[0] = w;
+    j.out_idx[0] = out_idx;
+    j.out_pool[0] = out_pool;
+    j.out_scores[0] = out_scores;
+    const LevelWs lw = level_ws(&j, 1, batch, max_seq_len);
+    st = check_ws(workspace, workspace_bytes, lw.fused_bytes + lw.old_bytes);
     if (st) return st;
     int *fp = flags_ptr();
     if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-    const int64_t cap = max_seq_len > pool_len ? max_seq_len : (pool ? pool_len : max_seq_len);
-    SelectPlan plan;
-    memset(&plan, 0, sizeof(plan));
-    plan.bufs = carve_select(static_cast<uint8_t *>(workspace), batch, cap, max_seq_len);
-    plan.n_row_blocks = 1;
-    plan.batch = batch;
-    plan.topk = topk;
-    plan.pool_out_len = out_pool ? pool_out_len : 0;
-    plan.max_len = max_seq_len;
-    plan.seq_lens = seq_lens;
-    plan.rows[0].out_idx = out_idx;
-    plan.rows[0].out_pool = out_pool;
-    plan.rows[0].pool = pool;
-    plan.rows[0].pool_len = pool ? pool_len : 0;
-
-    ScanJob job;
-    memset(&job, 0, sizeof(job));
-    job.keys = view_of(*keys);
-    job.q_idx[0] = q_idx;
-    job.w[0] = w;
-    job.pool = pool;
-    job.pool_len = pool ? pool_len : 0;
-    job.n_q = 1;
-    job.row[0] = 0;
-    float *scores[1][2] = {{out_scores, nullptr}};
-    const int max_cand = pool ? pool_len : max_seq_len;
-
-    cudaError_t e = cudaMemsetAsync(workspace, 0, select_head_bytes(batch), s);
-    if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
-    e = launch_scan(&job, 1, plan, max_cand, scores, max_cand, fp, s);
-    if (e != cudaSuccess) return cuda_fail(e, "scan launch");
-    e = launch_select(plan, max_cand, fp, s, nullptr);
-    return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "select launch");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int64_t stride = pool ? pool_len : max_seq_len;
+    cudaError_t e = run_level(&j, 1, lw, batch, seq_lens, max_seq_len, topk, out_pool ? pool_out_len : 0, stride, ws,
+                              ws + lw.fused_bytes, fp, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "index launch");
 }
 
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window)
@@ -323,6 +463,8 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
         st = check_cache(swa, CSA2_FMT_FP8_SWA, batch, swa_window, "swa");
         if (st) return st;
     }
+    (void)workspace;
+    (void)workspace_bytes;
     const int eff_topk = idx ? topk : 0;
     int *fp = flags_ptr();
     if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
@@ -336,8 +478,6 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     en.lse = lse;
     en.has_kv = idx ? 1 : 0;
     en.has_swa = swa_window > 0 ? 1 : 0;
-    st = check_ws(workspace, workspace_bytes, attn_workspace_bytes(&en, 1, batch, eff_topk, swa_window, workspace_bytes));
-    if (st) return st;
     AttnPlan plan;
     plan.entries = &en;
     plan.n_entries = 1;
@@ -345,9 +485,8 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     plan.topk = eff_topk;
     plan.window = swa_window;
     plan.seq_lens = seq_lens;
-    plan.workspace = workspace;
-    plan.workspace_bytes = workspace_bytes;
-    plan.q_packed = 0;
+    plan.max_group = 1;
+    plan.pdl = 1;
     cudaError_t e = launch_attention(plan, fp, static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
 }
@@ -368,7 +507,10 @@ std::vector<AttnEntry> step_entries(const csa2_layer_desc *layers, int n_layers,
         en.out = d.out;
         en.lse = d.lse;
         en.has_swa = swa_window > 0 ? 1 : 0;
-        if (swa_window > 0) en.swa = view_of(*d.swa);
+        if (swa_window > 0) {
+            en.swa = view_of(*d.swa);
+            en.new_swa = d.new_swa;
+        }
         if (d.mode != CSA2_MODE_SWA_ONLY) {
             en.kv = view_of(*layers[d.kv_src].kv);
             en.has_kv = 1;
@@ -378,95 +520,146 @@ std::vector<AttnEntry> step_entries(const csa2_layer_desc *layers, int n_layers,
     return entries;
 }
 
+// Checks layer l of a schedule and the sources it names.
+csa2_status check_layer(const csa2_layer_desc *layers, int32_t l, int32_t batch, int32_t max_seq_len,
+                        int32_t pool_len, int32_t swa_window)
+{
+    const csa2_layer_desc &d = layers[l];
+    char name[32];
+    snprintf(name, sizeof(name), "layer %d", l);
+    if (!d.q || !d.out || !aligned(d.q, 16) || !aligned(d.out, 16))
+        return fail(CSA2_ERR_INVALID_ARG, "%s: q/out NULL or not 16-byte aligned", name);
+    if (swa_window > 0) {
+        csa2_status st = check_cache(d.swa, CSA2_FMT_FP8_SWA, batch, swa_window, name);
+        if (st) return st;
+    }
+    if (d.new_swa && (!d.swa || !aligned(d.new_swa, 16)))
+        return fail(CSA2_ERR_INVALID_ARG, "%s: new_swa needs swa and 16-byte alignment", name);
+    switch (d.mode) {
+    case CSA2_MODE_FULL: {
+        if (d.kv_src != l) return fail(CSA2_ERR_INVALID_ARG, "%s: FULL kv_src must be its own index", name);
+        csa2_status st = check_cache(d.kv, CSA2_FMT_FP4_KV, batch, max_seq_len, name);
+        if (st) return st;
+        st = check_cache(d.idx_keys, CSA2_FMT_FP4_IDX, batch, max_seq_len, name);
+        if (st) return st;
+        if (!d.q_idx || !d.w || !d.idx_out) return fail(CSA2_ERR_INVALID_ARG, "%s: q_idx, w, idx_out required", name);
+        if (pool_len > 0 && !d.pool_out) return fail(CSA2_ERR_INVALID_ARG, "%s: pool_out required when pool_len > 0", name);
+        if ((d.new_kv && !aligned(d.new_kv, 16)) || (d.new_idx_key && !aligned(d.new_idx_key, 16)))
+            return fail(CSA2_ERR_INVALID_ARG, "%s: new rows must be 16-byte aligned", name);
+        break;
+    }
+    case CSA2_MODE_REINDEX:
+    case CSA2_MODE_REUSE: {
+        if (d.kv_src < 0 || d.kv_src >= l || layers[d.kv_src].mode != CSA2_MODE_FULL)
+            return fail(CSA2_ERR_INVALID_ARG, "%s: kv_src must name an earlier FULL layer", name);
+        if (d.mode == CSA2_MODE_REINDEX) {
+            if (!d.q_idx || !d.w || !d.idx_out) return fail(CSA2_ERR_INVALID_ARG, "%s: q_idx, w, idx_out required", name);
+            if (d.use_pool && pool_len <= 0) return fail(CSA2_ERR_INVALID_ARG, "%s: use_pool needs pool_len > 0", name);
+        } else {
+            if (d.idx_src < 0 || d.idx_src >= l ||
+                (layers[d.idx_src].mode != CSA2_MODE_FULL && layers[d.idx_src].mode != CSA2_MODE_REINDEX))
+                return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src must name an earlier FULL/REINDEX layer", name);
+            if (layers[d.idx_src].mode == CSA2_MODE_REINDEX && layers[d.idx_src].kv_src != d.kv_src)
+                return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src indexes a different KV cache", name);
+            if (layers[d.idx_src].mode == CSA2_MODE_FULL && d.idx_src != d.kv_src)
+                return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src indexes a different KV cache", name);
+        }
+        break;
+    }
+    case CSA2_MODE_SWA_ONLY:
+        if (swa_window <= 0) return fail(CSA2_ERR_INVALID_ARG, "%s: SWA_ONLY needs swa_window > 0", name);
+        break;
+    default: return fail(CSA2_ERR_INVALID_ARG, "%s: unknown mode %d", name, d.mode);
+    }
+    return CSA2_OK;
+}
+
+csa2_status check_sizes(int32_t batch, int32_t max_seq_len, int32_t topk, int32_t pool_len, int32_t swa_window)
+{
+    if (batch <= 0 || batch > 65535) return fail(CSA2_ERR_INVALID_ARG, "batch must be in [1, 65535]");
+    if (max_seq_len < 1 || max_seq_len > (1 << 24)) return fail(CSA2_ERR_INVALID_ARG, "max_seq_len must be in [1, 2^24]");
+    if (topk < 1 || topk > 65536) return fail(CSA2_ERR_INVALID_ARG, "topk must be in [1, 65536]");
+    if (pool_len < 0 || pool_len > 65536) return fail(CSA2_ERR_INVALID_ARG, "pool_len must be in [0, 65536]");
+    if (swa_window < 0 || swa_window > 65536) return fail(CSA2_ERR_INVALID_ARG, "swa_window must be in [0, 65536]");
+    return CSA2_OK;
+}
+
+// The indexing job of layer l (FULL or REINDEX), alone or joined to `open`
+// when it scores the same keys and candidates (at most two queries a job).
+void add_index_job(const csa2_layer_desc *layers, int l, int32_t pool_len, std::vector<IdxJob> &jobs)
+{
+    const csa2_layer_desc &d = layers[l];
+    const int f = d.kv_src;
+    const bool use_pool = d.mode == CSA2_MODE_REINDEX && d.use_pool;
+    const int32_t *pool = use_pool ? layers[f].pool_out : nullptr;
+    for (IdxJob &j : jobs) {
+        if (j.n_q == 1 && j.keys->data == layers[f].idx_keys->data && j.pool == pool) {
+            j.q_idx[1] = d.q_idx;
+            j.w[1] = d.w;
+            j.out_idx[1] = d.idx_out;
+            j.out_pool[1] = (d.mode == CSA2_MODE_FULL && pool_len > 0) ? d.pool_out : nullptr;
+            j.n_q = 2;
+            if (d.mode == CSA2_MODE_FULL) {
+                j.kv = d.kv;
+                j.new_kv = d.new_kv;
+                j.new_key = d.new_idx_key;
+            }
+            return;
+        }
+    }
+    IdxJob j;
+    memset(&j, 0, sizeof(j));
+    j.keys = layers[f].idx_keys;
+    j.pool = pool;
+    j.pool_len = pool ? pool_len : 0;
+    j.n_q = 1;
+    j.q_idx[0] = d.q_idx;
+    j.w[0] = d.w;
+    j.out_idx[0] = d.idx_out;
+    j.out_pool[0] = (d.mode == CSA2_MODE_FULL && pool_len > 0) ? d.pool_out : nullptr;
+    if (d.mode == CSA2_MODE_FULL) {
+        j.kv = d.kv;
+        j.new_kv = d.new_kv;
+        j.new_key = d.new_idx_key;
+    }
+    jobs.push_back(j);
+}
+
+// One decode step in the phased order: level 0 (Full layers and pool-free
+// Reindex layers), level 1 (pool-restricted Reindex layers), then the
+// attention of every layer.
 struct StepLayout {
-    int n_idx = 0;              // indexing layers (FULL + REINDEX)
-    std::vector<int> row_block; // per layer: row block id or -1
-    int n_level0 = 0, n_level1 = 0;
-    int64_t cand_cap = 1;
-    size_t select_off = 0, select_size = 0, part_off = 0, part_size = 0, total = 0;
+    std::vector<IdxJob> level[2];
+    LevelWs lw[2];
+    size_t fused_bytes = 0, old_bytes = 0, total = 0;
 };
 
 csa2_status plan_step(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch, int32_t max_seq_len,
                       int32_t topk, int32_t pool_len, int32_t swa_window, StepLayout &P)
 {
     if (!layers || n_layers <= 0) return fail(CSA2_ERR_INVALID_ARG, "no layers");
-    if (batch <= 0 || batch > 65535) return fail(CSA2_ERR_INVALID_ARG, "batch must be in [1, 65535]");
-    if (max_seq_len < 1 || max_seq_len > (1 << 24)) return fail(CSA2_ERR_INVALID_ARG, "max_seq_len must be in [1, 2^24]");
-    if (topk < 1 || topk > 65536) return fail(CSA2_ERR_INVALID_ARG, "topk must be in [1, 65536]");
-    if (pool_len < 0 || pool_len > 65536) return fail(CSA2_ERR_INVALID_ARG, "pool_len must be in [0, 65536]");
-    if (swa_window < 0 || swa_window > 65536) return fail(CSA2_ERR_INVALID_ARG, "swa_window must be in [0, 65536]");
-    P.row_block.assign(n_layers, -1);
-    // level 0: FULL and pool-free REINDEX; level 1: pool-restricted REINDEX
-    for (int pass = 0; pass < 2; ++pass)
-        for (int l = 0; l < n_layers; ++l) {
-            const csa2_layer_desc &d = layers[l];
-            const bool lvl1 = d.mode == CSA2_MODE_REINDEX && d.use_pool;
-            if ((d.mode == CSA2_MODE_FULL || d.mode == CSA2_MODE_REINDEX) && (lvl1 == (pass == 1))) {
-                P.row_block[l] = P.n_idx++;
-                (pass == 0 ? P.n_level0 : P.n_level1)++;
-            }
-        }
-    if (P.n_level0 > kMaxSelectRows || P.n_level1 > kMaxSelectRows)
-        return fail(CSA2_ERR_UNSUPPORTED, "at most %d indexing layers per level", kMaxSelectRows);
+    csa2_status st = check_sizes(batch, max_seq_len, topk, pool_len, swa_window);
+    if (st) return st;
+    if (n_layers > kMaxAttnEntries) return fail(CSA2_ERR_UNSUPPORTED, "at most %d layers per step", kMaxAttnEntries);
+    for (int l = 0; l < n_layers; ++l) {
+        st = check_layer(layers, l, batch, max_seq_len, pool_len, swa_window);
+        if (st) return st;
+    }
     for (int l = 0; l < n_layers; ++l) {
         const csa2_layer_desc &d = layers[l];
-        char name[32];
-        snprintf(name, sizeof(name), "layer %d", l);
-        if (!d.q || !d.out || !aligned(d.q, 16) || !aligned(d.out, 16))
-            return fail(CSA2_ERR_INVALID_ARG, "%s: q/out NULL or not 16-byte aligned", name);
-        if (swa_window > 0) {
-            csa2_status st = check_cache(d.swa, CSA2_FMT_FP8_SWA, batch, swa_window, name);
-            if (st) return st;
-        }
-        if (d.new_swa && (!d.swa || !aligned(d.new_swa, 16)))
-            return fail(CSA2_ERR_INVALID_ARG, "%s: new_swa needs swa and 16-byte alignment", name);
-        switch (d.mode) {
-        case CSA2_MODE_FULL: {
-            if (d.kv_src != l) return fail(CSA2_ERR_INVALID_ARG, "%s: FULL kv_src must be its own index", name);
-            csa2_status st = check_cache(d.kv, CSA2_FMT_FP4_KV, batch, max_seq_len, name);
-            if (st) return st;
-            st = check_cache(d.idx_keys, CSA2_FMT_FP4_IDX, batch, max_seq_len, name);
-            if (st) return st;
-            if (!d.q_idx || !d.w || !d.idx_out) return fail(CSA2_ERR_INVALID_ARG, "%s: q_idx, w, idx_out required", name);
-            if (pool_len > 0 && !d.pool_out) return fail(CSA2_ERR_INVALID_ARG, "%s: pool_out required when pool_len > 0", name);
-            if ((d.new_kv && !aligned(d.new_kv, 16)) || (d.new_idx_key && !aligned(d.new_idx_key, 16)))
-                return fail(CSA2_ERR_INVALID_ARG, "%s: new rows must be 16-byte aligned", name);
-            break;
-        }
-        case CSA2_MODE_REINDEX:
-        case CSA2_MODE_REUSE: {
-            if (d.kv_src < 0 || d.kv_src >= l || layers[d.kv_src].mode != CSA2_MODE_FULL)
-                return fail(CSA2_ERR_INVALID_ARG, "%s: kv_src must name an earlier FULL layer", name);
-            if (d.mode == CSA2_MODE_REINDEX) {
-                if (!d.q_idx || !d.w || !d.idx_out) return fail(CSA2_ERR_INVALID_ARG, "%s: q_idx, w, idx_out required", name);
-                if (d.use_pool && pool_len <= 0) return fail(CSA2_ERR_INVALID_ARG, "%s: use_pool needs pool_len > 0", name);
-            } else {
-                if (d.idx_src < 0 || d.idx_src >= l ||
-                    (layers[d.idx_src].mode != CSA2_MODE_FULL && layers[d.idx_src].mode != CSA2_MODE_REINDEX))
-                    return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src must name an earlier FULL/REINDEX layer", name);
-                if (layers[d.idx_src].mode == CSA2_MODE_REINDEX && layers[d.idx_src].kv_src != d.kv_src)
-                    return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src indexes a different KV cache", name);
-                if (layers[d.idx_src].mode == CSA2_MODE_FULL && d.idx_src != d.kv_src)
-                    return fail(CSA2_ERR_INVALID_ARG, "%s: idx_src indexes a different KV cache", name);
-            }
-            break;
-        }
-        case CSA2_MODE_SWA_ONLY:
-            if (swa_window <= 0) return fail(CSA2_ERR_INVALID_ARG, "%s: SWA_ONLY needs swa_window > 0", name);
-            break;
-        default: return fail(CSA2_ERR_INVALID_ARG, "%s: unknown mode %d", name, d.mode);
-        }
+        if (d.mode != CSA2_MODE_FULL && d.mode != CSA2_MODE_REINDEX) continue;
+        const int level = (d.mode == CSA2_MODE_REINDEX && d.use_pool) ? 1 : 0;
+        add_index_job(layers, l, pool_len, P.level[level]);
     }
-    P.cand_cap = max_seq_len > pool_len ? max_seq_len : pool_len;
-    P.select_off = 0;
-    P.select_size = P.n_idx ? round256(select_bytes(P.n_idx * batch, P.cand_cap, max_seq_len)) : 0;
-    P.part_off = P.select_size;
-    if (n_layers > kMaxAttnEntries) return fail(CSA2_ERR_UNSUPPORTED, "at most %d layers per step", kMaxAttnEntries);
-    {
-        const std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
-        P.part_size = round256(attn_workspace_bytes(entries.data(), n_layers, batch, topk, swa_window));
+    for (int lv = 0; lv < 2; ++lv) {
+        int rows = 0;
+        for (const IdxJob &j : P.level[lv]) rows += j.n_q;
+        if (rows > kMaxSelectRows) return fail(CSA2_ERR_UNSUPPORTED, "at most %d indexing layers per level", kMaxSelectRows);
+        P.lw[lv] = level_ws(P.level[lv].data(), (int)P.level[lv].size(), batch, max_seq_len);
+        P.fused_bytes = std::max(P.fused_bytes, P.lw[lv].fused_bytes);
+        P.old_bytes = std::max(P.old_bytes, P.lw[lv].old_bytes);
     }
-    P.total = P.part_off + P.part_size;
+    P.total = P.fused_bytes + P.old_bytes;
     return CSA2_OK;
 }
 
@@ -477,7 +670,7 @@ size_t csa2_decode_layers_workspace(const csa2_layer_desc *layers, int32_t n_lay
 {
     StepLayout P;
     if (plan_step(layers, n_layers, batch, max_seq_len, topk, pool_len, swa_window, P) != CSA2_OK) return 0;
-    return P.total;
+    return std::max<size_t>(P.total, 256);
 }
 
 csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch,
@@ -495,27 +688,16 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaError_t e;
-
-    // appends (quantise-and-write the new token of each Full layer and each SWA ring)
-    std::vector<QuantJob> qjobs;
-    auto add_append = [&](const float *src, const csa2_cache *c) {
-        QuantJob j;
-        j.src = src;
-        j.start_pos = nullptr;
-        j.seq_lens = seq_lens;
-        j.dst = view_of(*c);
-        j.rows_per_seq = 1;
-        j.n_seqs = batch;
-        j.append_last = 1;
-        qjobs.push_back(j);
-    };
-    for (int l = 0; l < n_layers; ++l) {
-        const csa2_layer_desc &d = layers[l];
-        if (d.mode == CSA2_MODE_FULL && d.new_kv) add_append(d.new_kv, d.kv);
-        if (d.mode == CSA2_MODE_FULL && d.new_idx_key) add_append(d.new_idx_key, d.idx_keys);
-        if (d.new_swa && swa_window > 0) add_append(d.new_swa, d.swa);
+    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "event");
+    for (int lv = 0; lv < 2; ++lv) {
+        if (!P.level[lv].empty()) {
+            e = run_level(P.level[lv].data(), (int)P.level[lv].size(), P.lw[lv], batch, seq_lens, max_seq_len, topk,
+                          lv == 0 ? pool_len : 0, 0, ws, ws + P.fused_bytes, fp, s);
+            if (e != cudaSuccess) return cuda_fail(e, "index launch");
+        }
+        if (lv == 0 && ((e = mark(1, s)) != cudaSuccess || (e = mark(2, s)) != cudaSuccess)) return cuda_fail(e, "event");
     }
-    // the attention's queries to fp16 ride in the same launch
+    if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "event");
     std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
     AttnPlan ap;
     ap.entries = entries.data();
@@ -524,103 +706,89 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     ap.topk = topk;
     ap.window = swa_window;
     ap.seq_lens = seq_lens;
-    ap.workspace = ws + P.part_off;
-    ap.workspace_bytes = P.part_size;
-    ap.q_packed = 1;
-    {
-        const size_t n0 = qjobs.size();
-        qjobs.resize(n0 + (size_t)n_layers);
-        qjobs.resize(n0 + (size_t)attn_pack_jobs(ap, qjobs.data() + n0, n_layers));
-    }
-    if (P.n_idx) {
-        e = cudaMemsetAsync(ws + P.select_off, 0, select_head_bytes(P.n_idx * batch), s);
-        if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
-    }
-    if (!qjobs.empty()) {
-        e = launch_quantize(qjobs.data(), (int)qjobs.size(), fp, s);
-        if (e != cudaSuccess) return cuda_fail(e, "append launch");
-    }
-    if ((e = mark(0, s)) != cudaSuccess) return cuda_fail(e, "event");
-
-    SelectBufs bufs;
-    if (P.n_idx) bufs = carve_select(ws + P.select_off, P.n_idx * batch, P.cand_cap, max_seq_len);
-    for (int level = 0; level < 2; ++level) {
-        const int n_rows = level == 0 ? P.n_level0 : P.n_level1;
-        if (n_rows == 0) {
-            if (level == 0) {
-                if ((e = mark(1, s)) != cudaSuccess || (e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "event");
-            }
-            continue;
-        }
-        const int rb0 = level == 0 ? 0 : P.n_level0;
-        SelectPlan plan;
-        memset(&plan, 0, sizeof(plan));
-        plan.bufs = bufs;
-        plan.n_row_blocks = n_rows;
-        plan.batch = batch;
-        plan.topk = topk;
-        plan.pool_out_len = (level == 0) ? pool_len : 0;
-        plan.max_len = max_seq_len;
-        plan.seq_lens = seq_lens;
-        // rebase buffers so that plan row block i is global row block rb0 + i
-        const int64_t row_off = (int64_t)rb0 * batch;
-        plan.bufs.keys += row_off * bufs.cand_cap;
-        plan.bufs.hist += row_off * kHistBins;
-        std::vector<ScanJob> jobs;
-        int max_cand = 1;
-        for (int l = 0; l < n_layers; ++l) {
-            const int rb = P.row_block[l];
-            if (rb < rb0 || rb >= rb0 + n_rows) continue;
-            const csa2_layer_desc &d = layers[l];
-            SelectRow &R = plan.rows[rb - rb0];
-            R.out_idx = d.idx_out;
-            R.out_pool = (d.mode == CSA2_MODE_FULL && pool_len > 0) ? d.pool_out : nullptr;
-            R.pool = (level == 1) ? layers[d.kv_src].pool_out : nullptr;
-            R.pool_len = (level == 1) ? pool_len : 0;
-            R.out_scores = nullptr;
-            // pair this query with an open job over the same keys and candidates
-            const int f = d.kv_src;
-            const int32_t *pool = R.pool;
-            bool placed = false;
-            for (auto &j : jobs) {
-                if (j.n_q == 1 && j.keys.data == layers[f].idx_keys->data && j.pool == pool) {
-                    j.q_idx[1] = d.q_idx;
-                    j.w[1] = d.w;
-                    j.row[1] = rb - rb0;
-                    j.n_q = 2;
-                    placed = true;
-                    break;
-                }
-            }
-            if (!placed) {
-                ScanJob j;
-                memset(&j, 0, sizeof(j));
-                j.keys = view_of(*layers[f].idx_keys);
-                j.q_idx[0] = d.q_idx;
-                j.w[0] = d.w;
-                j.pool = pool;
-                j.pool_len = pool ? pool_len : 0;
-                j.n_q = 1;
-                j.row[0] = rb - rb0;
-                jobs.push_back(j);
-            }
-            const int mc = pool ? pool_len : max_seq_len;
-            if (mc > max_cand) max_cand = mc;
-        }
-        e = launch_scan(jobs.data(), (int)jobs.size(), plan, max_cand, nullptr, 0, fp, s);
-        if (e != cudaSuccess) return cuda_fail(e, "scan launch");
-        if (level == 0 && (e = mark(1, s)) != cudaSuccess) return cuda_fail(e, "event");
-        e = launch_select(plan, max_cand, fp, s, nullptr);
-        if (e != cudaSuccess) return cuda_fail(e, "select launch");
-        if (level == 0 && (e = mark(2, s)) != cudaSuccess) return cuda_fail(e, "event");
-    }
-    if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "event");
-
-    // attention of every layer
-    cudaEvent_t mid = (g_n_events > 4) ? static_cast<cudaEvent_t>(g_events[4]) : nullptr;
-    e = launch_attention(ap, fp, s, mid);
+    ap.max_group = 2;
+    ap.pdl = 1;
+    e = launch_attention(ap, fp, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
-    if ((e = mark(5, s)) != cudaSuccess) return cuda_fail(e, "event");
+    if ((e = mark(4, s)) != cudaSuccess || (e = mark(5, s)) != cudaSuccess) return cuda_fail(e, "event");
+    return CSA2_OK;
+}
+
+size_t csa2_decode_layer_workspace(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch,
+                                   int32_t max_seq_len, int32_t topk, int32_t pool_len, int32_t swa_window)
+{
+    if (!layers || n_layers <= 0 || check_sizes(batch, max_seq_len, topk, pool_len, swa_window)) return 0;
+    size_t need = 256;
+    for (int l = 0; l < n_layers; ++l) {
+        if (check_layer(layers, l, batch, max_seq_len, pool_len, swa_window)) return 0;
+        const csa2_layer_desc &d = layers[l];
+        if (d.mode != CSA2_MODE_FULL && d.mode != CSA2_MODE_REINDEX) continue;
+        std::vector<IdxJob> jobs;
+        add_index_job(layers, l, pool_len, jobs);
+        const LevelWs lw = level_ws(jobs.data(), 1, batch, max_seq_len);
+        need = std::max(need, lw.fused_bytes + lw.old_bytes);
+    }
+    return need;
+}
+
+csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, int32_t layer, int32_t batch,
+                              const int32_t *seq_lens, int32_t max_seq_len, int32_t topk, int32_t pool_len,
+                              int32_t swa_window, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!layers || n_layers <= 0 || layer < 0 || layer >= n_layers)
+        return fail(CSA2_ERR_INVALID_ARG, "layer %d outside the schedule of %d layers", layer, n_layers);
+    csa2_status st = check_sizes(batch, max_seq_len, topk, pool_len, swa_window);
+    if (st) return st;
+    st = check_layer(layers, layer, batch, max_seq_len, pool_len, swa_window);
+    if (st) return st;
+    if (!seq_lens) return fail(CSA2_ERR_INVALID_ARG, "seq_lens is required");
+    int *fp = flags_ptr();
+    if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const csa2_layer_desc &d = layers[layer];
+    cudaError_t e;
+    if (d.mode == CSA2_MODE_FULL || d.mode == CSA2_MODE_REINDEX) {
+        std::vector<IdxJob> jobs;
+        add_index_job(layers, layer, pool_len, jobs);
+        const LevelWs lw = level_ws(jobs.data(), 1, batch, max_seq_len);
+        st = check_ws(workspace, workspace_bytes, lw.fused_bytes + lw.old_bytes);
+        if (st) return st;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        e = run_level(jobs.data(), 1, lw, batch, seq_lens, max_seq_len, topk, d.mode == CSA2_MODE_FULL ? pool_len : 0, 0,
+                      ws, ws + lw.fused_bytes, fp, s);
+        if (e != cudaSuccess) return cuda_fail(e, "index launch");
+    }
+    AttnEntry en;
+    memset(&en, 0, sizeof(en));
+    en.q = d.q;
+    en.out = d.out;
+    en.lse = d.lse;
+    en.has_swa = swa_window > 0 ? 1 : 0;
+    if (swa_window > 0) {
+        en.swa = view_of(*d.swa);
+        en.new_swa = d.new_swa;
+    }
+    if (d.mode != CSA2_MODE_SWA_ONLY) {
+        en.kv = view_of(*layers[d.kv_src].kv);
+        en.has_kv = 1;
+        en.idx = (d.mode == CSA2_MODE_REUSE) ? layers[d.idx_src].idx_out : d.idx_out;
+    }
+    AttnPlan ap;
+    ap.entries = &en;
+    ap.n_entries = 1;
+    ap.batch = batch;
+    ap.topk = d.mode == CSA2_MODE_SWA_ONLY ? 0 : topk;
+    ap.window = swa_window;
+    ap.seq_lens = seq_lens;
+    ap.max_group = 1;
+    ap.pdl = 1;
+    e = launch_attention(ap, fp, s, nullptr);
+    return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
+}
+
+csa2_status csa2_test_set_wait_limit(int32_t polls)
+{
+    fused_set_first_wait_limit(polls);
     return CSA2_OK;
 }
 

@@ -134,6 +134,26 @@ __device__ __forceinline__ float key_score(uint32_t k)
     return __uint_as_float(u);
 }
 
+// One 16-channel FP4 block: scale = E4M3(absmax / 6); code = E2M1(x / scale).
+__device__ __forceinline__ void fp4_block16(const float x[16], uint2 &codes, uint32_t &scale)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    scale = e4m3_code(__fdiv_rn(amax, 6.0f));
+    float s = e4m3_value(scale);
+    uint32_t w[2] = {0u, 0u};
+    if (s != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t lo = e2m1_code(__fdiv_rn(x[2 * i], s));
+            uint32_t hi = e2m1_code(__fdiv_rn(x[2 * i + 1], s));
+            w[i >> 2] |= (lo | (hi << 4)) << (8 * (i & 3));
+        }
+    }
+    codes = make_uint2(w[0], w[1]);
+}
+
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace csa2

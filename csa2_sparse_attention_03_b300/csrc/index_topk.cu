@@ -34,6 +34,8 @@
 #include <cooperative_groups.h>
 
 #include "internal.h"
+#include "scan.cuh"
+#include "tc.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -44,7 +46,6 @@ constexpr int kScanWarps = 8;
 constexpr int kScanKeys = 1024;                 // candidates per scan CTA
 constexpr int kScanTiles = kScanKeys / kIdxTile;  // 16 key tiles
 constexpr int kSelThreads = 512;
-constexpr uint32_t kWaitLimit = 1u << 24;       // mbarrier polls before giving up
 
 struct ScanBatch {
     ScanJob jobs[kMaxScanJobs];
@@ -52,103 +53,6 @@ struct ScanBatch {
     int64_t scores_stride;
     int32_t n_jobs;
 };
-
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};\n"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f),
-          "f"(0.0f));
-}
-
-__device__ __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
-                                           -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
-
-// ---- mbarrier + bulk copy (sm_90+ PTX) ----------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for phase `parity` of `bar`; false if it gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-            smem_u32(smem_dst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Codes (the 4 words this thread needs) and the 4 block scales of one key.
-struct KeyLoad {
-    uint32_t w[4];
-    uint32_t sc;
-    bool ok;
-};
-
-// thread t of a quad uses bytes 8j+2t, 8j+2t+1 of block j: word 2j + t/2, half t%2
-__device__ __forceinline__ KeyLoad key_from_tile(const uint8_t *tile, int rr, int t)
-{
-    KeyLoad k;
-    const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) k.w[j] = codes[2 * j + (t >> 1)];
-    k.sc = *reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4);
-    k.ok = true;
-    return k;
-}
-
-__device__ __forceinline__ KeyLoad key_from_global(const CacheView &keys, int b, int64_t pos, int t, int *flags)
-{
-    KeyLoad k;
-    k.ok = false;
-    k.sc = 0;
-    k.w[0] = k.w[1] = k.w[2] = k.w[3] = 0;
-    if (pos < 0) return k;
-    const int64_t slot = slot_of(keys, b, pos);
-    if (slot < 0) {
-        raise_flag(flags, kFlagBounds);
-        return k;
-    }
-    const uint8_t *tile = keys.data + (slot / kIdxTile) * kIdxTileBytes;
-    const int rr = (int)(slot % kIdxTile);
-    const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) k.w[j] = __ldg(codes + 2 * j + (t >> 1));
-    k.sc = __ldg(reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4));
-    k.ok = true;
-    return k;
-}
 
 struct __align__(128) ScanSmem {
     uint8_t tiles[kScanTiles][kIdxTileBytes];  // 36,864 B
@@ -183,7 +87,7 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
 
     // 1. issue the bulk copies of this CTA's key tiles (full-context scans)
     if (direct && tid == 0) {
-        mbar_init(&S.bar, 1);
+        tc::mbar_init(&S.bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         uint32_t bytes = 0;
         const uint8_t *src[kScanTiles];
@@ -204,50 +108,18 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
             }
             S.tile_ok[i] = ok;
         }
-        mbar_expect_tx(&S.bar, bytes);
+        tc::mbar_expect_tx(&S.bar, bytes);
         for (int i = 0; i < kScanTiles; ++i)
-            if (src[i]) bulk_g2s(S.tiles[i], src[i], kIdxTileBytes, &S.bar);
+            if (src[i]) tc::bulk_g2s(S.tiles[i], src[i], kIdxTileBytes, &S.bar);
     }
 
     for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&S.hist[0][0])[i] = 0u;
     S.sk_lut[tid] = e4m3_value((uint32_t)tid);  // 256 threads
-    // quantise the queries (FP4 rule) and pre-scale: qpre = scale * E2M1(code), exact in fp16.
-    // 8 threads per 16-value block, two values each; the block max by shuffles.
-    {
-        const int bi = tid >> 3, pr = tid & 7;  // block (query, head, 16 channels), pair in block
-        const int qi = bi >> 4, h = (bi >> 2) & 3, blk = bi & 3;
-        const bool have = qi < job.n_q;
-        float v0 = 0.0f, v1 = 0.0f;
-        if (have) {
-            const float *src = job.q_idx[qi] + ((int64_t)b * kIdxHeads + h) * kIdxDim + blk * 16 + 2 * pr;
-            v0 = __ldg(src);
-            v1 = __ldg(src + 1);
-        }
-        float amax = fmaxf(fabsf(v0), fabsf(v1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-        const float sq = have ? e4m3_value(e4m3_code(__fdiv_rn(amax, 6.0f))) : 0.0f;
-        const float e0 = (sq != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v0, sq))] : 0.0f;
-        const float e1 = (sq != 0.0f) ? kE2M1[e2m1_code(__fdiv_rn(v1, sq))] : 0.0f;
-        S.qpre[qi][h][blk * 16 + 2 * pr] = __float2half_rn(e0 * sq);
-        S.qpre[qi][h][blk * 16 + 2 * pr + 1] = __float2half_rn(e1 * sq);
-        if (blk == 0 && pr == 0) S.wq[qi][h] = have ? __ldg(job.w[qi] + (int64_t)b * kIdxHeads + h) : 0.0f;
-    }
+    scan::prep_queries(tid, job.n_q, job.q_idx, job.w, b, S.qpre, S.wq);
     __syncthreads();
 
-    // B fragments, block j: column g = (query g/4, head g%4); k-slot 2t+e <-> channel 4t+e,
-    // k-slot 2t+8+e <-> channel 4t+2+e (a permutation of the block applied to both operands)
     uint32_t bfrag[4][2];
-    {
-        const int qi = g >> 2, h = g & 3;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half *q = &S.qpre[qi][h][j * 16 + 4 * t];
-            bfrag[j][0] = (uint32_t)__half_as_ushort(q[0]) | ((uint32_t)__half_as_ushort(q[1]) << 16);
-            bfrag[j][1] = (uint32_t)__half_as_ushort(q[2]) | ((uint32_t)__half_as_ushort(q[3]) << 16);
-        }
-    }
+    scan::build_bfrag(S.qpre, g, t, bfrag);
     const int my_q = t >> 1;  // query of this thread's two columns
     const bool finisher = (t & 1) != 0;
     const float w0 = S.wq[my_q][0], w1 = S.wq[my_q][1], w2 = S.wq[my_q][2], w3 = S.wq[my_q][3];
@@ -260,10 +132,10 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
     // 2. wait for the tiles (bounded)
     bool have_tiles = true;
     if (direct) {
-        have_tiles = mbar_wait_bounded(&S.bar, 0);
+        have_tiles = tc::mbar_wait(&S.bar, 0);
         if (!have_tiles) {
             if (tid == 0) raise_flag(flags, kFlagTimeout);
-            mbar_wait_bounded(&S.bar, 0);  // give copies in flight a last chance to land
+            tc::mbar_wait(&S.bar, 0);  // give copies in flight a last chance to land
         }
     }
 
@@ -272,7 +144,7 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
     const bool scoring = finisher && my_q < job.n_q;
 #pragma unroll 1
     for (int gA = warp; gA < kScanKeys / 16; gA += 2 * kScanWarps) {
-        KeyLoad k[4];
+        scan::KeyLoad k[4];
         int64_t cc[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -280,47 +152,18 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
             cc[i] = base + grp * 16 + g + 8 * (i & 1);
             if (direct) {
                 const int ti = grp >> 2;  // 4 groups of 16 keys per 64-key tile
-                k[i] = key_from_tile(S.tiles[ti], (grp & 3) * 16 + g + 8 * (i & 1), t);
+                k[i] = scan::key_from_tile(S.tiles[ti], (grp & 3) * 16 + g + 8 * (i & 1), t);
                 k[i].ok = have_tiles && S.tile_ok[ti] && cc[i] < n_cand;
                 if (!k[i].ok) k[i].w[0] = k[i].w[1] = k[i].w[2] = k[i].w[3] = k[i].sc = 0u;
             } else {
                 int64_t pos = -1;
                 if (cc[i] < n_cand) pos = (int64_t)__ldg(pool + cc[i]);
                 if (pos >= L) pos = -1;
-                k[i] = key_from_global(job.keys, b, pos, t, flags);
+                k[i] = scan::key_from_global(job.keys, b, pos, t, flags);
             }
         }
-        float d[2][4][4];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t uA = (k[2 * h2].w[j] >> (16 * (t & 1))) & 0xFFFFu;
-                const uint32_t uB = (k[2 * h2 + 1].w[j] >> (16 * (t & 1))) & 0xFFFFu;
-                mma16816(d[h2][j], e2m1x2_half2_bits(uA & 0xFFu), e2m1x2_half2_bits(uB & 0xFFu),
-                         e2m1x2_half2_bits(uA >> 8), e2m1x2_half2_bits(uB >> 8), bfrag[j][0], bfrag[j][1]);
-            }
         float sc[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // s = t0 + t1 + t2 + t3 in order; t_j = sk_j * (sq_j * P_j) is exact, so fma == add
-            const float *dd = &d[i >> 1][0][0];
-            const int e0 = 2 * (i & 1);  // accumulator pair of this key
-            float s0 = S.sk_lut[k[i].sc & 0xFFu] * dd[e0];
-            float s1 = S.sk_lut[k[i].sc & 0xFFu] * dd[e0 + 1];
-#pragma unroll
-            for (int j = 1; j < 4; ++j) {
-                const float skj = S.sk_lut[(k[i].sc >> (8 * j)) & 0xFFu];
-                s0 = __fmaf_rn(skj, dd[4 * j + e0], s0);
-                s1 = __fmaf_rn(skj, dd[4 * j + e0 + 1], s1);
-            }
-            const float r0 = s0 > 0.0f ? s0 : 0.0f, r1 = s1 > 0.0f ? s1 : 0.0f;
-            // heads 0,1 live on even t, heads 2,3 on odd t: chain w0*r0 -> +w1 r1 -> +w2 r2 -> +w3 r3
-            float acc = __fmaf_rn(w1, r1, __fmul_rn(w0, r0));
-            acc = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-            float v = __fmaf_rn(w3, r1, __fmaf_rn(w2, r0, acc));
-            sc[i] = (v == 0.0f) ? 0.0f : v;
-        }
+        scan::score4(k, bfrag, S.sk_lut, w0, w1, w2, w3, t, sc);
         if (scoring) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -495,17 +338,17 @@ __global__ void __launch_bounds__(kSelThreads)
     // stage the slice with bulk async copies (16-B multiples; the row is padded to 64 keys)
     const uint32_t stage_bytes = staged ? (uint32_t)(ceil_div(s1 - s0, 4) * 16) : 0u;
     if (stage_bytes && tid == 0) {
-        mbar_init(&stage_bar, 1);
+        tc::mbar_init(&stage_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-        mbar_expect_tx(&stage_bar, stage_bytes);
+        tc::mbar_expect_tx(&stage_bar, stage_bytes);
         for (uint32_t off = 0; off < stage_bytes; off += 16384u)
-            bulk_g2s(reinterpret_cast<uint8_t *>(staged_keys) + off,
+            tc::bulk_g2s(reinterpret_cast<uint8_t *>(staged_keys) + off,
                      reinterpret_cast<const uint8_t *>(keys + s0) + off, min(16384u, stage_bytes - off), &stage_bar);
     }
     __syncthreads();
-    if (stage_bytes && !mbar_wait_bounded(&stage_bar, 0)) {
+    if (stage_bytes && !tc::mbar_wait(&stage_bar, 0)) {
         if (tid == 0) raise_flag(flags, kFlagTimeout);
-        mbar_wait_bounded(&stage_bar, 0);  // give copies in flight a last chance to land
+        tc::mbar_wait(&stage_bar, 0);  // give copies in flight a last chance to land
     }
     const Thresh t0 = find_threshold<kSelThreads>(S.red, 2048, K, S.scratch);
     const bool all_valid = t0.bin < 0;  // fewer candidates than K: take every valid one

@@ -93,6 +93,44 @@ size_t select_bytes(int n_rows, int64_t cand_cap, int max_seq_len);
 size_t select_hist_bytes(int n_rows);  // the leading part of the region to zero before a scan
 SelectBufs carve_select(uint8_t *base, int n_rows, int64_t cand_cap, int max_seq_len);
 
+// ---- step 2, fused: scan + Top-K in one co-resident launch ------------------
+struct FusedJobDesc {
+    CacheView keys;
+    const int32_t *pool;     // [B][pool_len] ascending positions or null (= every position < L)
+    int32_t pool_len;
+    int32_t n_q;             // selection rows (queries) over these keys: 1 or 2
+    const float *q_idx[2];   // [B][4][64]
+    const float *w[2];       // [B][4]
+    int32_t *out_idx[2];     // [B][topk]
+    int32_t *out_pool[2];    // [B][pool_out] or null
+    float *out_scores[2];    // optional [B][scores_stride]
+    CacheView kv;            // Full layer appends: main-KV cache written when new_kv
+    const float *new_kv;     // [B][512] or null: quantised to position L-1 of kv
+    const float *new_key;    // [B][64] or null: quantised to position L-1 of keys
+};
+
+struct FusedLaunch {
+    const FusedJobDesc *jobs;
+    int n_jobs;
+    const int32_t *seq_lens;
+    uint8_t *state;          // fused_state_bytes(n_jobs * batch), zero at the first call, left zero
+    int64_t scores_stride;
+    int batch, topk, pool_out, max_len;
+    int pdl;
+};
+
+struct FusedPlan {
+    int G, chunk, ring_slots, cap;
+    size_t smem;
+};
+
+// Whether the fused launch fits (every CTA co-resident); fills the plan.
+bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp);
+size_t fused_state_bytes(int n_groups);
+cudaError_t launch_fused(const FusedLaunch &L, const FusedPlan &fp, int *flags, cudaStream_t stream);
+// Test hook: polls of each CTA's first tile wait (< 0: the normal limit).
+void fused_set_first_wait_limit(int polls);
+
 // ---- step 3: sparse attention --------------------------------------------
 struct AttnEntry {
     CacheView kv;
@@ -101,6 +139,7 @@ struct AttnEntry {
     const int32_t *idx;    // [B][topk] or null
     float *out;            // [B][16][512]
     float *lse;            // [B][16] or null
+    const float *new_swa;  // optional [B][512]: window row appended at position L-1 first
     int32_t has_kv;
     int32_t has_swa;
 };
@@ -113,24 +152,14 @@ struct AttnPlan {
     int topk;              // rows per index list (0 when no entry has one)
     int window;
     const int32_t *seq_lens;
-    void *workspace;       // at least attn_workspace_bytes(..., workspace_bytes) bytes, 256-B aligned
-    size_t workspace_bytes;
-    int q_packed;          // 1: the jobs of attn_pack_jobs() already ran on this stream
+    int max_group;         // layers that may share one gather (1 or 2)
+    int pdl;               // 1: the launch may overlap the stream's previous kernel
 };
 
-// Workspace of one launch_attention call: every layer's query rows as fp16,
-// and the split partials (per layer, sequence and part: running max and sum
-// per head and half, unnormalised output).  The size of the fastest chunking
-// whose workspace is at most `budget` (or of the smallest, when none is);
-// launch_attention plans within plan.workspace_bytes the same way.
+// Attention needs no workspace: every (layer group, sequence) is one cluster
+// whose CTAs merge their partials through distributed shared memory.
 size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window,
                             size_t budget = SIZE_MAX);
-// csa2_sparse_attn's workspace for one layer, planned within `budget`.
-size_t sparse_attn_workspace_within(int32_t batch, int32_t topk, int32_t swa_window, size_t budget);
-// The quantize jobs that pack the plan's queries to fp16 in its workspace (one
-// per entry; returns how many were written, at most `cap`).  A caller that
-// runs them in its own launch sets plan.q_packed.
-int attn_pack_jobs(const AttnPlan &plan, QuantJob *jobs, int cap);
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
                              cudaEvent_t mid_event);
 

@@ -55,26 +55,6 @@ __device__ __forceinline__ void load16(const float *p, float x[16])
     }
 }
 
-// One 16-channel FP4 block: scale = E4M3(absmax / 6); code = E2M1(x / scale).
-__device__ __forceinline__ void fp4_block(const float x[16], uint2 &codes, uint32_t &scale)
-{
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    scale = e4m3_code(__fdiv_rn(amax, 6.0f));
-    float s = e4m3_value(scale);
-    uint32_t w[2] = {0u, 0u};
-    if (s != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t lo = e2m1_code(__fdiv_rn(x[2 * i], s));
-            uint32_t hi = e2m1_code(__fdiv_rn(x[2 * i + 1], s));
-            w[i >> 2] |= (lo | (hi << 4)) << (8 * (i & 3));
-        }
-    }
-    codes = make_uint2(w[0], w[1]);
-}
-
 __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QuantBatch qb, int *flags)
 {
     const int lane = threadIdx.x & 31;
@@ -118,7 +98,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
             load16(job.src + r * kDim + lane * 16, x);
             uint2 codes;
             uint32_t sc;
-            fp4_block(x, codes, sc);
+            fp4_block16(x, codes, sc);
             uint8_t *row = job.dst.data + slot * kKvRow;
             *reinterpret_cast<uint2 *>(row + lane * 8) = codes;
             row[kKvCodes + lane] = (uint8_t)sc;
@@ -138,7 +118,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ Q
             load16(job.src + r * kIdxDim + blk * 16, x);
             uint2 codes;
             uint32_t sc;
-            fp4_block(x, codes, sc);
+            fp4_block16(x, codes, sc);
             uint8_t *tile = job.dst.data + (slot / kIdxTile) * kIdxTileBytes;
             const int rr = (int)(slot % kIdxTile);
             *reinterpret_cast<uint2 *>(tile + rr * 32 + blk * 8) = codes;

@@ -85,6 +85,32 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
     return r;
 }
 
+// Loads from another CTA's shared memory (shared::cluster address from mapa).
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f2(uint32_t caddr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
+    return v;
+}
+
+// ---- programmatic dependent launch -----------------------------------------
+// Waits until the grids this one depends on have completed and their memory
+// is visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next grid in the stream launch (its own pdl_wait still waits for
+// this grid to complete).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // try_wait that acquires at cluster scope (the arrivals came from another CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
 {

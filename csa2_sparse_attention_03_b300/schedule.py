@@ -19,8 +19,9 @@ import numpy as np
 import torch
 
 from . import (FMT_FP4_IDX, FMT_FP4_KV, FMT_FP8_SWA, MODE_FULL, MODE_REINDEX, MODE_REUSE, MODE_SWA_ONLY,
-               Cache, csa2_cache, csa2_decode_layers, csa2_decode_layers_workspace, csa2_index_topk,
-               csa2_layer_desc, csa2_quantize_kv, csa2_sparse_attn, layer_array, load, synth)
+               Cache, csa2_cache, csa2_decode_layer, csa2_decode_layer_workspace, csa2_decode_layers,
+               csa2_decode_layers_workspace, csa2_index_topk, csa2_layer_desc, csa2_quantize_kv, csa2_sparse_attn,
+               layer_array, load, new_workspace, synth)
 
 _MODE = {synth.FULL: MODE_FULL, synth.REINDEX: MODE_REINDEX, synth.REUSE: MODE_REUSE,
          synth.SWA_ONLY: MODE_SWA_ONLY}
@@ -36,14 +37,19 @@ class DecodeStep:
 
     fill="host": values come from synth's numpy streams (bit-identical to what
     the oracle sees); fill="device": from seeded torch CUDA generators (bench
-    sizes).  The token at position L_b - 1 is left out of the build and passed
-    as the step's append input, so every step re-writes it (idempotent).
+    sizes); fill="sampled": the caches of the sequences in ``host_seqs`` from
+    the host streams, the others' caches from the device generators, every
+    per-layer input (queries, weights, window rows) from the host streams -- a
+    full-size step whose sampled sequences the oracle can follow.  The token at
+    position L_b - 1 is left out of the build and passed as the step's append
+    input, so every step re-writes it (idempotent).
     """
 
-    def __init__(self, w: synth.Workload, device="cuda", fill="host", append=True):
+    def __init__(self, w: synth.Workload, device="cuda", fill="host", append=True, host_seqs=()):
         self.w = w
         self.device = device
         self.fill = fill
+        self.host_seqs = set(int(b) for b in host_seqs)
         B, Lmax = w.batch, w.max_len
         self.B, self.Lmax = B, Lmax
         self.seq_lens = torch.tensor(w.seq_lens, dtype=torch.int32, device=device)
@@ -90,11 +96,18 @@ class DecodeStep:
         if self.ws_bytes == 0:
             from . import csa2_last_error
             raise RuntimeError("workspace query failed: " + csa2_last_error())
-        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.workspace = new_workspace(self.ws_bytes, device)
 
     # ---- value sources ----
-    def _rows(self, kind, layer, b, row0, n, width, scale=1.0):
+    def _host(self, kind, b):
         if self.fill == "host":
+            return True
+        if self.fill == "sampled":
+            return kind == "swa" or b in self.host_seqs
+        return False
+
+    def _rows(self, kind, layer, b, row0, n, width, scale=1.0):
+        if self._host(kind, b):
             name = {"kv": "kv", "idxk": "idxk", "swa": "swa"}[kind]
             if kind == "swa":
                 v = synth.swa_values(self.w, layer, b)[row0:row0 + n]
@@ -151,8 +164,9 @@ class DecodeStep:
     def _alloc_layers(self):
         B, dev = self.B, self.device
         self.q, self.q_idx, self.wts, self.out, self.lse, self.idx, self.pool = {}, {}, {}, {}, {}, {}, {}
+        host_inputs = self.fill in ("host", "sampled")
         for l, ly in enumerate(self.w.layers):
-            if self.fill == "host":
+            if host_inputs:
                 self.q[l] = torch.from_numpy(synth.query(self.w, l)).to(dev)
             else:
                 self.q[l] = synth.device_normal_(torch.empty((B, 16, 512), device=dev), self.w.seed, "q", l,
@@ -160,7 +174,7 @@ class DecodeStep:
             self.out[l] = torch.zeros((B, 16, 512), dtype=torch.float32, device=dev)
             self.lse[l] = torch.zeros((B, 16), dtype=torch.float32, device=dev)
             if ly.mode in (synth.FULL, synth.REINDEX):
-                if self.fill == "host":
+                if host_inputs:
                     self.q_idx[l] = torch.from_numpy(synth.index_query(self.w, l)).to(dev)
                     self.wts[l] = torch.from_numpy(synth.index_weights(self.w, l)).to(dev)
                 else:
@@ -251,21 +265,30 @@ class DecodeStep:
         return g
 
     def run_sequential(self, stream=None):
-        """The same step in the layer-sequential order a model runs it in: for
-        each layer in schedule order its appends, then its indexing (Full, or
-        Reindex over its Full layer's keys or pool), then its attention, each
-        through the per-layer entry points (csa2_quantize_kv, csa2_index_topk,
-        csa2_sparse_attn).  Writes the same outputs as ``run``; the attention's
-        chunking is planned per layer, so outputs agree within the attention
-        tolerance rather than bit for bit.  Graph-capturable."""
+        """The same step in the layer-sequential order a model runs it in: one
+        ``csa2_decode_layer`` call per layer, in schedule order (each layer's
+        appends, its indexing when it is a Full or Reindex layer, its
+        attention).  Writes the same outputs as ``run``.  Graph-capturable."""
         if not hasattr(self, "_seq_ws"):
+            need = csa2_decode_layer_workspace(self.descs, self.B, self.Lmax, self.topk, self.pool_len, self.window)
+            if need == 0:
+                from . import csa2_last_error
+                raise RuntimeError("layer workspace query failed: " + csa2_last_error())
+            self._seq_ws = new_workspace(need, self.device)
+        for l in range(len(self.descs)):
+            csa2_decode_layer(self.descs, l, self.B, self.seq_lens, self.Lmax, self.topk, self.pool_len,
+                              self.window, self._seq_ws, stream=stream, arr=self.arr)
+
+    def run_sequential_calls(self, stream=None):
+        """The layer-sequential order through the step-1..3 entry points
+        (csa2_quantize_kv, csa2_index_topk, csa2_sparse_attn), one call each."""
+        if not hasattr(self, "_calls_ws"):
             lib = load()
             need = max(int(lib.csa2_index_topk_workspace(self.B, self.Lmax, self.pool_len, self.topk,
-                                                           self.pool_len)),
-                       int(lib.csa2_sparse_attn_workspace(self.B, self.topk, self.window)), 1)
-            self._seq_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+                                                           self.pool_len)), 1)
+            self._calls_ws = new_workspace(need, self.device)
             self._seq_last = (self.seq_lens - 1).clamp(min=0)
-        ws, last = self._seq_ws, self._seq_last
+        ws, last = self._calls_ws, self._seq_last
         for l, ly in enumerate(self.w.layers):
             if ly.mode == synth.FULL and ("kv", l) in self.new_rows:
                 kv, ik = self.caches[l]
@@ -291,7 +314,39 @@ class DecodeStep:
                 idx = self.idx[l] if ly.mode in (synth.FULL, synth.REINDEX) else self.idx[ly.idx_src]
                 topk = self.topk
             csa2_sparse_attn(kv, self.swa[l], self.q[l], self.seq_lens, self.Lmax, idx, topk, self.window,
-                             out=self.out[l], lse=self.lse[l], workspace=ws, stream=stream)
+                             out=self.out[l], lse=self.lse[l], stream=stream)
+
+    def attention_only(self, l, stream=None):
+        """Layer l's attention alone (csa2_sparse_attn over its selection and
+        window, no append), for timing the attention kernel."""
+        ly = self.w.layers[l]
+        if ly.mode == synth.SWA_ONLY:
+            kv, idx, topk = None, None, 0
+        else:
+            kv = self.caches[ly.kv_src][0]
+            idx = self.idx[l] if ly.mode in (synth.FULL, synth.REINDEX) else self.idx[ly.idx_src]
+            topk = self.topk
+        csa2_sparse_attn(kv, self.swa[l], self.q[l], self.seq_lens, self.Lmax, idx, topk, self.window,
+                         out=self.out[l], lse=self.lse[l], stream=stream)
+
+    def index_only(self, l, stream=None):
+        """Indexing layer l's scoring and Top-K alone (csa2_index_topk, no
+        append), for timing the indexing kernel."""
+        if not hasattr(self, "_calls_ws"):
+            need = max(int(load().csa2_index_topk_workspace(self.B, self.Lmax, self.pool_len, self.topk,
+                                                            self.pool_len)), 1)
+            self._calls_ws = new_workspace(need, self.device)
+            self._seq_last = (self.seq_lens - 1).clamp(min=0)
+        ly = self.w.layers[l]
+        if ly.mode == synth.FULL:
+            csa2_index_topk(MODE_FULL, self.caches[l][1], self.q_idx[l], self.wts[l], self.seq_lens, self.Lmax,
+                            self.topk, out_idx=self.idx[l], out_pool=self.pool.get(l), workspace=self._calls_ws,
+                            stream=stream)
+        elif ly.mode == synth.REINDEX:
+            pool = self.pool.get(ly.kv_src) if ly.use_pool else None
+            csa2_index_topk(MODE_REINDEX, self.caches[ly.kv_src][1], self.q_idx[l], self.wts[l], self.seq_lens,
+                            self.Lmax, self.topk, pool=pool, out_idx=self.idx[l], workspace=self._calls_ws,
+                            stream=stream)
 
     # ---- inputs/outputs moved per step in the end-to-end measurement ----
     def step_inputs(self):

@@ -22,6 +22,10 @@
  *  - Every data pointer is a DEVICE pointer owned by the caller unless stated.
  *    The library allocates nothing: scratch comes from a caller workspace of
  *    the size the matching *_workspace() function returns (256-B aligned).
+ *    A workspace must be zero-filled before its first use (cudaMemset once
+ *    after allocating it): part of it holds barrier counters and histograms
+ *    that every call leaves zero again.  After a call whose device check
+ *    reports CSA2_ERR_TIMEOUT, zero it again before reusing it.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    All work is enqueued asynchronously on it; no call synchronises, except
  *    csa2_check_device().  Calls may be captured in a CUDA graph.
@@ -143,7 +147,11 @@ csa2_status csa2_quantize_kv(const float *src, int32_t n_seqs, int64_t rows_per_
  *   out_pool    device int32 [batch][pool_out_len] or NULL
  *   out_scores  optional device fp32 [batch][pool ? pool_len : max_seq_len]:
  *               the score of each candidate (unwritten past the candidates)
- * Limits: topk, pool_out_len in [1, 65536]; max_seq_len <= 2^24. */
+ * Limits: topk, pool_out_len in [1, 65536]; max_seq_len <= 2^24.
+ * Execution: when every CTA fits on the device at once (batch x the
+ * candidates per sequence small enough), scoring and selection are one
+ * launch whose CTAs meet at bounded group barriers; otherwise a scan launch
+ * and a cluster-select launch.  Either way the result is the same. */
 size_t csa2_index_topk_workspace(int32_t batch, int32_t max_seq_len, int32_t pool_len,
                                  int32_t topk, int32_t pool_out_len);
 csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q_idx,
@@ -166,12 +174,15 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
  *               (SWA-only layer)
  *   swa_window  window length in tokens (0 = no window branch)
  *   out         device fp32 [batch][16][512];  lse: optional [batch][16]
- * Numerics: q and softmax weights enter the tensor cores as fp16 (the FP4 and
- * FP8 values are exact in fp16), accumulation and softmax in fp32; the
- * weights' exponential is the hardware ex2 (relative error about 2^-22).
- * Workspace: csa2_sparse_attn_workspace() is the size of the fastest plan; a
- * smaller workspace is accepted down to the smallest plan's size (the rows are
- * then split into fewer, longer chunks), below it CSA2_ERR_WORKSPACE. */
+ * Numerics: the FP4 rows, and the FP8 window codes times 2^-8, are exact in
+ * fp16; each query enters the tensor cores as two fp16 parts (its rounded
+ * value and the rounded remainder), so logits keep the fp32 query to about
+ * 2^-22; softmax and every accumulation are fp32; the softmax weights enter
+ * the PV product as fp16 (at most e^2 each, times the window row's fp32
+ * scale x 2^8 -- window rows with |x| above ~15,000 would overflow it).
+ * Workspace: none (csa2_sparse_attn_workspace() returns 0; `workspace` may
+ * be NULL): each (sequence) is one thread-block cluster whose CTAs merge
+ * their partial softmax results through distributed shared memory. */
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window);
 csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                              int32_t batch, int32_t n_heads, int32_t head_dim,
@@ -180,23 +191,17 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
                              float *out, float *lse, void *workspace, size_t workspace_bytes,
                              void *stream);
 
-/* Attention without a workspace, for callers that cannot allocate device
- * memory: a serving process that reserved nearly all HBM for its cache pool
- * up front (cudaMalloc would fail there, and it synchronises the device), or
- * a plugin living inside another runtime's allocator.  The paper has no
- * counterpart; this is a deployment convenience of this library.
+/* Attention without a workspace argument, for callers that cannot allocate
+ * device memory: a serving process that reserved nearly all HBM for its
+ * cache pool up front (cudaMalloc would fail there, and it synchronises the
+ * device), or a plugin living inside another runtime's allocator.  The paper
+ * has no counterpart; this is a deployment convenience of this library.
  * Arguments, layouts, numerics and error codes are those of
- * csa2_sparse_attn minus the workspace.  The fp16 queries and the split
- * partials go to a 4 MiB array the library holds on every device that loads
- * it, until exit, planned to fit it (the fastest plan that fits); a call for
- * which even the smallest plan needs more (beyond about 50 sequences)
- * returns CSA2_ERR_UNSUPPORTED with a message.  It calls no allocator.  Every
- * call on a device shares the array, so calls that overlap on the GPU (other
- * streams, other threads) race and give wrong results: serialise them.  Each
- * call rewrites everything it reads there, so nothing needs clearing between
- * calls.  The first call on each device looks the array's device address up
- * (with that device current); make that first call before any stream
- * capture. */
+ * csa2_sparse_attn minus the workspace.  The attention kernel keeps all of
+ * its intermediate state in shared and tensor memory, so this call uses no
+ * device memory beyond its inputs and outputs, holds no library-owned
+ * array, and calls no allocator; calls on different streams do not
+ * interfere. */
 csa2_status csa2_sparse_attn_noalloc(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                                      int32_t batch, int32_t n_heads, int32_t head_dim,
                                      const int32_t *seq_lens, int32_t max_seq_len,
@@ -231,9 +236,15 @@ typedef struct csa2_layer_desc {
 } csa2_layer_desc;
 
 /* Layer sources must point backwards (kv_src/idx_src < own index) except a
- * FULL layer's kv_src (itself).  A step enqueues: appends, all level-0
- * indexing (Full + pool-free Reindex layers sharing one key scan), level-1
- * indexing (pool-restricted Reindex), then the attention of every layer. */
+ * FULL layer's kv_src (itself).
+ *
+ * csa2_decode_layers runs the whole step in the *phased* order, valid when
+ * every layer's inputs exist when the call is made: all level-0 indexing
+ * (Full + pool-free Reindex layers, a Full layer and its Reindex partner
+ * sharing one key scan; the Full layers' appended main-KV rows and keys are
+ * quantised there), level-1 indexing (pool-restricted Reindex), then the
+ * attention of every layer (each appends its own window row first).  Up to
+ * three launches. */
 size_t csa2_decode_layers_workspace(const csa2_layer_desc *layers, int32_t n_layers,
                                     int32_t batch, int32_t max_seq_len, int32_t topk,
                                     int32_t pool_len, int32_t swa_window);
@@ -241,6 +252,24 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
                                const int32_t *seq_lens, int32_t max_seq_len, int32_t topk,
                                int32_t pool_len, int32_t swa_window, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/* Layer `layer` of the same schedule alone, in the order a model runs it:
+ * its appends, its indexing (FULL / REINDEX: one launch, or two when the
+ * problem is too large to be co-resident) and its attention (one launch).
+ * A model calls it for layer 0, 1, ... with its own work in between; the
+ * layers a call reads (kv_src's caches and pool, idx_src's indices) must
+ * have run before on the same stream.  Launches may overlap the tail of
+ * the stream's previous kernel (programmatic dependent launch); they read
+ * nothing that kernel writes before it completes.  Workspace: the size of
+ * csa2_decode_layer_workspace() (zero-filled before its first use, see
+ * the conventions above), shared by every layer's call. */
+size_t csa2_decode_layer_workspace(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch,
+                                   int32_t max_seq_len, int32_t topk, int32_t pool_len,
+                                   int32_t swa_window);
+csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, int32_t layer,
+                              int32_t batch, const int32_t *seq_lens, int32_t max_seq_len,
+                              int32_t topk, int32_t pool_len, int32_t swa_window,
+                              void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---- diagnostics ------------------------------------------------------ */
 /* Message for the last failure on the calling thread ("" if none). */
@@ -253,14 +282,22 @@ csa2_status csa2_check_device(void *stream);
  * 1 = out-of-range access skipped, 2 = a bounded wait gave up. */
 int32_t csa2_last_device_flags(void);
 /* Profiling hook: when n > 0, csa2_decode_layers records events[i] (cudaEvent_t
- * created by the caller) on its stream after phase i: 0 appends, 1 level-0
- * scoring, 2 level-0 selection, 3 level-1 scoring+selection, 4 attention,
- * 5 merge.  Pass n = 0 to disable.  Process-wide; not thread-safe. */
+ * created by the caller) on its stream after phase i: 0 start, 1 and 2
+ * level-0 scoring and selection (one mark when fused), 3 level-1
+ * scoring+selection, 4 and 5 attention.  Pass n = 0 to disable.
+ * Process-wide; not thread-safe. */
 csa2_status csa2_set_phase_events(void *const *events, int32_t n);
 /* Kernels this library has enqueued since it was loaded, all threads and
  * devices together (a stream capture counts its launches once; replays of
  * the captured graph add nothing). */
 int64_t csa2_launch_count(void);
+/* Test hook: every CTA of a fused indexing launch polls its first tile
+ * copy at most `polls` times before it records a timeout (CSA2_ERR_TIMEOUT
+ * at the next csa2_check_device()); it then still waits, with the normal
+ * bound, for the copy to land, so no CTA leaves with a copy in flight and
+ * the results stay correct.  polls < 0 restores the normal bound.
+ * Process-wide; for tests of the timeout path only. */
+csa2_status csa2_test_set_wait_limit(int32_t polls);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t csa2_version(void);
 

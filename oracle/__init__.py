@@ -43,7 +43,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no FMA contraction, no fast-math)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
                                "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -74,6 +74,10 @@ def lib():
         L.orc_topk.restype = i32
         L.orc_topk.argtypes = [P, P, i64, i32, P]
         L.orc_attend.argtypes = [P, i32, i32, P, i64, P, P]
+        L.orc_set_threads.argtypes = [i32]
+        L.orc_get_threads.restype = i32
+        # single-threaded unless a caller asks for more
+        L.orc_set_threads(1)
         _lib = L
     return _lib
 
@@ -81,6 +85,16 @@ def lib():
 def _p(a: np.ndarray):
     assert a.flags["C_CONTIGUOUS"]
     return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's loops over independent units (results do not
+    depend on the count)."""
+    lib().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().orc_get_threads())
 
 
 # ---- scalar codecs ----

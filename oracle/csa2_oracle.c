@@ -6,7 +6,10 @@
  *
  * Plain, slow, scalar C11.  Build with -O2 -ffp-contract=off (no contraction
  * of a*b+c into an FMA unless written as fmaf).  Each function names the
- * passage it follows.  Sources (web pages about DeepSeek V4.1 Flash):
+ * passage it follows.  Loops over independent units (rows, positions,
+ * heads) may be spread over OpenMP threads (orc_set_threads); no unit's
+ * arithmetic depends on how they are spread, so results are identical for
+ * every thread count.  Sources (web pages about DeepSeek V4.1 Flash):
  *   [HC]   Helmcode, "DeepSeek V4.1 Flash" architecture explainer
  *          (sections "03 · CSA2", "04 · FP4", "07 · compute, memory, bill")
  *   [LB]   Louis Bouchard, "DeepSeek V4.1 Flash: KV cache and writing benchmark"
@@ -23,9 +26,14 @@
  * 3 mantissa bits, subnormals, no infinities, S.1111.111 = NaN, max 448.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads for the loops over independent units (1 = single-threaded). */
+void orc_set_threads(int32_t n) { omp_set_num_threads(n > 0 ? n : 1); }
+int32_t orc_get_threads(void) { return omp_get_max_threads(); }
 
 /* ------------------------------------------------------------------------ */
 /* E2M1 (FP4) -- [HC] "04 · FP4": "E2M1 with an E4M3 scale for every 16      */
@@ -121,6 +129,7 @@ static void fp4_block(const float *x, uint8_t *codes /* 8 bytes */, uint8_t *sca
 /* n rows of C channels (C % 16 == 0) -> codes [n][C/2], scales [n][C/16]. */
 void orc_quant_fp4_rows(const float *x, int64_t n, int32_t C, uint8_t *codes, uint8_t *scales)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; ++r)
         for (int32_t b = 0; b < C / 16; ++b)
             fp4_block(x + r * C + 16 * b, codes + r * (C / 2) + 8 * b, scales + r * (C / 16) + b);
@@ -146,6 +155,7 @@ void orc_dequant_fp4_rows(const uint8_t *codes, const uint8_t *scales, int64_t n
 
 void orc_quant_fp8_rows(const float *x, int64_t n, int32_t C, uint8_t *codes, float *scales)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; ++r) {
         const float *xr = x + r * C;
         float amax = 0.0f;
@@ -188,6 +198,7 @@ void orc_index_scores(const uint8_t *q_codes /* [Hi][Di/2] */, const uint8_t *q_
                       int64_t n, float *scores /* [n] */)
 {
     const int32_t nb = Di / 16;
+#pragma omp parallel for schedule(static)
     for (int64_t p = 0; p < n; ++p) {
         const uint8_t *kc = k_codes + p * (Di / 2);
         const uint8_t *ks = k_scales + p * nb;
@@ -271,8 +282,9 @@ int32_t orc_topk(const float *scores, const int32_t *pos, int64_t n, int32_t K, 
 void orc_attend(const float *q /* [H][D] */, int32_t H, int32_t D, const double *rows /* [n][D] */,
                 int64_t n, double *out /* [H][D] */, double *lse /* [H] */)
 {
-    double *z = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+#pragma omp parallel for schedule(static)
     for (int32_t h = 0; h < H; ++h) {
+        double *z = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
         const float *qh = q + (int64_t)h * D;
         double m = -INFINITY;
         for (int64_t j = 0; j < n; ++j) {
@@ -294,6 +306,6 @@ void orc_attend(const float *q /* [H][D] */, int32_t H, int32_t D, const double 
         } else {
             lse[h] = -INFINITY;
         }
+        free(z);
     }
-    free(z);
 }

@@ -16,30 +16,49 @@ KV, IDX, SWA = 288, 36, 516            # packed row bytes: FP4 main, FP4 indexer
 Q = OUT = 16 * 512 * 4                 # per layer and sequence, fp32
 LSE = 16 * 4
 IDXQ = 4 * 64 * 4 + 4 * 4              # indexer query and head weights
+N_FULL, N_REINDEX, N_SWA_ONLY, N_LAYERS = 4, 4, 2, 40
 
 
-def test_step_bytes_l131072():
+def test_layer_sequential_step_bytes_l131072():
+    """Every Full and every Reindex layer reads all 131,072 keys (each key pass
+    counted), every layer but the SWA-only ones gathers its 2,048 rows."""
     import bench
 
     w = synth.workload(2)
     p = bench.step_bytes(w)
-    n_full, n_reindex, n_swa_only = 4, 4, 2
-    n_layers = 40
-    # one key pass per Full layer: its pool-free Reindex partner scores in the same pass
-    assert p["scan"] == n_full * L * IDX
-    assert p["gather"] == (n_layers - n_swa_only) * K * KV
-    assert p["swa"] == n_layers * W * SWA
-    io = (n_layers * (Q + OUT + LSE)
-          + (n_full + n_reindex) * (IDXQ + K * 4)          # indexer inputs, indices written
-          + (n_layers - n_swa_only) * K * 4                # indices read by attention
-          + n_full * (512 * 4 + KV + 64 * 4 + IDX)         # the appended token: fp32 in, packed out
-          + n_layers * (512 * 4 + SWA))                    # each layer's window append
+    assert p["scan"] == (N_FULL + N_REINDEX) * L * IDX == 37_748_736
+    assert p["gather"] == (N_LAYERS - N_SWA_ONLY) * K * KV == 22_413_312
+    assert p["swa"] == N_LAYERS * W * SWA
+    io = (N_LAYERS * (Q + OUT + LSE)
+          + (N_FULL + N_REINDEX) * (IDXQ + K * 4)          # indexer inputs, indices written
+          + (N_LAYERS - N_SWA_ONLY) * K * 4                # indices read by attention
+          + N_FULL * (512 * 4 + KV + 64 * 4 + IDX)         # the appended token: fp32 in, packed out
+          + N_LAYERS * (512 * 4 + SWA))                    # each layer's window append
     assert p["io"] == io
-    assert p["total"] == p["scan"] + p["gather"] + p["swa"] + p["io"] == 47_051_824
+    assert p["total"] == p["scan"] + p["gather"] + p["swa"] + p["io"] == 65_926_192
 
 
-def test_attention_bytes_l131072():
+def test_fused_step_bytes_l131072():
+    """The phased launch sequence: one key pass per Full/Reindex pair, and the
+    rows of a selection gathered once per unit of two layers (a Full layer
+    alone: 1 unit; Reindex + its Reuse layers, 8 or 9 layers: 4 or 5 units)."""
     import bench
 
     w = synth.workload(2)
-    assert bench.attention_bytes(w) == (38 * (K * KV + K * 4) + 40 * W * SWA + 40 * (Q + OUT + LSE))
+    p = bench.fused_step_bytes(w)
+    assert p["scan"] == N_FULL * L * IDX
+    # groups: F alone x4 (1 unit each); R + 7 U (8 layers, 4 units) x2; R + 8 U (9 layers, 5 units) x2
+    units = 4 * 1 + 2 * 4 + 2 * 5
+    assert p["gather"] == units * K * KV
+    assert p["total"] == p["scan"] + p["gather"] + p["swa"] + p["io"]
+
+
+def test_launch_bytes_l131072():
+    import bench
+
+    w = synth.workload(2)
+    reuse = w.layers[2]
+    assert reuse.mode == synth.REUSE
+    assert bench.attention_launch_bytes(w, reuse) == K * KV + W * SWA + Q + OUT + LSE + K * 4
+    full = w.layers[0]
+    assert bench.index_launch_bytes(w, full) == L * IDX + IDXQ + K * 4 + 512 * 4 + KV + 64 * 4 + IDX

@@ -70,3 +70,40 @@ def test_graph_replay_and_determinism(cuda, orc):
             assert torch.equal(a, b)
     st, flags = cuda.csa2_check_device()
     assert st == 0
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_decode_step_layer_sequential_small(cuda, orc, cfg):
+    """The same step through csa2_decode_layer, one call per layer in schedule
+    order (the order a model runs it in), against the oracle layer by layer."""
+    w = synth.workload(cfg, small=True)
+    step = DecodeStep(w, fill="host")
+    step.run_sequential()
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags, cuda.csa2_last_error())
+    ref, _, _ = oracle_step(orc, w)
+    _compare(step, ref, w)
+
+
+def test_layer_sequential_graph_replays_identically(cuda, orc):
+    w = synth.workload(2, small=True)
+    step = DecodeStep(w, fill="host")
+    step.run_sequential()
+    torch.cuda.synchronize()
+    first = [t.clone() for t in step.step_outputs()]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step.run_sequential(stream=s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            step.run_sequential(stream=s)
+    for _ in range(3):
+        for t in step.step_outputs():
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(first, step.step_outputs()):
+            assert torch.equal(a, b)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags)

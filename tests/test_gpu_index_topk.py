@@ -142,3 +142,50 @@ def test_fewer_candidates_than_k_pads(cuda, orc):
                                      seq, 64, K)
     got = idx[0].cpu().numpy()
     assert np.array_equal(got[:L], np.arange(L)) and (got[L:] == -1).all()
+
+
+def test_batched_fallback_path(cuda, orc):
+    """64 sequences of up to 20,000 keys do not fit one co-resident launch:
+    the scan + cluster-select kernels take the call, with the same result."""
+    rs = np.random.default_rng(21)
+    lens = rs.integers(12000, 20000, 64).tolist()
+    xs = [synth.normal_rows(22, "tk", (b,), 0, L, 64) for b, L in enumerate(lens)]
+    Lmax = max(lens)
+    cache, ref = _keys(cuda, orc, xs, (Lmax + 63) // 64 * 64)
+    q, w = _queries(64, 23)
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    K = 256
+    idx, _, _ = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(),
+                                     seq, Lmax, K)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, flags
+    idx = idx.cpu().numpy()
+    for b, L in enumerate(lens):
+        s = orc.index_scores(q[b], w[b], ref[b][0], ref[b][1])
+        assert np.array_equal(idx[b], orc.topk(s, np.arange(L, dtype=np.int32), K)), b
+
+
+def test_forced_wait_expiry_reports_timeout(cuda, orc):
+    """With the first tile wait limited to zero polls every CTA records a
+    timeout, then still waits (normal bound) for its copies: the call reports
+    CSA2_ERR_TIMEOUT, its result is still right, and the next call is clean."""
+    L, K = 3000, 256
+    x = synth.normal_rows(24, "tk", (0,), 0, L, 64)
+    cache, ref = _keys(cuda, orc, [x], 3008)
+    q, w = _queries(1, 25)
+    seq = torch.tensor([L], dtype=torch.int32, device="cuda")
+    want = orc.topk(orc.index_scores(q[0], w[0], ref[0][0], ref[0][1]), np.arange(L, dtype=np.int32), K)
+    cuda.csa2_test_set_wait_limit(0)
+    try:
+        idx, _, _ = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(),
+                                         torch.from_numpy(w).cuda(), seq, L, K)
+        st, flags = cuda.csa2_check_device()
+    finally:
+        cuda.csa2_test_set_wait_limit(-1)
+    assert st == cuda.ERR_TIMEOUT and (flags & 2), (st, flags)
+    assert np.array_equal(idx[0].cpu().numpy(), want)
+    idx, _, _ = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(),
+                                     seq, L, K)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags)
+    assert np.array_equal(idx[0].cpu().numpy(), want)
