@@ -44,6 +44,16 @@ class csa2_layer_desc(ctypes.Structure):
                 ("pool_out", ctypes.c_void_p)]
 
 
+class csa2_footprint(ctypes.Structure):
+    _fields_ = [("global_bytes_per_token", ctypes.c_int64), ("cache_bytes", ctypes.c_int64),
+                ("step_bytes", ctypes.c_int64), ("sessions", ctypes.c_int64)]
+
+
+class csa2_cost(ctypes.Structure):
+    _fields_ = [("index_flops", ctypes.c_double), ("attn_flops", ctypes.c_double),
+                ("weighted_flops", ctypes.c_double), ("bytes_sequential", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -81,6 +91,10 @@ def load():
     L.csa2_decode_layer.restype = i32
     L.csa2_decode_layer.argtypes = [ctypes.POINTER(csa2_layer_desc), i32, i32, i32, P, i32, i32, i32, i32, P, sz,
                                     P]
+    L.csa2_plan_footprint.restype = i32
+    L.csa2_plan_footprint.argtypes = [P, i32, i64, i32, i32, i32, i64, ctypes.POINTER(csa2_footprint)]
+    L.csa2_plan_cost.restype = i32
+    L.csa2_plan_cost.argtypes = [P, i32, i64, i32, i32, i32, ctypes.POINTER(csa2_cost)]
     L.csa2_test_set_wait_limit.restype = i32
     L.csa2_test_set_wait_limit.argtypes = [i32]
     L.csa2_last_error.restype = ctypes.c_char_p
@@ -273,6 +287,27 @@ def new_workspace(nbytes, device):
     """A workspace as the C interface wants it: zero-filled before first use."""
     import torch
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _modes_arr(modes):
+    arr = (ctypes.c_int32 * len(modes))(*[int(m) for m in modes])
+    return arr
+
+
+def csa2_plan_footprint(modes, context, topk, pool_len, window, hbm_bytes) -> dict:
+    """Footprint of one session (see include/csa2.h); modes: CSA2_MODE_* per layer."""
+    out = csa2_footprint()
+    _check(load().csa2_plan_footprint(_modes_arr(modes), len(modes), int(context), int(topk), int(pool_len),
+                                      int(window), int(hbm_bytes), ctypes.byref(out)))
+    return {k: int(getattr(out, k)) for k, _ in csa2_footprint._fields_}
+
+
+def csa2_plan_cost(modes, context, topk, pool_len, window) -> dict:
+    """Compute and traffic of one decode token (see include/csa2.h)."""
+    out = csa2_cost()
+    _check(load().csa2_plan_cost(_modes_arr(modes), len(modes), int(context), int(topk), int(pool_len),
+                                 int(window), ctypes.byref(out)))
+    return {k: float(getattr(out, k)) for k, _ in csa2_cost._fields_}
 
 
 def csa2_check_device(stream=None):

@@ -25,8 +25,12 @@
 // The CTAs of a cluster then merge their partials through distributed shared
 // memory: each publishes its running (max, sum) per query, scales its O^T by
 // its share of the cluster's softmax denominator, and each CTA sums one slice
-// of the output channels over the cluster and writes it.  Nothing goes
-// through global memory between the CTAs, so the launch needs no workspace.
+// of the output channels over the cluster and writes it.  When one (unit,
+// sequence) has more tiles than a cluster takes well, it is split over
+// several clusters, each a contiguous part of the tiles: each writes its
+// merged partial (max, sum, normalised output) to the workspace, and the last
+// cluster to finish (a ticket counter, left zero again) merges the parts the
+// same way.  With no workspace every (unit, sequence) is one cluster.
 //
 // Value precision: E2M1 x E4M3 values and E4M3 codes x 2^-8 are exact in
 // fp16; an FP8 window row's fp32 scale (x 2^8) multiplies its logit in fp32
@@ -55,13 +59,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileBytes = kRows * kDim * 2;     // 131,072: one tile, fp16
 constexpr int kQBytes = 32 * kDim * 2;           // 32,768 per layer: 16 heads x (value, remainder)
 constexpr int kPBytes = kRows * 16 * 2;          // 4,096 per layer
+constexpr int kQStage = kDim * 4 + 16;           // 2,064 B per fp32 query row staged in the idle tile buffer
+static_assert(kMaxNL * 16 * kQStage <= kTileBytes, "query staging fits the tile buffer");
+
+constexpr int kSAcc = 1;                         // QK^T accumulators (partial sums over the channels)
+constexpr int kChunks = 4;                       // channel chunks of a tile: dequantised and multiplied in turn
 
 template <int NL>
 struct Cols {
-    static constexpr uint32_t S = 0;             // S^T: 32 NL columns
-    static constexpr uint32_t O = 32 * NL;       // O^T: 4 blocks x 16 NL columns
-    static constexpr uint32_t alloc = NL == 1 ? 128 : 256;
+    static constexpr uint32_t S = 0;               // S^T: kSAcc partial sums of 32 NL columns each
+    static constexpr uint32_t O = kSAcc * 32 * NL; // O^T: 4 blocks x 16 NL columns
+    static constexpr uint32_t alloc = NL == 1 ? 256 : 512;
 };
+static_assert(Cols<2>::O + 64 * 2 <= Cols<2>::alloc && Cols<1>::O + 64 <= Cols<1>::alloc, "tensor memory plan");
 
 struct UnitDev {
     CacheView kv;            // FP4_KV cache of the selected rows
@@ -84,8 +94,15 @@ struct AttnParams {
     UnitDev units[kMaxUnits];
     EntryDev entries[kMaxAttnEntries];
     int32_t n_units, batch, topk, window, win_tiles, cs;
+    int32_t split;           // clusters per (unit, sequence); > 1 merges through `parts`
     const int32_t *seq_lens;
+    float *parts;            // split > 1: [unit][b][part][kPartFloats]
+    uint32_t *tickets;       // split > 1: [unit][b], zero at launch, left zero
 };
+
+// One cluster's merged result in the workspace: (max, sum) per query, then the
+// output normalised by that sum, [query][channel].
+constexpr int kPartFloats = 2 * 16 * kMaxNL + 16 * kMaxNL * kDim;
 
 struct Misc {
     uint32_t vmask[4];               // valid rows of the tile in the buffer
@@ -93,14 +110,16 @@ struct Misc {
     float red[4][16 * kMaxNL];       // cross-warp reductions of the softmax warps
     float m_run[16 * kMaxNL];        // running maximum per query
     float l_run[16 * kMaxNL];        // running sum per query (relative to m_run)
-    float ml[2][16 * kMaxNL];        // merge: (m, l) per query, read by the cluster
-    float fac[16 * kMaxNL];          // merge: this CTA's weight per query
+    float2 mlall[kMaxCS][16 * kMaxNL];  // merge: every CTA's (m, l) per query, pushed by that CTA
+    float wall[kMaxCS][16 * kMaxNL];    // merge: every CTA's (or part's) weight per query
+    float cm[16 * kMaxNL], cl[16 * kMaxNL];  // merge: the cluster's (max, sum) per query
+    int32_t last;                    // split: this cluster merges the parts
     float mu[16 * kMaxNL];           // the maximum a tile's weights are taken against
     float alpha[16 * kMaxNL];        // factor moving O^T to that maximum
     __align__(16) uint8_t app[kMaxNL][kDim];  // appended window row per layer slot (E4M3 codes)
     float app_scale[kMaxNL];
-    int32_t app_pos[kMaxNL];         // its position, or -1
-    uint64_t bar_qk, bar_pv;
+    uint64_t bar_qk, bar_pv, bar_q;
+    uint64_t bar_deq[kChunks];       // every thread has converted its part of channel chunk k
     uint32_t tmem_slot;
     int32_t ok;
     int32_t any_resc;
@@ -148,9 +167,11 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane)
     if (N == 16) v[0] = op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
 }
 
-// Raw bytes of one row half (thread: row r, channels 256 h .. 256 h + 255).
+// Raw bytes of one thread's share of a row: row r, channels 128 k + 64 h ..
+// 128 k + 64 h + 63 of every chunk k (so that each channel chunk of the tile
+// is complete once every thread has converted its part of it).
 struct Raw {
-    uint4 g[16];     // FP4: 8 granules of codes + 1 of scales; FP8: 16 granules of codes
+    uint4 g[16];     // FP4: chunk k's codes in g[2k], g[2k+1], its 4 scales in word k of g[8]; FP8: g[4k..4k+3]
     float scale;     // FP8: the row's fp32 scale
     int32_t app;     // FP8: layer slot whose appended row this is, or -1
     bool valid;
@@ -166,16 +187,25 @@ struct Ctx {
 
 __device__ __forceinline__ bool tile_is_window(const UnitDev &U, int tile) { return tile >= U.row_tiles; }
 
-// Issues the loads of this thread's half row of `tile` into registers.
-__device__ __forceinline__ void gather(const Ctx &c, int tile, int r, int h, Raw &raw)
+// Selected position of row r of a row tile (-1: none, or a window tile).
+// Loaded a tile ahead of the row gather so that the gather never waits on it.
+__device__ __forceinline__ int32_t load_pos(const Ctx &c, int tile, int r)
+{
+    const UnitDev &U = *c.U;
+    if (tile_is_window(U, tile)) return -1;
+    const int v = tile * kRows + r;
+    return v < c.P->topk ? __ldcg(U.idx + (int64_t)c.b * c.P->topk + v) : -1;
+}
+
+// Issues the loads of this thread's half row of `tile` into registers (`pos`:
+// load_pos of the row for a row tile).
+__device__ __forceinline__ void gather(const Ctx &c, int tile, int32_t pos, int r, int h, Raw &raw)
 {
     const UnitDev &U = *c.U;
     raw.valid = false;
     raw.scale = 0.0f;
     raw.app = -1;
     if (!tile_is_window(U, tile)) {
-        const int v = tile * kRows + r;
-        const int32_t pos = v < c.P->topk ? __ldcg(U.idx + (int64_t)c.b * c.P->topk + v) : -1;
         const uint8_t *ptr = nullptr;
         if (pos >= 0) {
             const int64_t slot = pos < c.L ? slot_of(U.kv, c.b, pos) : -1;
@@ -187,10 +217,13 @@ __device__ __forceinline__ void gather(const Ctx &c, int tile, int r, int h, Raw
         }
         raw.valid = ptr != nullptr;
         if (ptr) {
-            const uint4 *codes = reinterpret_cast<const uint4 *>(ptr + 128 * h);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) raw.g[i] = __ldcg(codes + i);
-            raw.g[8] = __ldcg(reinterpret_cast<const uint4 *>(ptr + kKvCodes + 16 * h));
+            for (int k = 0; k < kChunks; ++k) {
+                const uint4 *codes = reinterpret_cast<const uint4 *>(ptr + 64 * k + 32 * h);
+                raw.g[2 * k] = __ldcg(codes);
+                raw.g[2 * k + 1] = __ldcg(codes + 1);
+                (&raw.g[8].x)[k] = __ldcg(reinterpret_cast<const uint32_t *>(ptr + kKvCodes + 8 * k + 4 * h));
+            }
         }
     } else {
         const int wt = tile - U.row_tiles;
@@ -200,19 +233,22 @@ __device__ __forceinline__ void gather(const Ctx &c, int tile, int r, int h, Raw
         const int64_t pos = (int64_t)c.L - c.W + rowi;
         if (rowi < c.W && pos >= 0) {
             const EntryDev &E = c.P->entries[U.entry[j]];
-            if (pos == c.M->app_pos[j]) {
+            if (E.new_swa && pos == (int64_t)c.L - 1) {
+                // the row this CTA appends itself: taken from shared memory at dequantisation
                 raw.valid = true;
                 raw.app = j;
-                raw.scale = c.M->app_scale[j];
             } else {
                 const int64_t slot = slot_of(E.swa, c.b, pos);
                 if (slot < 0) {
                     if (h == 0) raise_flag(c.flags, kFlagBounds);
                 } else {
                     raw.valid = true;
-                    const uint4 *codes = reinterpret_cast<const uint4 *>(E.swa.data + slot * kDim + 256 * h);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) raw.g[i] = __ldcg(codes + i);
+                    for (int k = 0; k < kChunks; ++k) {
+                        const uint4 *codes = reinterpret_cast<const uint4 *>(E.swa.data + slot * kDim + 128 * k + 64 * h);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) raw.g[4 * k + i] = __ldcg(codes + i);
+                    }
                     raw.scale = __ldcg(reinterpret_cast<const float *>(E.swa.data + E.swa.n_slots * kDim) + slot);
                 }
             }
@@ -220,41 +256,40 @@ __device__ __forceinline__ void gather(const Ctx &c, int tile, int r, int h, Raw
     }
 }
 
-// Dequantises this thread's half row into the tile buffer (exact fp16).
-__device__ __forceinline__ void dequant(const Ctx &c, bool window, int r, int h, const Raw &raw, uint8_t *T)
+// Dequantises this thread's part of channel chunk k of its row into the tile
+// buffer (exact fp16): channels 128 k + 64 h .. + 63.
+__device__ __forceinline__ void dequant_chunk(const Ctx &c, bool window, int r, int h, int k, const Raw &raw,
+                                              uint8_t *T)
 {
+    const int ch0 = 128 * k + 64 * h;
     if (!raw.valid) {
 #pragma unroll
-        for (int g = 0; g < 32; ++g)
-            *reinterpret_cast<uint4 *>(T + cm_off(r, 256 * h + 8 * g)) = make_uint4(0u, 0u, 0u, 0u);
+        for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 8 * g)) = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
     if (!window) {
+        const uint32_t sw = (&raw.g[8].x)[k];  // the four 16-channel blocks' scales
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int ch = 256 * h + 32 * i;  // channels ch..ch+31: two 16-channel blocks
-            const uint32_t sb = (&raw.g[8].x)[i >> 1] >> (16 * (i & 1));
-            const __half2 s0 = __half2half2(__float2half_rn(e4m3_value(sb & 0xFFu)));
-            const __half2 s1 = __half2half2(__float2half_rn(e4m3_value((sb >> 8) & 0xFFu)));
-            const uint32_t wd[4] = {raw.g[i].x, raw.g[i].y, raw.g[i].z, raw.g[i].w};
-            uint32_t hv[16];
+        for (int blk = 0; blk < 4; ++blk) {
+            const __half2 s2 = __half2half2(__float2half_rn(e4m3_value((sw >> (8 * blk)) & 0xFFu)));
+            const uint4 cw = raw.g[2 * k + (blk >> 1)];
+            const uint32_t w0 = (blk & 1) ? cw.z : cw.x, w1 = (blk & 1) ? cw.w : cw.y;  // 16 codes
+            uint32_t hv[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const uint32_t bits = e2m1x2_half2_bits((wd[k >> 2] >> (8 * (k & 3))) & 0xFFu);
-                hv[k] = pack_h2(__hmul2(*reinterpret_cast<const __half2 *>(&bits), k < 8 ? s0 : s1));
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t bits = e2m1x2_half2_bits(((i < 4 ? w0 : w1) >> (8 * (i & 3))) & 0xFFu);
+                hv[i] = pack_h2(__hmul2(*reinterpret_cast<const __half2 *>(&bits), s2));
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(T + cm_off(r, ch + 8 * k)) =
-                    make_uint4(hv[4 * k], hv[4 * k + 1], hv[4 * k + 2], hv[4 * k + 3]);
+            *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk + 8)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
         }
     } else {
         const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));  // 2^-8
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            uint4 cw = raw.g[i];
-            if (raw.app >= 0) cw = *reinterpret_cast<const uint4 *>(&c.M->app[raw.app][256 * h + 16 * i]);
-            const int ch = 256 * h + 16 * i;
+        for (int i = 0; i < 4; ++i) {
+            uint4 cw = raw.g[4 * k + i];
+            if (raw.app >= 0) cw = *reinterpret_cast<const uint4 *>(&c.M->app[raw.app][ch0 + 16 * i]);
+            const int ch = ch0 + 16 * i;
             *reinterpret_cast<uint4 *>(T + cm_off(r, ch)) =
                 make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.x & 0xFFFFu), k2m8)),
                            pack_h2(__hmul2(e4m3x2_half2(cw.x >> 16), k2m8)),
@@ -305,10 +340,7 @@ __device__ __forceinline__ void append_window_row(const Ctx &c, const EntryDev &
         *reinterpret_cast<uint4 *>(E.swa.data + slot * kDim + lane * 16) = cw;
         if (lane == 0) reinterpret_cast<float *>(E.swa.data + E.swa.n_slots * kDim)[slot] = s;
     }
-    if (lane == 0) {
-        c.M->app_scale[j] = s;
-        c.M->app_pos[j] = (int32_t)pos;
-    }
+    if (lane == 0) c.M->app_scale[j] = s;
 }
 
 // Softmax of one tile (warps 0-3, thread = row r = TMEM lane).  Writes P as
@@ -325,17 +357,29 @@ __device__ __forceinline__ void softmax_tile(const Ctx &c, uint32_t tmem, uint8_
     const bool window = tile_is_window(U, tile);
     const int owner = window ? (tile - U.row_tiles) / c.P->win_tiles : -1;
     const int qlane = NQ == 16 ? (lane >> 1) : lane;
-    float s[2 * NQ], v[NQ];
-    tc::tmem_ld32(tc::taddr(tmem, 32u * warp, Cols<NL>::S), s);
-    if (NL == 2) tc::tmem_ld32(tc::taddr(tmem, 32u * warp, Cols<NL>::S + 32), s + 32);
+    // S^T: per query the value and remainder columns (of each of the kSAcc
+    // partial sums over the channels, added in a fixed order)
+    float s[NQ], v[NQ];
+#pragma unroll
+    for (int a = 0; a < kSAcc; ++a)
+#pragma unroll
+        for (int c0 = 0; c0 < 2 * NQ; c0 += 32) {
+            float t[32];
+            tc::tmem_ld32(tc::taddr(tmem, 32u * warp, Cols<NL>::S + (uint32_t)(a * 2 * NQ + c0)), t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int col = c0 + i, q = col % NQ;
+                s[q] = (a == 0 && col < NQ) ? t[i] : s[q] + t[i];
+            }
+        }
     const bool valid = (M.vmask[r >> 5] >> (r & 31)) & 1u;
     const float fac = M.rowfac[r];
-    // logits: the value and remainder halves of each query, times the row factor
+    // logits times the row factor
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         const int j = q >> 4;
         const bool own = window ? (j == owner) : (j < U.n_layers);
-        s[q] = (valid && own) ? fac * (s[q] + s[NQ + q]) : -INFINITY;
+        s[q] = (valid && own) ? fac * s[q] : -INFINITY;
         v[q] = s[q];
     }
     warp_transpose_reduce<NQ, true>(v, lane);
@@ -407,12 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cs = P.cs;
     const int rank = (int)tc::cluster_rank();
-    const UnitDev &U = P.units[blockIdx.x / cs];
+    const int cluster = (int)blockIdx.x / cs;
+    const int unit = cluster / P.split, part = cluster % P.split;
+    const UnitDev &U = P.units[unit];
 
     // ---- prologue: nothing here reads memory another kernel writes
     if (tid == 0) {
         tc::mbar_init(&M.bar_qk, 1);
         tc::mbar_init(&M.bar_pv, 1);
+        tc::mbar_init(&M.bar_q, 1);
+        for (int k = 0; k < kChunks; ++k) tc::mbar_init(&M.bar_deq[k], kThreads);
         tc::mbar_init_fence();
         M.ok = 1;
     }
@@ -420,12 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         M.m_run[tid] = -INFINITY;
         M.l_run[tid] = 0.0f;
     }
-    if (tid < kMaxNL) M.app_pos[tid] = -1;
     if (warp == 0) tc::tmem_alloc(&M.tmem_slot, Cols<NL>::alloc);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = M.tmem_slot;
+    tc::cluster_arrive_relaxed();  // waited for before the first access to a peer's shared memory
     tc::pdl_wait();
     tc::pdl_launch_dependents();
 
@@ -437,29 +485,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     c.b = blockIdx.y;
     c.L = max(0, __ldcg(P.seq_lens + c.b));
     c.W = P.window;
-    const int n_my = U.n_tiles > rank ? (U.n_tiles - 1 - rank) / cs + 1 : 0;
+    // this cluster's tiles: a contiguous part of the unit's; this CTA's: every cs-th
+    const int per_part = (U.n_tiles + P.split - 1) / P.split;
+    const int t0 = part * per_part + rank, t_end = min(U.n_tiles, (part + 1) * per_part);
+    const int n_my = t_end > t0 ? (t_end - 1 - t0) / cs + 1 : 0;
     const int r = tid & (kRows - 1), h = tid >> 7;
+
+    // the unit's queries go out first, as one bulk copy per (layer, head) into
+    // the idle tile buffer (fp32 rows kQStage apart, so the conversion below
+    // reads them without bank conflicts); the first tile's positions and rows,
+    // the next tile's positions and the appended window rows load meanwhile
+    if (warp == 0) {
+        if (lane == 0) tc::mbar_expect_tx(&M.bar_q, (uint32_t)(U.n_layers * kHeads * kDim * 4));
+        __syncwarp();
+        for (int i = lane; i < U.n_layers * kHeads; i += 32)
+            tc::bulk_g2s(T + i * kQStage, P.entries[U.entry[i >> 4]].q + ((int64_t)c.b * kHeads + (i & 15)) * kDim,
+                         kDim * 4, &M.bar_q);
+    }
+    Raw raw;
+    int32_t pos_next = -1;
+    if (n_my > 0) {
+        const int32_t pos0 = load_pos(c, t0, r);
+        if (n_my > 1) pos_next = load_pos(c, t0 + cs, r);
+        gather(c, t0, pos0, r, h, raw);
+    }
 
     // appended window rows of this CTA's window tiles (position L-1 of each layer)
     if (P.window > 0 && c.L > 0 && warp < U.n_layers) {
         const int j = warp;
         const EntryDev &E = P.entries[U.entry[j]];
         const int t_app = U.row_tiles + j * P.win_tiles + (P.window - 1) / kRows;
-        if (E.new_swa && t_app < U.n_tiles && t_app % cs == rank) append_window_row(c, E, j, lane);
+        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0) append_window_row(c, E, j, lane);
     }
 
-    // queries: fp16 value and fp16 remainder, K-major core matrices (query
+    // queries to fp16 value and fp16 remainder, K-major core matrices (query
     // rows n, 8,192 B per 8 rows; remainders at n + 16 NL)
-    for (int item = tid; item < NQ * 64; item += kThreads) {
+    if (!tc::mbar_wait(&M.bar_q, 0)) {
+        M.ok = 0;
+        tc::mbar_wait(&M.bar_q, 0);  // a last chance for the copies in flight
+    }
+#pragma unroll
+    for (int k = 0; k < 4 * NL; ++k) {
+        const int item = tid + kThreads * k;
         const int qi = (item & 7) | ((item >> 9) << 3);
         const int cg = (item >> 3) & 63;
-        const int j = qi >> 4, head = qi & 15;
-        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (j < U.n_layers) {
-            const float4 *src = reinterpret_cast<const float4 *>(P.entries[U.entry[j]].q +
-                                                                 ((int64_t)c.b * kHeads + head) * kDim + 8 * cg);
-            const float4 a = __ldcg(src), bb = __ldcg(src + 1);
-            x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = bb.x, x[5] = bb.y, x[6] = bb.z, x[7] = bb.w;
+        float x[8];
+        if ((qi >> 4) < U.n_layers) {
+            const float4 *src = reinterpret_cast<const float4 *>(T + qi * kQStage + 32 * cg);
+            const float4 a = src[0], b = src[1];
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.0f;
         }
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -472,36 +550,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         *reinterpret_cast<uint4 *>(Qs + cm_off(qi, 8 * cg)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(Qs + cm_off(NQ + qi, 8 * cg)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    __syncthreads();  // appended rows visible before the gathers look at app_pos
+    __syncthreads();  // queries and appended rows in shared memory before any dequantisation
 
     constexpr uint32_t kIdescQK = tc::idesc_f16(128, 2 * NQ, false, false);
     constexpr uint32_t kIdescPV = tc::idesc_f16(128, NQ, true, true);
-    Raw raw;
-    if (n_my > 0) gather(c, rank, r, h, raw);
     for (int it = 0; it < n_my; ++it) {
-        const int tile = rank + it * cs;
+        const int tile = t0 + it * cs;
         const bool window = tile_is_window(U, tile);
         if (it > 0 && tid == 0 && !tc::mbar_wait(&M.bar_pv, (it - 1) & 1)) M.ok = 0;  // tile and P buffers free
         __syncthreads();
         tc::fence_after_sync();
-        dequant(c, window, r, h, raw, T);
         if (h == 0) {
             const uint32_t m = __ballot_sync(0xFFFFFFFFu, raw.valid);
             if (lane == 0) M.vmask[warp] = m;
-            M.rowfac[r] = window ? raw.scale * 256.0f : 1.0f;
+            M.rowfac[r] = window ? (raw.app >= 0 ? M.app_scale[raw.app] : raw.scale) * 256.0f : 1.0f;
         }
-        if (it + 1 < n_my) gather(c, tile + cs, r, h, raw);  // in flight during this tile
-        tc::fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        // channel chunk by chunk: every thread converts its part of chunk k and
+        // arrives; thread 0 multiplies chunk k - 1 once all have arrived, so the
+        // tensor core works on one chunk while the threads convert the next
+        const uint64_t a0 = tc::sdesc(tc::smem_u32(T), 128, 8192);
+        const uint64_t b0 = tc::sdesc(tc::smem_u32(Qs), 128, 8192);
+        auto issue_chunk = [&](int k) {
+            if (!tc::mbar_wait(&M.bar_deq[k], it & 1)) M.ok = 0;
             tc::fence_after_sync();
-            const uint64_t a0 = tc::sdesc(tc::smem_u32(T), 128, 8192);
-            const uint64_t b0 = tc::sdesc(tc::smem_u32(Qs), 128, 8192);
 #pragma unroll
-            for (int ks = 0; ks < kDim / 16; ++ks)
+            for (int ks = 8 * k; ks < 8 * k + 8; ++ks)
                 tc::mma_f16(tmem + Cols<NL>::S, a0 + 16 * ks, b0 + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+        };
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            dequant_chunk(c, window, r, h, k, raw, T);
+            tc::fence_async_smem();
+            tc::mbar_arrive(&M.bar_deq[k]);
+            if (tid == 0 && k > 0) issue_chunk(k - 1);
+        }
+        if (tid == 0) {
+            issue_chunk(kChunks - 1);
             tc::mma_commit(&M.bar_qk);
         }
+        if (it + 1 < n_my) {  // in flight during this tile
+            gather(c, tile + cs, pos_next, r, h, raw);
+            pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * cs, r) : -1;
+        }
+        __syncthreads();  // row masks and factors before the softmax
         if (warp < 4) {
             if (!tc::mbar_wait(&M.bar_qk, it & 1) && tid == 0) M.ok = 0;
             tc::fence_after_sync();
@@ -510,10 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
+            // the four channel blocks are independent accumulators: interleaved
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb)
+            for (int ks = 0; ks < kRows / 16; ++ks)
 #pragma unroll
-                for (int ks = 0; ks < kRows / 16; ++ks)
+                for (int cb = 0; cb < 4; ++cb)
                     tc::mma_f16(tmem + Cols<NL>::O + cb * NQ,
                                 tc::sdesc(tc::smem_u32(T) + 2048u * cb + 16384u * ks, 8192, 128),
                                 tc::sdesc(tc::smem_u32(Ps) + (uint32_t)(2 * 256 * NL * ks), 256 * NL, 128), kIdescPV,
@@ -529,40 +621,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     tc::fence_after_sync();
     if (tid == 0 && !M.ok) raise_flag(flags, kFlagTimeout);
 
-    // ---- merge across the cluster
-    if (tid < NQ) {
-        M.ml[0][tid] = M.m_run[tid];
-        M.ml[1][tid] = M.l_run[tid];
+    // ---- merge across the cluster: every CTA stages its output normalised by its
+    // own sum, with its (max, sum); one cluster barrier; each CTA then weighs
+    // and sums one slice of the channels over the cluster
+    float *stage = reinterpret_cast<float *>(T);  // [query][channel] fp32, in the idle tile buffer
+    // this CTA's (m, l) of every query into every CTA's table (remote stores,
+    // visible after the cluster barrier; every peer has started by now)
+    tc::cluster_wait();
+    for (int i = tid; i < NQ * cs; i += kThreads) {
+        const int q = i % NQ, dst = i / NQ;
+        tc::st_cluster_f2(tc::mapa(tc::smem_u32(&M.mlall[rank][q]), (uint32_t)dst), M.m_run[q], M.l_run[q]);
     }
-    tc::cluster_sync();
-    if (tid < NQ) {
-        const int q = tid;
-        const uint32_t ml_addr = tc::smem_u32(&M.ml[0][q]);
-        float ms[kMaxCS], ls[kMaxCS];
-        float mx = -INFINITY;
-        for (int s = 0; s < cs; ++s) {
-            const uint32_t a = tc::mapa(ml_addr, (uint32_t)s);
-            asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(ms[s]) : "r"(a) : "memory");
-            asm volatile("ld.shared::cluster.f32 %0, [%1];\n"
-                         : "=f"(ls[s])
-                         : "r"(a + (uint32_t)(sizeof(float) * 16 * kMaxNL))
-                         : "memory");
-            if (ls[s] > 0.0f) mx = fmaxf(mx, ms[s]);
-        }
-        float lsum = 0.0f;
-        for (int s = 0; s < cs; ++s)
-            if (ls[s] > 0.0f) lsum += ls[s] * __expf(ms[s] - mx);
-        const float m_own = M.m_run[q], l_own = M.l_run[q];
-        M.fac[q] = (lsum > 0.0f && l_own > 0.0f) ? __expf(m_own - mx) / lsum : 0.0f;
-        const int j = q >> 4;
-        if (rank == 0 && j < U.n_layers) {
-            float *lse = P.entries[U.entry[j]].lse;
-            if (lse) lse[(int64_t)c.b * kHeads + (q & 15)] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
-        }
-    }
-    __syncthreads();
-    // this CTA's share of the output, [query][channel] fp32, into the idle tile buffer
-    float *stage = reinterpret_cast<float *>(T);
     {
         const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32 quad.., column half
         const int ch_in = 32 * quad + lane;
@@ -578,17 +647,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int col = c0 + i, cb = col / NQ, q = col % NQ;
-                stage[q * kDim + 128 * cb + ch_in] = o[i] * M.fac[q];
+                const float l = M.l_run[q];
+                stage[q * kDim + 128 * cb + ch_in] = l > 0.0f ? o[i] / l : 0.0f;
             }
         }
     }
     tc::fence_before_sync();
     tc::cluster_sync();
-    // each CTA sums one slice of the channels over the cluster and writes it
+    if (warp == 0) {  // O^T is staged: tensor memory is done
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Cols<NL>::alloc);
+    }
+    if (tid < NQ) {
+        // the cluster's maximum and sum; each CTA's weight l_s exp(m_s - M) / L
+        const int q = tid;
+        float mx = -INFINITY;
+        for (int s = 0; s < cs; ++s)
+            if (M.mlall[s][q].y > 0.0f) mx = fmaxf(mx, M.mlall[s][q].x);
+        float lsum = 0.0f;
+        for (int s = 0; s < cs; ++s)
+            if (M.mlall[s][q].y > 0.0f) lsum += M.mlall[s][q].y * __expf(M.mlall[s][q].x - mx);
+        for (int s = 0; s < cs; ++s)
+            M.wall[s][q] = (lsum > 0.0f && M.mlall[s][q].y > 0.0f) ? M.mlall[s][q].y * __expf(M.mlall[s][q].x - mx) / lsum
+                                                                   : 0.0f;
+        M.cm[q] = mx;
+        M.cl[q] = lsum;
+    }
+    __syncthreads();
+    const int cpc = ((kDim + cs - 1) / cs + 3) & ~3;
+    const int c_lo = rank * cpc, c_hi = min(kDim, c_lo + cpc);
+    const int n4 = max(0, (c_hi - c_lo) / 4);
+    float *part_rec = P.split > 1
+                          ? P.parts + (((int64_t)unit * P.batch + c.b) * P.split + part) * (int64_t)kPartFloats
+                          : nullptr;
     {
-        const int cpc = ((kDim + cs - 1) / cs + 3) & ~3;
-        const int c_lo = rank * cpc, c_hi = min(kDim, c_lo + cpc);
-        const int n4 = max(0, (c_hi - c_lo) / 4);
         const uint32_t st_addr = tc::smem_u32(stage);
         for (int item = tid; item < NQ * n4; item += kThreads) {
             const int q = item / n4, ch = c_lo + 4 * (item % n4);
@@ -596,23 +688,104 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             if (j >= U.n_layers) continue;
             const uint32_t off = (uint32_t)(q * kDim + ch) * 4u;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < cs; ++s) {
-                const float4 v = tc::ld_cluster_f4(tc::mapa(st_addr + off, (uint32_t)s));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+            // eight remote loads in flight, then their weighted sum
+#pragma unroll
+            for (int s0 = 0; s0 < kMaxCS; s0 += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (s0 + k < cs) v[k] = tc::ld_cluster_f4(tc::mapa(st_addr + off, (uint32_t)(s0 + k)));
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (s0 + k < cs) {
+                        const float wgt = M.wall[s0 + k][q];
+                        acc.x += wgt * v[k].x;
+                        acc.y += wgt * v[k].y;
+                        acc.z += wgt * v[k].z;
+                        acc.w += wgt * v[k].w;
+                    }
             }
-            float *out = P.entries[U.entry[j]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch;
-            *reinterpret_cast<float4 *>(out) = acc;
+            float *dst = part_rec ? part_rec + 2 * 16 * kMaxNL + q * kDim + ch
+                                  : P.entries[U.entry[j]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch;
+            *reinterpret_cast<float4 *>(dst) = acc;
+        }
+        if (tid < NQ && rank == 0) {
+            const int q = tid, j = q >> 4;
+            if (part_rec) {
+                part_rec[q] = M.cm[q];
+                part_rec[16 * kMaxNL + q] = M.cl[q];
+            } else if (j < U.n_layers && P.entries[U.entry[j]].lse) {
+                P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] =
+                    M.cl[q] > 0.0f ? M.cm[q] + logf(M.cl[q]) : -INFINITY;
+            }
         }
     }
-    tc::fence_before_sync();
-    tc::cluster_sync();  // no CTA leaves while another reads its shared memory
-    if (warp == 0) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, Cols<NL>::alloc);
+    if (P.split > 1) {
+        // the unit's clusters meet through a ticket: the last one to arrive sums the
+        // parts (each CTA its slice of the channels) and writes the output
+        __threadfence();
+        tc::fence_before_sync();
+        tc::cluster_sync();  // every part record of this cluster is written
+        if (rank == 0 && tid == 0) {
+            uint32_t *tk = P.tickets + (int64_t)unit * P.batch + c.b;
+            const uint32_t t = atomicAdd(tk, 1u);
+            M.last = (t == (uint32_t)P.split - 1) ? 1 : 0;
+            if (M.last) atomicExch(tk, 0u);  // every cluster has arrived: leave it zero
+            __threadfence();
+        }
+        tc::fence_before_sync();
+        tc::cluster_sync();
+        int last = 0;
+        {
+            const uint32_t a = tc::mapa(tc::smem_u32(&M.last), 0u);
+            asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(last) : "r"(a) : "memory");
+        }
+        if (last) {
+            __threadfence();
+            const float *base = P.parts + ((int64_t)unit * P.batch + c.b) * P.split * (int64_t)kPartFloats;
+            if (tid < NQ) {
+                const int q = tid;
+                float mx = -INFINITY;
+                for (int p2 = 0; p2 < P.split; ++p2) {
+                    const float *rec = base + (int64_t)p2 * kPartFloats;
+                    if (__ldcg(rec + 16 * kMaxNL + q) > 0.0f) mx = fmaxf(mx, __ldcg(rec + q));
+                }
+                float lsum = 0.0f;
+                for (int p2 = 0; p2 < P.split; ++p2) {
+                    const float *rec = base + (int64_t)p2 * kPartFloats;
+                    const float lp = __ldcg(rec + 16 * kMaxNL + q);
+                    if (lp > 0.0f) lsum += lp * __expf(__ldcg(rec + q) - mx);
+                }
+                for (int p2 = 0; p2 < P.split && p2 < kMaxCS; ++p2) {
+                    const float *rec = base + (int64_t)p2 * kPartFloats;
+                    const float lp = __ldcg(rec + 16 * kMaxNL + q);
+                    M.wall[p2][q] = (lsum > 0.0f && lp > 0.0f) ? lp * __expf(__ldcg(rec + q) - mx) / lsum : 0.0f;
+                }
+                const int j = q >> 4;
+                if (rank == 0 && j < U.n_layers && P.entries[U.entry[j]].lse)
+                    P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
+            }
+            __syncthreads();
+            for (int item = tid; item < NQ * n4; item += kThreads) {
+                const int q = item / n4, ch = c_lo + 4 * (item % n4);
+                const int j = q >> 4;
+                if (j >= U.n_layers) continue;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p2 = 0; p2 < P.split && p2 < kMaxCS; ++p2) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (int64_t)p2 * kPartFloats +
+                                                                            2 * 16 * kMaxNL + q * kDim + ch));
+                    const float wgt = M.wall[p2][q];
+                    acc.x += wgt * v.x;
+                    acc.y += wgt * v.y;
+                    acc.z += wgt * v.z;
+                    acc.w += wgt * v.w;
+                }
+                *reinterpret_cast<float4 *>(P.entries[U.entry[j]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch) =
+                    acc;
+            }
+        }
     }
+    tc::cluster_sync();  // no CTA leaves while another reads its shared memory
 }
 
 }  // namespace
@@ -686,85 +859,115 @@ int active_clusters(int dev, int cs)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_kernel<NL>, &cfg) != cudaSuccess) {
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<NL>, &cfg);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
+        log_plan("attention NL=%d: cluster size %d not available (%s)", NL, cs, cudaGetErrorString(e));
         n = 0;
     }
     if (dev >= 0 && dev < 64) cache[dev][cs] = n > 0 ? n : -1;
     return n;
 }
 
-// Cluster size: the one with the lowest modelled time, where a cluster costs
-// a fixed part (queries in, gather latency, merge) plus its longest CTA's
-// tiles, clusters running `active` at a time.
-template <int NL>
-int choose_cluster(int dev, int max_tiles, int n_clusters)
+struct Shape {
+    int split = 1, cs = 1;
+    size_t ws = 0;
+};
+
+// Workspace of a launch that splits each (unit, sequence) over `split` clusters.
+size_t split_bytes(int n_units, int batch, int split)
 {
-    constexpr double kFixed = 3.0, kPerTile = 1.0, kPerCta = 0.04;  // in tile units
-    int best = 1;
+    if (split <= 1) return 0;
+    auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    const size_t groups = (size_t)n_units * batch;
+    return r256(groups * split * kPartFloats * sizeof(float)) + r256(groups * sizeof(uint32_t));
+}
+
+// Launch shape: the (split, cluster size) with the lowest modelled time whose
+// workspace fits `budget`.  A cluster costs a fixed part (queries in, gathers'
+// latency, merge), its busiest CTA's tiles and a little per CTA; a split adds
+// the partials' round trip through global memory; clusters run `active` at a
+// time.  Costs are in units of one tile's processing.
+template <int NL>
+Shape choose_shape(int dev, int max_tiles, int n_groups, size_t budget)
+{
+    constexpr double kFixed = 2.0, kPerTile = 1.0, kPerCta = 0.02, kSplit = 0.35;
+    Shape best;
     double best_cost = 1e300;
-    for (int cs = 1; cs <= kMaxCS; ++cs) {
-        if (cs > 1 && cs > max_tiles) break;
-        const int act = active_clusters<NL>(dev, cs);
-        if (act <= 0) continue;
-        const int per = (max_tiles + cs - 1) / cs;
-        const double waves = std::ceil((double)n_clusters / act);
-        const double cost = waves * (kFixed + kPerTile * per + kPerCta * cs);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = cs;
+    for (int split = 1; split <= kMaxCS; ++split) {
+        if (split > 1 && split > max_tiles) break;
+        const size_t ws = split_bytes(1, n_groups, split);
+        if (ws > budget) continue;
+        const int tiles = (max_tiles + split - 1) / split;
+        for (int cs = 1; cs <= kMaxCS; ++cs) {
+            if (cs > 1 && cs > tiles) break;
+            const int act = active_clusters<NL>(dev, cs);
+            if (act <= 0) continue;
+            const int per = (tiles + cs - 1) / cs;
+            const double waves = std::ceil((double)n_groups * split / act);
+            const double cost = waves * (kFixed + kPerTile * per + kPerCta * cs) + (split > 1 ? kSplit : 0.0);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best.split = split;
+                best.cs = cs;
+                best.ws = ws;
+            }
         }
     }
     return best;
 }
 
 template <int NL>
-cudaError_t launch_nl(const AttnParams &p, int n_units, int batch, int max_tiles, bool pdl, int *flags,
-                      cudaStream_t stream)
+cudaError_t launch_nl(AttnParams &p, int max_tiles, const AttnPlan &plan, int *flags, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = prepare_kernel<NL>(dev)) != cudaSuccess) return e;
-    AttnParams &pp = const_cast<AttnParams &>(p);
-    pp.cs = choose_cluster<NL>(dev, std::max(1, max_tiles), n_units * batch);
+    const Shape sh = choose_shape<NL>(dev, std::max(1, max_tiles), p.n_units * plan.batch,
+                                      plan.workspace ? plan.workspace_bytes : 0);
+    p.cs = sh.cs;
+    p.split = sh.split;
+    if (sh.split > 1) {
+        uint8_t *ws = static_cast<uint8_t *>(plan.workspace);
+        const size_t groups = (size_t)p.n_units * plan.batch;
+        p.parts = reinterpret_cast<float *>(ws);
+        p.tickets = reinterpret_cast<uint32_t *>(ws + (((groups * sh.split * kPartFloats * sizeof(float)) + 255) &
+                                                      ~(size_t)255));
+    }
+    log_plan("attention NL=%d: %d units x %d sequences, %d tiles at most, %d cluster(s) of %d each (%d fit at once)",
+             NL, p.n_units, plan.batch, max_tiles, sh.split, sh.cs, active_clusters<NL>(dev, sh.cs));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(n_units * pp.cs), (unsigned)batch, 1);
+    cfg.gridDim = dim3((unsigned)(p.n_units * sh.split * sh.cs), (unsigned)plan.batch, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<NL>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pp.cs;
+    attr[0].val.clusterDim.x = (unsigned)sh.cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
+    cfg.numAttrs = plan.pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, attn_kernel<NL>, p, flags);
     count_launches(1);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
-}  // namespace
-
-size_t attn_workspace_bytes(const AttnEntry *, int, int, int, int, size_t) { return 0; }
-
-cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream, cudaEvent_t mid_event)
+// Units and tile counts of a plan; returns the largest layer count of a unit.
+int fill_params(const AttnPlan &plan, AttnParams &p, int &max_tiles)
 {
-    (void)mid_event;
-    if (plan.n_entries <= 0 || plan.n_entries > kMaxAttnEntries || plan.batch <= 0) return cudaErrorInvalidValue;
     const int max_group = std::max(1, std::min(kMaxNL, plan.max_group));
     const UnitPlan up = group_units(plan.entries, plan.n_entries, max_group);
-    if ((int)up.units.size() > kMaxUnits) return cudaErrorInvalidValue;
-    std::vector<uint8_t> pbuf(sizeof(AttnParams), 0);
-    AttnParams &p = *reinterpret_cast<AttnParams *>(pbuf.data());
+    if ((int)up.units.size() > kMaxUnits) return -1;
     p.batch = plan.batch;
     p.topk = plan.topk;
     p.window = plan.window;
     p.win_tiles = plan.window > 0 ? (plan.window + kRows - 1) / kRows : 0;
     p.seq_lens = plan.seq_lens;
+    p.split = 1;
     for (int e = 0; e < plan.n_entries; ++e) {
         const AttnEntry &en = plan.entries[e];
         EntryDev &E = p.entries[e];
@@ -774,7 +977,8 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
         E.out = en.out;
         E.lse = en.lse;
     }
-    int max_tiles = 0, nl_used = 1;
+    int nl_used = 1;
+    max_tiles = 0;
     for (size_t u = 0; u < up.units.size(); ++u) {
         UnitDev &U = p.units[u];
         const std::vector<int> &g = up.units[u];
@@ -789,8 +993,38 @@ cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stre
         nl_used = std::max(nl_used, U.n_layers);
     }
     p.n_units = (int)up.units.size();
-    if (nl_used == 1) return launch_nl<1>(p, p.n_units, plan.batch, max_tiles, plan.pdl != 0, flags, stream);
-    return launch_nl<2>(p, p.n_units, plan.batch, max_tiles, plan.pdl != 0, flags, stream);
+    return nl_used;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(const AttnPlan &plan, size_t budget)
+{
+    if (plan.n_entries <= 0 || plan.n_entries > kMaxAttnEntries || plan.batch <= 0) return 0;
+    std::vector<uint8_t> pbuf(sizeof(AttnParams), 0);
+    AttnParams &p = *reinterpret_cast<AttnParams *>(pbuf.data());
+    int max_tiles = 0;
+    const int nl = fill_params(plan, p, max_tiles);
+    if (nl < 0) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if ((nl == 1 ? prepare_kernel<1>(dev) : prepare_kernel<2>(dev)) != cudaSuccess) return 0;
+    const Shape sh = nl == 1 ? choose_shape<1>(dev, std::max(1, max_tiles), p.n_units * plan.batch, budget)
+                             : choose_shape<2>(dev, std::max(1, max_tiles), p.n_units * plan.batch, budget);
+    return split_bytes(p.n_units, plan.batch, sh.split);
+}
+
+cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream, cudaEvent_t mid_event)
+{
+    (void)mid_event;
+    if (plan.n_entries <= 0 || plan.n_entries > kMaxAttnEntries || plan.batch <= 0) return cudaErrorInvalidValue;
+    std::vector<uint8_t> pbuf(sizeof(AttnParams), 0);
+    AttnParams &p = *reinterpret_cast<AttnParams *>(pbuf.data());
+    int max_tiles = 0;
+    const int nl = fill_params(plan, p, max_tiles);
+    if (nl < 0) return cudaErrorInvalidValue;
+    if (nl == 1) return launch_nl<1>(p, max_tiles, plan, flags, stream);
+    return launch_nl<2>(p, max_tiles, plan, flags, stream);
 }
 
 }  // namespace csa2

@@ -8,7 +8,10 @@
 #include <cstdio>
 #include <algorithm>
 #include <array>
+#include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <set>
 #include <string>
 #include <utility>
 #include <vector>
@@ -39,6 +42,24 @@ csa2_status fail(csa2_status s, const char *fmt, ...)
 }
 
 }  // namespace
+
+void csa2::log_plan(const char *fmt, ...)
+{
+    static const bool on = [] {
+        const char *v = getenv("CSA2_LOG");
+        return v && v[0] && !(v[0] == '0' && v[1] == 0);
+    }();
+    if (!on) return;
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    static std::mutex mu;
+    static std::set<std::string> seen;
+    std::lock_guard<std::mutex> lock(mu);
+    if (seen.insert(buf).second) fprintf(stderr, "[csa2] %s\n", buf);
+}
 
 csa2_status csa2::set_error(csa2_status s, const char *fmt, ...)
 {
@@ -140,11 +161,25 @@ namespace csa2 {
 
 size_t sparse_attn_workspace_within(int32_t batch, int32_t topk, int32_t swa_window, size_t budget)
 {
-    (void)batch;
-    (void)topk;
-    (void)swa_window;
-    (void)budget;
-    return 0;  // attention merges its partials inside each cluster
+    if (batch <= 0 || topk < 0 || swa_window < 0) return 0;
+    static const int32_t any_index = 0;  // stands for "an index list is given"
+    static const float any_q = 0.0f;
+    AttnEntry en;
+    memset(&en, 0, sizeof(en));
+    en.has_kv = topk > 0 ? 1 : 0;
+    en.idx = topk > 0 ? &any_index : nullptr;
+    en.kv.data = reinterpret_cast<uint8_t *>(const_cast<int32_t *>(&any_index));
+    en.has_swa = swa_window > 0 ? 1 : 0;
+    en.q = &any_q;
+    AttnPlan plan;
+    memset(&plan, 0, sizeof(plan));
+    plan.entries = &en;
+    plan.n_entries = 1;
+    plan.batch = batch;
+    plan.topk = topk;
+    plan.window = swa_window;
+    plan.max_group = 1;
+    return attn_workspace_bytes(plan, budget);
 }
 
 }  // namespace csa2
@@ -463,8 +498,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
         st = check_cache(swa, CSA2_FMT_FP8_SWA, batch, swa_window, "swa");
         if (st) return st;
     }
-    (void)workspace;
-    (void)workspace_bytes;
+    if (workspace && !aligned(workspace, 256)) return fail(CSA2_ERR_WORKSPACE, "workspace must be 256-byte aligned");
     const int eff_topk = idx ? topk : 0;
     int *fp = flags_ptr();
     if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
@@ -487,6 +521,8 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     plan.seq_lens = seq_lens;
     plan.max_group = 1;
     plan.pdl = 1;
+    plan.workspace = workspace;
+    plan.workspace_bytes = workspace ? workspace_bytes : 0;
     cudaError_t e = launch_attention(plan, fp, static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
 }
@@ -625,14 +661,40 @@ void add_index_job(const csa2_layer_desc *layers, int l, int32_t pool_len, std::
     jobs.push_back(j);
 }
 
+// The per-layer call's workspace: [indexing region][attention region].
+size_t layer_attn_offset(size_t idx_bytes) { return round256(idx_bytes); }
+size_t layer_attn_bytes(int32_t batch, int32_t topk, int32_t swa_window)
+{
+    return round256(std::max(sparse_attn_workspace_within(batch, topk, swa_window, SIZE_MAX),
+                             sparse_attn_workspace_within(batch, 0, swa_window, SIZE_MAX)));
+}
+
 // One decode step in the phased order: level 0 (Full layers and pool-free
 // Reindex layers), level 1 (pool-restricted Reindex layers), then the
 // attention of every layer.
 struct StepLayout {
     std::vector<IdxJob> level[2];
     LevelWs lw[2];
-    size_t fused_bytes = 0, old_bytes = 0, total = 0;
+    size_t fused_bytes = 0, old_bytes = 0, attn_bytes = 0, total = 0;
 };
+
+AttnPlan step_attn_plan(const std::vector<AttnEntry> &entries, int32_t batch, const int32_t *seq_lens, int32_t topk,
+                        int32_t swa_window, void *ws, size_t ws_bytes)
+{
+    AttnPlan ap;
+    memset(&ap, 0, sizeof(ap));
+    ap.entries = entries.data();
+    ap.n_entries = (int)entries.size();
+    ap.batch = batch;
+    ap.topk = topk;
+    ap.window = swa_window;
+    ap.seq_lens = seq_lens;
+    ap.max_group = 2;
+    ap.pdl = 1;
+    ap.workspace = ws;
+    ap.workspace_bytes = ws_bytes;
+    return ap;
+}
 
 csa2_status plan_step(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch, int32_t max_seq_len,
                       int32_t topk, int32_t pool_len, int32_t swa_window, StepLayout &P)
@@ -659,7 +721,11 @@ csa2_status plan_step(const csa2_layer_desc *layers, int32_t n_layers, int32_t b
         P.fused_bytes = std::max(P.fused_bytes, P.lw[lv].fused_bytes);
         P.old_bytes = std::max(P.old_bytes, P.lw[lv].old_bytes);
     }
-    P.total = P.fused_bytes + P.old_bytes;
+    {
+        const std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
+        P.attn_bytes = round256(attn_workspace_bytes(step_attn_plan(entries, batch, nullptr, topk, swa_window, nullptr, 0)));
+    }
+    P.total = P.fused_bytes + P.old_bytes + P.attn_bytes;
     return CSA2_OK;
 }
 
@@ -699,15 +765,8 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
     }
     if ((e = mark(3, s)) != cudaSuccess) return cuda_fail(e, "event");
     std::vector<AttnEntry> entries = step_entries(layers, n_layers, swa_window);
-    AttnPlan ap;
-    ap.entries = entries.data();
-    ap.n_entries = n_layers;
-    ap.batch = batch;
-    ap.topk = topk;
-    ap.window = swa_window;
-    ap.seq_lens = seq_lens;
-    ap.max_group = 2;
-    ap.pdl = 1;
+    const AttnPlan ap = step_attn_plan(entries, batch, seq_lens, topk, swa_window,
+                                       P.attn_bytes ? ws + P.fused_bytes + P.old_bytes : nullptr, P.attn_bytes);
     e = launch_attention(ap, fp, s, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     if ((e = mark(4, s)) != cudaSuccess || (e = mark(5, s)) != cudaSuccess) return cuda_fail(e, "event");
@@ -718,7 +777,7 @@ size_t csa2_decode_layer_workspace(const csa2_layer_desc *layers, int32_t n_laye
                                    int32_t max_seq_len, int32_t topk, int32_t pool_len, int32_t swa_window)
 {
     if (!layers || n_layers <= 0 || check_sizes(batch, max_seq_len, topk, pool_len, swa_window)) return 0;
-    size_t need = 256;
+    size_t idx_need = 0;
     for (int l = 0; l < n_layers; ++l) {
         if (check_layer(layers, l, batch, max_seq_len, pool_len, swa_window)) return 0;
         const csa2_layer_desc &d = layers[l];
@@ -726,9 +785,9 @@ size_t csa2_decode_layer_workspace(const csa2_layer_desc *layers, int32_t n_laye
         std::vector<IdxJob> jobs;
         add_index_job(layers, l, pool_len, jobs);
         const LevelWs lw = level_ws(jobs.data(), 1, batch, max_seq_len);
-        need = std::max(need, lw.fused_bytes + lw.old_bytes);
+        idx_need = std::max(idx_need, lw.fused_bytes + lw.old_bytes);
     }
-    return need;
+    return std::max<size_t>(256, layer_attn_offset(idx_need) + layer_attn_bytes(batch, topk, swa_window));
 }
 
 csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, int32_t layer, int32_t batch,
@@ -773,7 +832,21 @@ csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, i
         en.has_kv = 1;
         en.idx = (d.mode == CSA2_MODE_REUSE) ? layers[d.idx_src].idx_out : d.idx_out;
     }
+    // the attention's region follows the largest indexing region of the schedule
+    size_t idx_need = 0;
+    for (int l = 0; l < n_layers; ++l) {
+        const csa2_layer_desc &dl = layers[l];
+        if (dl.mode != CSA2_MODE_FULL && dl.mode != CSA2_MODE_REINDEX) continue;
+        std::vector<IdxJob> jobs;
+        add_index_job(layers, l, pool_len, jobs);
+        const LevelWs lw = level_ws(jobs.data(), 1, batch, max_seq_len);
+        idx_need = std::max(idx_need, lw.fused_bytes + lw.old_bytes);
+    }
+    const size_t a_off = layer_attn_offset(idx_need), a_bytes = layer_attn_bytes(batch, topk, swa_window);
+    st = check_ws(workspace, workspace_bytes, a_off + a_bytes);
+    if (st) return st;
     AttnPlan ap;
+    memset(&ap, 0, sizeof(ap));
     ap.entries = &en;
     ap.n_entries = 1;
     ap.batch = batch;
@@ -782,6 +855,8 @@ csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, i
     ap.seq_lens = seq_lens;
     ap.max_group = 1;
     ap.pdl = 1;
+    ap.workspace = a_bytes ? static_cast<uint8_t *>(workspace) + a_off : nullptr;
+    ap.workspace_bytes = a_bytes;
     e = launch_attention(ap, fp, s, nullptr);
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "attention launch");
 }

@@ -106,8 +106,7 @@ struct Sel {
 };
 
 struct Misc {
-    __half qpre[2][kIdxHeads][kIdxDim];
-    float wq[2][kIdxHeads];
+    scan::QuerySet qs;
     float sk_lut[256];
     Sel sel[kMaxSel];
     uint32_t scratch[48];
@@ -131,52 +130,57 @@ struct Thresh {
     uint32_t at;
 };
 
-__device__ Thresh find_threshold(const uint32_t *h, int nbins, uint32_t need, uint32_t *scratch)
+__device__ __noinline__ Thresh find_threshold(const uint32_t *h, int nbins, uint32_t need, uint32_t *scratch)
 {
-    const int tid = threadIdx.x;
-    const int per = nbins / kThreads;
-    const int hi = nbins - tid * per;
-    uint32_t local = 0;
-    for (int i = 1; i <= per; ++i) local += h[hi - i];
-    uint32_t incl = local;
-    const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) scratch[warp] = incl;
+    // bins by rank from the top (rank k = bin nbins-1-k); warp w sums ranks
+    // [w seg, (w+1) seg) with coalesced reads, a prefix over the warps finds
+    // the segment holding the need-th key, and that warp walks it 32 at a time
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int seg = nbins / kWarps;
+    uint32_t wsum = 0;
+    for (int k = lane; k < seg; k += 32) wsum += h[nbins - 1 - (warp * seg + k)];
+    wsum = __reduce_add_sync(0xFFFFFFFFu, wsum);
+    if (lane == 0) scratch[warp] = wsum;
     __syncthreads();
-    if (warp == 0) {
-        const uint32_t v = (lane < kWarps) ? scratch[lane] : 0u;
-        uint32_t s = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, s, o);
-            if (lane >= o) s += u;
+    if (tid == 0) {
+        uint32_t run = 0;
+        int wsel = -1;
+        uint32_t before = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            if (wsel < 0 && run + scratch[w] >= need) {
+                wsel = w;
+                before = run;
+            }
+            run += scratch[w];
         }
-        if (lane < kWarps) scratch[lane] = s - v;
-        if (lane == kWarps - 1) scratch[kWarps] = s;
+        scratch[kWarps] = run;                      // total
+        scratch[kWarps + 3] = (uint32_t)wsel;       // warp holding the threshold, or -1
+        scratch[kWarps + 4] = before;               // count above its segment
+        scratch[kWarps + 1] = 0xFFFFFFFFu;
+        scratch[kWarps + 2] = run;
     }
     __syncthreads();
-    const uint32_t excl = scratch[warp] + incl - local;
-    const uint32_t total = scratch[kWarps];
-    __syncthreads();
-    if (total < need) {
-        if (tid == 0) {
-            scratch[kWarps + 1] = 0xFFFFFFFFu;
-            scratch[kWarps + 2] = total;
-        }
-    } else if (excl < need && need <= excl + local) {
-        uint32_t above = excl;
-        for (int i = 1; i <= per; ++i) {
-            const uint32_t c = h[hi - i];
-            if (need <= above + c) {
-                scratch[kWarps + 1] = (uint32_t)(hi - i);
-                scratch[kWarps + 2] = above;
+    if (warp == (int)scratch[kWarps + 3]) {
+        uint32_t above = scratch[kWarps + 4];
+        for (int k0 = 0; k0 < seg; k0 += 32) {
+            const int rk = warp * seg + k0 + lane;
+            const uint32_t c = h[nbins - 1 - rk];
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, above + incl >= need);
+            if (hit) {
+                const int first = __ffs(hit) - 1;
+                if (lane == first) {
+                    scratch[kWarps + 1] = (uint32_t)(nbins - 1 - rk);
+                    scratch[kWarps + 2] = above + incl - c;
+                }
                 break;
             }
-            above += c;
+            above += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
     }
     __syncthreads();
@@ -189,7 +193,7 @@ __device__ Thresh find_threshold(const uint32_t *h, int nbins, uint32_t need, ui
 }
 
 // Exclusive prefix of v[0..n) in place (n <= kMaxG); returns the total.
-__device__ uint32_t block_exclusive_scan(uint32_t *v, int n, uint32_t *scratch)
+__device__ __noinline__ uint32_t block_exclusive_scan(uint32_t *v, int n, uint32_t *scratch)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (n + kThreads - 1) / kThreads;
@@ -227,16 +231,39 @@ __device__ uint32_t block_exclusive_scan(uint32_t *v, int n, uint32_t *scratch)
     return total;
 }
 
-// Bounded group barrier: counter `bar` reaches `target` (G per round).
+// dst[0..n) = src[0..n) (global, L2) by the CTA, eight independent loads in
+// flight per thread before any is stored.
+template <typename T>
+__device__ __forceinline__ void load_to_smem(T *dst, const T *src, int n)
+{
+    for (int base = 0; base < n; base += 8 * kThreads) {
+        T v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = base + k * kThreads + (int)threadIdx.x;
+            if (i < n) v[k] = __ldcg(src + i);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = base + k * kThreads + (int)threadIdx.x;
+            if (i < n) dst[i] = v[k];
+        }
+    }
+}
+
+// Bounded group barrier: counter `bar` reaches `target` (G per round).  The
+// CTA barrier orders every thread's writes before thread 0's fence, whose
+// gpu-scope ordering is cumulative; thread 0 alone arrives, polls (relaxed)
+// and fences again before the CTA barrier releases the others.
 __device__ __forceinline__ void group_barrier(uint32_t *bar, uint32_t target, uint32_t limit, Misc &M)
 {
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        atomicAdd(bar, 1u);
+        __threadfence();
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;\n" ::"l"(bar) : "memory");
         uint32_t v = 0, i = 0;
         do {
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(bar) : "memory");
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(bar) : "memory");
         } while (v < target && ++i < limit);
         if (v < target) M.ok = 0;
         __threadfence();
@@ -275,18 +302,23 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     __syncthreads();
     tc::pdl_wait();
 
-    int L = __ldcg(P.seq_lens + b);
-    if (L < 0 || L > P.max_len) {
-        if (tid == 0 && g == 0) raise_flag(flags, kFlagBounds);
-        L = L < 0 ? 0 : P.max_len;
-    }
     const bool direct = job.pool == nullptr;
-    const int64_t n_cand = direct ? L : job.pool_len;
     const int64_t c0 = (int64_t)g * P.chunk;
-    const int64_t c1 = min(n_cand, c0 + P.chunk);
-    const int nk = (int)max((int64_t)0, c1 - c0);
-    const int n_batches = (nk + kBatchKeys - 1) / kBatchKeys;
-    const int32_t *pool = direct ? nullptr : job.pool + (int64_t)b * job.pool_len;
+    auto load_len = [&]() {
+        int v = __ldcg(P.seq_lens + b);
+        if (v < 0 || v > P.max_len) {
+            if (tid == 0 && g == 0) raise_flag(flags, kFlagBounds);
+            v = v < 0 ? 0 : P.max_len;
+        }
+        return v;
+    };
+    // contiguous caches: the tile copies cover the candidates up to max_len and go
+    // out before the sequence length is known (positions past it are ignored);
+    // paged caches map only the sequence's own pages, so they wait for it
+    const bool early = direct && job.keys.page_size == 0;
+    int L = early ? -1 : load_len();
+    const int64_t c1_max = min((int64_t)(direct ? (early ? P.max_len : L) : job.pool_len), c0 + P.chunk);
+    const int nb_max = (int)max((int64_t)0, (c1_max - c0 + kBatchKeys - 1) / kBatchKeys);
 
     auto issue_batch = [&](int k) {
         // thread 0: the bulk copies of batch k's tiles into ring slot k % slots
@@ -296,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         for (int i = 0; i < kBatchTiles; ++i) {
             src[i] = nullptr;
             const int64_t p0 = c0 + (int64_t)k * kBatchKeys + (int64_t)i * kIdxTile;
-            if (p0 < c1) {
+            if (p0 < c1_max) {
                 const int64_t s = slot_of(job.keys, b, p0);
                 // a 64-aligned position block is one whole tile (page and stride are multiples of 64)
                 if (s >= 0 && s + kIdxTile <= job.keys.n_slots) {
@@ -310,12 +342,27 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         }
         M.tile_ok[slot] = okm;
         tc::mbar_expect_tx(&M.bar[slot], bytes);
-        for (int i = 0; i < kBatchTiles; ++i)
-            if (src[i]) tc::bulk_g2s(ring + (size_t)slot * kBatchBytes + i * kIdxTileBytes, src[i], kIdxTileBytes, &M.bar[slot]);
+        // runs of tiles adjacent in memory (always, in a contiguous cache) go as one copy
+        for (int i = 0; i < kBatchTiles;) {
+            if (!src[i]) {
+                ++i;
+                continue;
+            }
+            int n = 1;
+            while (i + n < kBatchTiles && src[i + n] == src[i] + (size_t)n * kIdxTileBytes) ++n;
+            tc::bulk_g2s(ring + (size_t)slot * kBatchBytes + i * kIdxTileBytes, src[i], (uint32_t)n * kIdxTileBytes,
+                         &M.bar[slot]);
+            i += n;
+        }
     };
     if (direct && tid == 0) {
-        for (int k = 0; k < min(n_batches, P.ring_slots); ++k) issue_batch(k);
+        for (int k = 0; k < min(nb_max, P.ring_slots); ++k) issue_batch(k);
     }
+    if (L < 0) L = load_len();
+    const int64_t n_cand = direct ? L : job.pool_len;
+    const int64_t c1 = min(n_cand, c0 + P.chunk);
+    const int nk = (int)max((int64_t)0, c1 - c0);
+    const int32_t *pool = direct ? nullptr : job.pool + (int64_t)b * job.pool_len;
 
     // appends of a Full layer: the new main-KV row (warp 0 of the last CTA) and
     // the new indexer key (warp 1 of the CTA that scans position L-1)
@@ -375,21 +422,12 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         }
     }
 
-    scan::prep_queries(tid, job.n_q, job.q_idx, job.w, b, M.qpre, M.wq);
+    scan::prep_query_set(tid, job.n_q, job.q_idx, job.w, b, M.qs);
     __syncthreads();
 
-    // ---- scan ------------------------------------------------------------------------
-    const int gq = lane >> 2, t = lane & 3;
-    uint32_t bfrag[4][2];
-    scan::build_bfrag(M.qpre, gq, t, bfrag);
-    const int my_q = t >> 1;
-    const bool scoring = (t & 1) && my_q < n_rows;
-    const float w0 = M.wq[my_q][0], w1 = M.wq[my_q][1], w2 = M.wq[my_q][2], w3 = M.wq[my_q][3];
-    float *score_out = (my_q < n_rows && job.out_scores[my_q]) ? job.out_scores[my_q] + (int64_t)b * P.scores_stride
-                                                                : nullptr;
-    uint32_t *my_keys = keys + (size_t)my_q * P.chunk;
-    uint32_t *my_hist = hist + my_q * kHistBins;
-    const int nb_loop = direct ? n_batches : (nk + kBatchKeys - 1) / kBatchKeys;
+    // ---- scan: one thread scores whole keys (all of this job's queries)
+    // every issued batch is waited for, also those past the sequence's end
+    const int nb_loop = direct ? nb_max : (nk + kBatchKeys - 1) / kBatchKeys;
     for (int k = 0; k < nb_loop; ++k) {
         const int slot = direct ? k % P.ring_slots : 0;
         bool have = true;
@@ -416,42 +454,51 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         const uint8_t *tiles = ring + (size_t)slot * kBatchBytes;
         const int base = k * kBatchKeys;  // local index of the batch's first candidate
 #pragma unroll 1
-        for (int gA = warp; gA < kBatchKeys / 16; gA += 2 * kWarps) {
-            scan::KeyLoad kl[4];
-            int li[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int grp = gA + kWarps * (i >> 1);
-                li[i] = base + grp * 16 + gq + 8 * (i & 1);
-                if (direct) {
-                    const int ti = grp >> 2;
-                    kl[i] = scan::key_from_tile(tiles + ti * kIdxTileBytes, (grp & 3) * 16 + gq + 8 * (i & 1), t);
-                    kl[i].ok = have && li[i] < nk && ((M.tile_ok[slot] >> ti) & 1u);
-                    if (!kl[i].ok) kl[i].w[0] = kl[i].w[1] = kl[i].w[2] = kl[i].w[3] = kl[i].sc = 0u;
-                } else {
-                    int64_t pos = -1;
-                    if (li[i] < nk) pos = (int64_t)__ldcg(pool + c0 + li[i]);
-                    if (pos >= L) pos = -1;
-                    kl[i] = scan::key_from_global(job.keys, b, pos, t, flags);
-                }
-            }
-            float sc[4];
-            scan::score4(kl, bfrag, M.sk_lut, w0, w1, w2, w3, t, sc);
-            if (scoring) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (li[i] >= nk) continue;
-                    const uint32_t key = kl[i].ok ? score_key(sc[i]) : 0u;
-                    my_keys[li[i]] = key;
-                    if (key) {
-                        atomicAdd(&my_hist[key >> (32 - kHistBits)], 1u);
-                        if (score_out) score_out[c0 + li[i]] = sc[i];
+        for (int i = tid; i < kBatchKeys && base < nk; i += kThreads) {
+            const int li = base + i;
+            bool ok = li < nk;
+            uint4 c0v = make_uint4(0u, 0u, 0u, 0u), c1v = c0v;
+            uint32_t scw = 0u;
+            if (ok && direct) {
+                const int ti = i / kIdxTile, rr = i % kIdxTile;
+                ok = have && ((M.tile_ok[slot] >> ti) & 1u);
+                const uint8_t *tile = tiles + ti * kIdxTileBytes;
+                c0v = *reinterpret_cast<const uint4 *>(tile + rr * 32);
+                c1v = *reinterpret_cast<const uint4 *>(tile + rr * 32 + 16);
+                scw = *reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4);
+            } else if (ok) {
+                int64_t pos = (int64_t)__ldcg(pool + c0 + li);
+                ok = pos >= 0 && pos < L;
+                if (ok) {
+                    const int64_t slotk = slot_of(job.keys, b, pos);
+                    if (slotk < 0) {
+                        raise_flag(flags, kFlagBounds);
+                        ok = false;
+                    } else {
+                        const uint8_t *tile = job.keys.data + (slotk / kIdxTile) * kIdxTileBytes;
+                        const int rr = (int)(slotk % kIdxTile);
+                        c0v = __ldcg(reinterpret_cast<const uint4 *>(tile + rr * 32));
+                        c1v = __ldcg(reinterpret_cast<const uint4 *>(tile + rr * 32 + 16));
+                        scw = __ldcg(reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4));
                     }
                 }
             }
+            uint32_t kw[16];
+            float sk[4];
+            scan::unpack_key(c0v, c1v, scw, M.sk_lut, kw, sk);
+            for (int q = 0; q < n_rows; ++q) {
+                const float sc = scan::score_key_int(kw, sk, M.qs, q);
+                const uint32_t key = ok ? score_key(sc) : 0u;
+                if (li < nk) keys[(size_t)q * P.chunk + li] = key;
+                // the histogram of the keys' top bits: one atomic per distinct bin of the warp
+                const uint32_t tag = key ? (key >> (32 - kHistBits)) : (0x80000000u | (uint32_t)lane);
+                const uint32_t same = __match_any_sync(__activemask(), tag);
+                if (key && (__ffs(same) - 1) == lane) atomicAdd(&hist[q * kHistBins + (key >> (32 - kHistBits))], __popc(same));
+                if (key && job.out_scores[q]) job.out_scores[q][(int64_t)b * P.scores_stride + c0 + li] = sc;
+            }
         }
         __syncthreads();
-        if (direct && tid == 0 && k + P.ring_slots < n_batches) {
+        if (direct && tid == 0 && k + P.ring_slots < nb_max) {
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             issue_batch(k + P.ring_slots);
         }
@@ -498,8 +545,16 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                 int64_t cut = INT64_MAX;
                 uint32_t ties_need = 0;
                 if (st == kPubCand) {
+                    // every CTA's published count above the prefix goes out with the
+                    // list's length and the list, one round trip to L2
+                    uint32_t cnt_pub[kMaxG / kThreads];
+#pragma unroll
+                    for (int j = 0; j < kMaxG / kThreads; ++j) {
+                        const int i = tid + j * kThreads;
+                        cnt_pub[j] = i < G ? __ldcg(&GS.cnt[si][i][0]) : 0u;
+                    }
                     const uint32_t n = min(__ldcg(&GS.hdr.cand_n[si]), (uint32_t)cap);
-                    for (uint32_t i = tid; i < n; i += kThreads) cands[i] = __ldcg(&GS.cand[si][i]);
+                    load_to_smem(cands, &GS.cand[si][0], (int)n);
                     for (int i = tid; i < G; i += kThreads) cnt_sel[i] = 0u;
                     __syncthreads();
                     // the need-th largest key among the candidates (they share the top nb bits)
@@ -560,7 +615,11 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                             atomicAdd(&cnt_sel[min((int)(cd.y / (uint32_t)P.chunk), G - 1)], 1u);
                     }
                     __syncthreads();
-                    for (int i = tid; i < G; i += kThreads) cnt_sel[i] += __ldcg(&GS.cnt[si][i][0]);
+#pragma unroll
+                    for (int j = 0; j < kMaxG / kThreads; ++j) {
+                        const int i = tid + j * kThreads;
+                        if (i < G) cnt_sel[i] += cnt_pub[j];
+                    }
                     __syncthreads();
                 } else {
                     // counts path: every valid key (all_valid) or keys above T plus the lowest ties
@@ -663,7 +722,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                     bits = 10;
                 }
                 uint32_t *h = reinterpret_cast<uint32_t *>(ring);  // idle after the scan
-                for (int i = tid; i < (1 << bits); i += kThreads) h[i] = __ldcg(gh + i);
+                load_to_smem(h, gh, 1 << bits);
                 __syncthreads();
                 const Thresh th = find_threshold(h, max(1 << bits, kThreads), S.need, M.scratch);
                 if (tid == 0) {
@@ -686,25 +745,39 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
             // publish what the next round reads
             const Sel S = M.sel[si];
             if (S.state == kPubCand) {
-                uint32_t na = 0;
+                // keys above the prefix are counted; keys at it go to the group's
+                // candidate list, one global reservation per CTA
+                uint32_t na = 0, nc = 0;
                 for (int i = tid; i < nk; i += kThreads) {
                     const uint32_t key = rk[i];
                     if (!key) continue;
                     const uint32_t pk = prefix_of(key, S.nb);
-                    if (pk > S.prefix) {
-                        ++na;
-                    } else if (pk == S.prefix) {
-                        const uint32_t at = atomicAdd(&GS.hdr.cand_n[si], 1u);
-                        if (at < (uint32_t)kCandCap) GS.cand[si][at] = make_uint2(key, (uint32_t)(c0 + i));
-                    }
+                    na += pk > S.prefix;
+                    nc += pk == S.prefix;
                 }
                 na = __reduce_add_sync(0xFFFFFFFFu, na);
-                if (lane == 0) M.warp_a[warp] = na;
+                nc = __reduce_add_sync(0xFFFFFFFFu, nc);
+                if (lane == 0) {
+                    M.warp_a[warp] = na;
+                    M.warp_t[warp] = nc;
+                }
                 __syncthreads();
                 if (tid == 0) {
-                    uint32_t s = 0;
-                    for (int w = 0; w < kWarps; ++w) s += M.warp_a[w];
-                    GS.cnt[si][g][0] = s;
+                    uint32_t sa = 0, sc = 0;
+                    for (int w = 0; w < kWarps; ++w) {
+                        sa += M.warp_a[w];
+                        sc += M.warp_t[w];
+                    }
+                    GS.cnt[si][g][0] = sa;
+                    M.bcast[0] = sc ? atomicAdd(&GS.hdr.cand_n[si], sc) : 0u;  // this CTA's first slot
+                }
+                __syncthreads();
+                for (int i = tid; i < nk; i += kThreads) {
+                    const uint32_t key = rk[i];
+                    if (key && prefix_of(key, S.nb) == S.prefix) {
+                        const uint32_t at = atomicAdd(&M.bcast[0], 1u);
+                        if (at < (uint32_t)kCandCap) GS.cand[si][at] = make_uint2(key, (uint32_t)(c0 + i));
+                    }
                 }
             } else if (S.state == kPubCount) {
                 uint32_t na = 0, nt = 0;
@@ -806,7 +879,10 @@ bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp)
     int G = (int)std::max<int64_t>(1, std::min<int64_t>((cand + 63) / 64, n_sm / n_groups));
     if (G < 1) G = 1;
     int64_t chunk = ((cand + G - 1) / G + 63) / 64 * 64;
-    if (chunk > kMaxChunk) return false;
+    if (chunk > kMaxChunk) {
+        log_plan("index: %lld candidates per CTA exceed %d: scan + select kernels", (long long)chunk, kMaxChunk);
+        return false;
+    }
     const int batches = (int)((chunk + kBatchKeys - 1) / kBatchKeys);
     const int slots = batches > 1 ? 2 : 1;
     const size_t smem = fused_smem(slots, (int)chunk);
@@ -821,12 +897,17 @@ bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_fused_kernel, kThreads, smem) != cudaSuccess ||
         per_sm < 1)
         return false;
-    if ((int64_t)G * n_groups > (int64_t)per_sm * n_sm) return false;
+    if ((int64_t)G * n_groups > (int64_t)per_sm * n_sm) {
+        log_plan("index: %d groups x %d CTAs do not fit (%d per SM): scan + select kernels", n_groups, G, per_sm);
+        return false;
+    }
     fp.G = G;
     fp.chunk = (int)chunk;
     fp.ring_slots = slots;
     fp.smem = smem;
     fp.cap = (int)std::min<size_t>(kCandCap, (size_t)slots * kBatchBytes / 8 - kMaxG / 2);
+    log_plan("index: %d groups x %d CTAs of %lld candidates (%d per SM fit), candidate capacity %d", n_groups, G,
+             (long long)chunk, per_sm, fp.cap);
     return true;
 }
 

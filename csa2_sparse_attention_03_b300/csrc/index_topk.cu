@@ -14,17 +14,14 @@
 //          1,024 candidates: for a full-context scan it pulls its 16 key
 //          tiles (2,304 B each) into shared memory with bulk async copies
 //          completing on one mbarrier, so every tile is in flight at once;
-//          for a pool scan it gathers each key.  A warp scores 16 keys per
-//          step: the E2M1 block dot products of up to two queries (a Full
-//          layer and the pool-free Reindex layer that shares its keys) x 4
-//          heads run as one m16n8k16 fp16 MMA per 16-channel block -- exact,
-//          because E2M1 codes and the block-scaled query (scale x code, <= 6
-//          significant bits) are exact in fp16 and every partial sum is a
-//          small multiple of the block's quantum.  The epilogue applies the
-//          key scales and head weights in the fixed order on CUDA cores,
-//          writes an order-preserving uint32 key per candidate (0 = not a
-//          candidate) and adds its CTA's 2,048-bin histogram of the keys'
-//          top 11 bits into the row's global histogram.
+//          for a pool scan it gathers each key.  A thread scores whole keys
+//          for up to two queries (a Full layer and the pool-free Reindex
+//          layer that shares its keys): the E2M1 block dot products as exact
+//          integer sums (dp4a over the doubled codes), then the key scales and
+//          head weights in the fixed order.  It writes an order-preserving
+//          uint32 key per candidate (0 = not a candidate) and adds its CTA's
+//          2,048-bin histogram of the keys' top 11 bits into the row's global
+//          histogram.  Used for problems too large for the fused launch.
 //  select  one cluster of 8 CTAs per (row, target): an exact radix select
 //          of the K-th largest key (11 + 11 + 10 bit digits) with the
 //          histograms reduced across the cluster through distributed shared
@@ -57,8 +54,7 @@ struct ScanBatch {
 struct __align__(128) ScanSmem {
     uint8_t tiles[kScanTiles][kIdxTileBytes];  // 36,864 B
     uint32_t hist[2][kHistBins];
-    __half qpre[2][kIdxHeads][kIdxDim];
-    float wq[2][kIdxHeads];
+    scan::QuerySet qs;
     int32_t tile_ok[kScanTiles];
     float sk_lut[256];  // E4M3 code -> value
     uint64_t bar;
@@ -73,8 +69,6 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
     const ScanJob &job = sb.jobs[blockIdx.z];
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
     int L = __ldg(seq_lens + b);
     if (L < 0 || L > max_len) {
         if (tid == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBounds);
@@ -115,18 +109,8 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
 
     for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&S.hist[0][0])[i] = 0u;
     S.sk_lut[tid] = e4m3_value((uint32_t)tid);  // 256 threads
-    scan::prep_queries(tid, job.n_q, job.q_idx, job.w, b, S.qpre, S.wq);
+    scan::prep_query_set(tid, job.n_q, job.q_idx, job.w, b, S.qs);
     __syncthreads();
-
-    uint32_t bfrag[4][2];
-    scan::build_bfrag(S.qpre, g, t, bfrag);
-    const int my_q = t >> 1;  // query of this thread's two columns
-    const bool finisher = (t & 1) != 0;
-    const float w0 = S.wq[my_q][0], w1 = S.wq[my_q][1], w2 = S.wq[my_q][2], w3 = S.wq[my_q][3];
-    const int64_t my_row = (int64_t)job.row[my_q < job.n_q ? my_q : 0] * batch + b;
-    uint32_t *key_out = bufs.keys + my_row * bufs.cand_cap;
-    float *score_out = (my_q < job.n_q) ? sb.out_scores[blockIdx.z][my_q] : nullptr;
-    if (score_out) score_out += (int64_t)b * sb.scores_stride;
     const int32_t *pool = job.pool ? job.pool + (int64_t)b * job.pool_len : nullptr;
 
     // 2. wait for the tiles (bounded)
@@ -139,40 +123,48 @@ __global__ void __launch_bounds__(kScanWarps * 32, 4) scan_kernel(const __grid_c
         }
     }
 
-    // Each warp scores two 16-key groups per step (32 keys, 8 MMAs), so the two
-    // groups' load -> convert -> MMA -> epilogue chains overlap.
-    const bool scoring = finisher && my_q < job.n_q;
+    // 3. one thread scores whole keys, for every query of the job
 #pragma unroll 1
-    for (int gA = warp; gA < kScanKeys / 16; gA += 2 * kScanWarps) {
-        scan::KeyLoad k[4];
-        int64_t cc[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int grp = gA + kScanWarps * (i >> 1);
-            cc[i] = base + grp * 16 + g + 8 * (i & 1);
-            if (direct) {
-                const int ti = grp >> 2;  // 4 groups of 16 keys per 64-key tile
-                k[i] = scan::key_from_tile(S.tiles[ti], (grp & 3) * 16 + g + 8 * (i & 1), t);
-                k[i].ok = have_tiles && S.tile_ok[ti] && cc[i] < n_cand;
-                if (!k[i].ok) k[i].w[0] = k[i].w[1] = k[i].w[2] = k[i].w[3] = k[i].sc = 0u;
-            } else {
-                int64_t pos = -1;
-                if (cc[i] < n_cand) pos = (int64_t)__ldg(pool + cc[i]);
-                if (pos >= L) pos = -1;
-                k[i] = scan::key_from_global(job.keys, b, pos, t, flags);
+    for (int i = tid; i < kScanKeys; i += kScanWarps * 32) {
+        const int64_t cc = base + i;
+        bool ok = cc < n_cand;
+        uint4 c0v = make_uint4(0u, 0u, 0u, 0u), c1v = c0v;
+        uint32_t scw = 0u;
+        if (ok && direct) {
+            const int ti = i / kIdxTile, rr = i % kIdxTile;
+            ok = have_tiles && S.tile_ok[ti];
+            c0v = *reinterpret_cast<const uint4 *>(S.tiles[ti] + rr * 32);
+            c1v = *reinterpret_cast<const uint4 *>(S.tiles[ti] + rr * 32 + 16);
+            scw = *reinterpret_cast<const uint32_t *>(S.tiles[ti] + kIdxTile * 32 + rr * 4);
+        } else if (ok) {
+            const int64_t pos = (int64_t)__ldcg(pool + cc);
+            ok = pos >= 0 && pos < L;
+            if (ok) {
+                const int64_t slotk = slot_of(job.keys, b, pos);
+                if (slotk < 0) {
+                    raise_flag(flags, kFlagBounds);
+                    ok = false;
+                } else {
+                    const uint8_t *tile = job.keys.data + (slotk / kIdxTile) * kIdxTileBytes;
+                    const int rr = (int)(slotk % kIdxTile);
+                    c0v = __ldcg(reinterpret_cast<const uint4 *>(tile + rr * 32));
+                    c1v = __ldcg(reinterpret_cast<const uint4 *>(tile + rr * 32 + 16));
+                    scw = __ldcg(reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4));
+                }
             }
         }
-        float sc[4];
-        scan::score4(k, bfrag, S.sk_lut, w0, w1, w2, w3, t, sc);
-        if (scoring) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (cc[i] >= n_cand) continue;
-                const uint32_t key = k[i].ok ? score_key(sc[i]) : 0u;
-                key_out[cc[i]] = key;
-                if (k[i].ok) {
-                    atomicAdd(&S.hist[my_q][key >> (32 - kHistBits)], 1u);
-                    if (score_out) score_out[cc[i]] = sc[i];
+        uint32_t kw[16];
+        float sk[4];
+        scan::unpack_key(c0v, c1v, scw, S.sk_lut, kw, sk);
+        for (int q = 0; q < job.n_q; ++q) {
+            const float sc = scan::score_key_int(kw, sk, S.qs, q);
+            const uint32_t key = ok ? score_key(sc) : 0u;
+            if (cc < n_cand) {
+                bufs.keys[((int64_t)job.row[q] * batch + b) * bufs.cand_cap + cc] = key;
+                if (ok) {
+                    atomicAdd(&S.hist[q][key >> (32 - kHistBits)], 1u);
+                    float *so = sb.out_scores[blockIdx.z][q];
+                    if (so) so[(int64_t)b * sb.scores_stride + cc] = sc;
                 }
             }
         }

@@ -20,6 +20,11 @@ inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t s)
 // Kernels enqueued by this library since load (process-wide, relaxed).
 void count_launches(int n);
 
+// When the environment variable CSA2_LOG is set (non-empty, not "0"), writes
+// the message to stderr, each distinct message once (launch plans: cluster
+// sizes, co-resident grids, fallbacks).
+void log_plan(const char *fmt, ...);
+
 // Sets the calling thread's csa2_last_error() message; returns `s`.
 csa2_status set_error(csa2_status s, const char *fmt, ...);
 
@@ -154,12 +159,15 @@ struct AttnPlan {
     const int32_t *seq_lens;
     int max_group;         // layers that may share one gather (1 or 2)
     int pdl;               // 1: the launch may overlap the stream's previous kernel
+    void *workspace;       // optional: lets a (group, sequence) split over several clusters
+    size_t workspace_bytes;
 };
 
-// Attention needs no workspace: every (layer group, sequence) is one cluster
-// whose CTAs merge their partials through distributed shared memory.
-size_t attn_workspace_bytes(const AttnEntry *entries, int n_entries, int batch, int topk, int window,
-                            size_t budget = SIZE_MAX);
+// Workspace of the fastest launch shape whose workspace is at most `budget`
+// (0: every (layer group, sequence) is one cluster, merged in distributed
+// shared memory).  Part of it is a ticket region that must be zero at the
+// first call and is left zero.
+size_t attn_workspace_bytes(const AttnPlan &plan, size_t budget = SIZE_MAX);
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream,
                              cudaEvent_t mid_event);
 

@@ -7,29 +7,16 @@
 //   t_hj = sq_hj * sk_j * P_hj (the E2M1 block dot product, exact);
 //   s_h = ((t_h0 + t_h1) + t_h2) + t_h3 in fp32;  r_h = max(s_h, +0);
 //   score = fma(w3, r3, fma(w2, r2, fma(w1, r1, w0 * r0))); 0 -> +0.
-// A warp scores 16 keys per MMA group: the block dot products of up to two
-// queries x 4 heads (the 8 columns of an m16n8k16 fp16 MMA) are exact --
-// E2M1 codes and the block-scaled query (scale x code, <= 6 significant
-// bits) are exact in fp16 and every partial sum is a small multiple of the
-// block's quantum -- and the epilogue applies the key scales and head weights
-// in the fixed order on the CUDA cores.
+// One thread scores a whole key for every query of its scan: the E2M1 codes
+// doubled are small integers, so the block dot products are exact integer
+// sums (dp4a), and the epilogue applies the scales and head weights in the
+// fixed order on the CUDA cores.
 #pragma once
 
 #include "common.cuh"
 
 namespace csa2 {
 namespace scan {
-
-__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};\n"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f),
-          "f"(0.0f));
-}
 
 // E2M1 value of a 4-bit code (sign bit 3).
 __device__ __forceinline__ float e2m1_value(uint32_t code)
@@ -39,57 +26,25 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
     return (code & 8u) ? -mag : mag;
 }
 
-// Codes (the 4 words this thread needs) and the 4 block scales of one key.
-struct KeyLoad {
-    uint32_t w[4];
-    uint32_t sc;
-    bool ok;
+// ---- integer scoring: one thread scores whole keys ------------------------------
+// Every E2M1 code doubled is an integer in [-12, 12], so each 16-channel block
+// product P_hb = sum (2 e_q)(2 e_k) is an exact int32 from four dp4a steps;
+// t_hb = (sq_hb * sk_b) * P_hb * 0.25 is exact in fp32 (at most 20
+// significant bits), and the epilogue adds and weighs in the stated order.
+
+// The queries of one scan in shared memory: doubled codes as int8 x 4
+// (channels 4w..4w+3 in word w of a head), block scales, head weights.
+struct QuerySet {
+    uint32_t qi8[2][kIdxHeads][kIdxDim / 4];
+    float sq[2][kIdxHeads][kIdxDim / 16];
+    float w[2][kIdxHeads];
 };
 
-// thread t of a quad uses bytes 8j+2t, 8j+2t+1 of block j: word 2j + t/2, half t%2
-__device__ __forceinline__ KeyLoad key_from_tile(const uint8_t *tile, int rr, int t)
+// 256 threads: thread = (query, head, block, pair of channels).
+__device__ __forceinline__ void prep_query_set(int tid, int n_q, const float *const q_idx[2], const float *const w[2],
+                                               int b, QuerySet &Q)
 {
-    KeyLoad k;
-    const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) k.w[j] = codes[2 * j + (t >> 1)];
-    k.sc = *reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4);
-    k.ok = true;
-    return k;
-}
-
-__device__ __forceinline__ KeyLoad key_from_global(const CacheView &keys, int b, int64_t pos, int t, int *flags)
-{
-    KeyLoad k;
-    k.ok = false;
-    k.sc = 0;
-    k.w[0] = k.w[1] = k.w[2] = k.w[3] = 0;
-    if (pos < 0) return k;
-    const int64_t slot = slot_of(keys, b, pos);
-    if (slot < 0) {
-        raise_flag(flags, kFlagBounds);
-        return k;
-    }
-    const uint8_t *tile = keys.data + (slot / kIdxTile) * kIdxTileBytes;
-    const int rr = (int)(slot % kIdxTile);
-    const uint32_t *codes = reinterpret_cast<const uint32_t *>(tile + rr * 32);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) k.w[j] = __ldcg(codes + 2 * j + (t >> 1));
-    k.sc = __ldcg(reinterpret_cast<const uint32_t *>(tile + kIdxTile * 32 + rr * 4));
-    k.ok = true;
-    return k;
-}
-
-
-// Query preparation by 256 threads (8 per 16-channel block of 2 queries x 4
-// heads): the FP4 rule's block scale and codes, pre-scaled (scale x E2M1
-// value, exact in fp16) into qpre[query][head][channel], and the head
-// weights into wq[query][head].  Queries qi >= n_q get zeros.
-__device__ __forceinline__ void prep_queries(int tid, int n_q, const float *const q_idx[2], const float *const w[2],
-                                             int b, __half (*qpre)[kIdxHeads][kIdxDim], float (*wq)[kIdxHeads])
-{
-    const int bi = tid >> 3, pr = tid & 7;
-    const int qi = bi >> 4, h = (bi >> 2) & 3, blk = bi & 3;
+    const int qi = tid >> 7, h = (tid >> 5) & 3, blk = (tid >> 3) & 3, pr = tid & 7;
     const bool have = qi < n_q;
     float v0 = 0.0f, v1 = 0.0f;
     if (have) {
@@ -102,64 +57,61 @@ __device__ __forceinline__ void prep_queries(int tid, int n_q, const float *cons
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
     const float sq = have ? e4m3_value(e4m3_code(__fdiv_rn(amax, 6.0f))) : 0.0f;
-    const float e0 = (sq != 0.0f) ? e2m1_value(e2m1_code(__fdiv_rn(v0, sq))) : 0.0f;
-    const float e1 = (sq != 0.0f) ? e2m1_value(e2m1_code(__fdiv_rn(v1, sq))) : 0.0f;
-    qpre[qi][h][blk * 16 + 2 * pr] = __float2half_rn(e0 * sq);
-    qpre[qi][h][blk * 16 + 2 * pr + 1] = __float2half_rn(e1 * sq);
-    if (blk == 0 && pr == 0) wq[qi][h] = have ? __ldcg(w[qi] + (int64_t)b * kIdxHeads + h) : 0.0f;
+    const int d0 = (sq != 0.0f) ? (int)(2.0f * e2m1_value(e2m1_code(__fdiv_rn(v0, sq)))) : 0;
+    const int d1 = (sq != 0.0f) ? (int)(2.0f * e2m1_value(e2m1_code(__fdiv_rn(v1, sq)))) : 0;
+    // two channels per thread; the even thread of a pair assembles the word
+    const uint32_t half = ((uint32_t)(d0 & 0xFF)) | ((uint32_t)(d1 & 0xFF) << 8);
+    const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, half, 1);
+    if ((pr & 1) == 0) Q.qi8[qi][h][blk * 4 + (pr >> 1)] = half | (other << 16);
+    if (pr == 0) Q.sq[qi][h][blk] = sq;
+    if (blk == 0 && pr == 0) Q.w[qi][h] = have ? __ldcg(w[qi] + (int64_t)b * kIdxHeads + h) : 0.0f;
 }
 
-// B fragments of the m16n8k16 MMA for block j: column g = (query g/4, head
-// g%4); k-slot 2t+e <-> channel 4t+e, k-slot 2t+8+e <-> channel 4t+2+e (a
-// permutation of the block applied to both operands).
-__device__ __forceinline__ void build_bfrag(const __half (*qpre)[kIdxHeads][kIdxDim], int g, int t,
-                                            uint32_t bfrag[4][2])
+// Eight doubled E2M1 codes (one 32-bit word of nibbles) -> two int8 x 4 words.
+__device__ __forceinline__ void e2m1_word_to_i8(uint32_t wd, uint32_t &lo4, uint32_t &hi4)
 {
-    const int qi = g >> 2, h = g & 3;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half *q = &qpre[qi][h][j * 16 + 4 * t];
-        bfrag[j][0] = (uint32_t)__half_as_ushort(q[0]) | ((uint32_t)__half_as_ushort(q[1]) << 16);
-        bfrag[j][1] = (uint32_t)__half_as_ushort(q[2]) | ((uint32_t)__half_as_ushort(q[3]) << 16);
-    }
+    // magnitudes {0,1,2,3,4,6,8,12} of the 3-bit codes, picked byte by byte
+    constexpr uint32_t kLo = 0x03020100u, kHi = 0x0C080604u;
+    const uint32_t m0 = __byte_perm(kLo, kHi, wd & 0x7777u);
+    const uint32_t m1 = __byte_perm(kLo, kHi, (wd >> 16) & 0x7777u);
+    // 0xFF for every negative code, then -m = (m ^ 0xFF) - 0xFF per byte
+    const uint32_t s0 = __byte_perm(0x0000FF00u, 0u, (wd >> 3) & 0x1111u);
+    const uint32_t s1 = __byte_perm(0x0000FF00u, 0u, (wd >> 19) & 0x1111u);
+    lo4 = __vsub4(m0 ^ s0, s0);
+    hi4 = __vsub4(m1 ^ s1, s1);
 }
 
-// Scores of four keys (two 16-key groups: k[0], k[1] in group A rows g and
-// g+8, k[2], k[3] in group B) for this thread's query (t >> 1); every thread
-// of the quad gets the same four scores for its query.
-__device__ __forceinline__ void score4(const KeyLoad k[4], const uint32_t bfrag[4][2], const float *sk_lut,
-                                       float w0, float w1, float w2, float w3, int t, float sc[4])
+// Score of one key (eight code words, four scale bytes) for query qi.
+__device__ __forceinline__ float score_key_int(const uint32_t (&kw)[16], const float (&sk)[4], const QuerySet &Q,
+                                               int qi)
 {
-    float d[2][4][4];
+    float score = 0.0f;
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2)
+    for (int h = 0; h < kIdxHeads; ++h) {
+        float s = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t uA = (k[2 * h2].w[j] >> (16 * (t & 1))) & 0xFFFFu;
-            const uint32_t uB = (k[2 * h2 + 1].w[j] >> (16 * (t & 1))) & 0xFFFFu;
-            mma16816(d[h2][j], e2m1x2_half2_bits(uA & 0xFFu), e2m1x2_half2_bits(uB & 0xFFu),
-                     e2m1x2_half2_bits(uA >> 8), e2m1x2_half2_bits(uB >> 8), bfrag[j][0], bfrag[j][1]);
+        for (int blk = 0; blk < 4; ++blk) {
+            int P = 0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) P = __dp4a((int)kw[4 * blk + w], (int)Q.qi8[qi][h][4 * blk + w], P);
+            const float t = __fmul_rn(__fmul_rn(__fmul_rn(Q.sq[qi][h][blk], sk[blk]), (float)P), 0.25f);
+            s = blk == 0 ? t : __fadd_rn(s, t);
         }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        // s = t0 + t1 + t2 + t3 in order; t_j = sk_j * (sq_j * P_j) is exact, so fma == add
-        const float *dd = &d[i >> 1][0][0];
-        const int e0 = 2 * (i & 1);  // accumulator pair of this key
-        float s0 = sk_lut[k[i].sc & 0xFFu] * dd[e0];
-        float s1 = sk_lut[k[i].sc & 0xFFu] * dd[e0 + 1];
-#pragma unroll
-        for (int j = 1; j < 4; ++j) {
-            const float skj = sk_lut[(k[i].sc >> (8 * j)) & 0xFFu];
-            s0 = __fmaf_rn(skj, dd[4 * j + e0], s0);
-            s1 = __fmaf_rn(skj, dd[4 * j + e0 + 1], s1);
-        }
-        const float r0 = s0 > 0.0f ? s0 : 0.0f, r1 = s1 > 0.0f ? s1 : 0.0f;
-        // heads 0,1 live on even t, heads 2,3 on odd t: chain w0*r0 -> +w1 r1 -> +w2 r2 -> +w3 r3
-        float acc = __fmaf_rn(w1, r1, __fmul_rn(w0, r0));
-        acc = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-        const float v = __fmaf_rn(w3, r1, __fmaf_rn(w2, r0, acc));
-        sc[i] = (v == 0.0f) ? 0.0f : v;
+        const float r = s > 0.0f ? s : 0.0f;
+        score = h == 0 ? __fmul_rn(Q.w[qi][0], r) : __fmaf_rn(Q.w[qi][h], r, score);
     }
+    return score == 0.0f ? 0.0f : score;
+}
+
+// The 64 channels of a key as int8 x 4 words, and its four block scales.
+__device__ __forceinline__ void unpack_key(const uint4 c0, const uint4 c1, uint32_t scales, const float *sk_lut,
+                                           uint32_t (&kw)[16], float (&sk)[4])
+{
+    const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) e2m1_word_to_i8(wd[j], kw[2 * j], kw[2 * j + 1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sk[j] = sk_lut[(scales >> (8 * j)) & 0xFFu];
 }
 
 }  // namespace scan

@@ -77,6 +77,16 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work between the arrival and the wait.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+// An arrival that orders nothing: marks this CTA as running, so that a later
+// cluster_wait() tells every CTA that all its peers have started.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+
 // Shared::cluster address of the object at local shared address `saddr` in CTA `rank`.
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank)
 {
@@ -101,6 +111,12 @@ __device__ __forceinline__ float2 ld_cluster_f2(uint32_t caddr)
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
     return v;
+}
+
+// Stores to another CTA's shared memory (visible there after a cluster barrier).
+__device__ __forceinline__ void st_cluster_f2(uint32_t caddr, float x, float y)
+{
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};\n" ::"r"(caddr), "f"(x), "f"(y) : "memory");
 }
 
 // ---- programmatic dependent launch -----------------------------------------

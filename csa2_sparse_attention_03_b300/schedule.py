@@ -170,7 +170,7 @@ class DecodeStep:
                 self.q[l] = torch.from_numpy(synth.query(self.w, l)).to(dev)
             else:
                 self.q[l] = synth.device_normal_(torch.empty((B, 16, 512), device=dev), self.w.seed, "q", l,
-                                                 scale=1.0 / np.sqrt(512))
+                                                 scale=synth.query_scale(self.w))
             self.out[l] = torch.zeros((B, 16, 512), dtype=torch.float32, device=dev)
             self.lse[l] = torch.zeros((B, 16), dtype=torch.float32, device=dev)
             if ly.mode in (synth.FULL, synth.REINDEX):

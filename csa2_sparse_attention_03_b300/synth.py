@@ -27,7 +27,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-CHUNK_ROWS = 65536
+CHUNK_ROWS = 4096  # small enough that a short slice (a window, one row) is cheap to draw
 
 # widths fixed by the workloads
 H_Q = 16          # attention heads (MQA over one shared 512-channel row)
@@ -185,10 +185,16 @@ def idx_key_values(w: Workload, full_layer: int, b: int, row0: int, n: int) -> n
     return normal_rows(w.seed, "idxk", (full_layer, b), row0, n, D_IDX)
 
 
+def query_scale(w: Workload) -> float:
+    """Standard deviation of the attention queries: 1/sqrt(512), times the
+    workload's optional ``extra["q_scale"]`` (logits spanning tens of units)."""
+    return float(w.extra.get("q_scale", 1.0)) / float(np.sqrt(D))
+
+
 def query(w: Workload, layer: int) -> np.ndarray:
     """[B, 16, 512] attention query of one layer."""
     return normal_rows(w.seed, "q", (layer,), 0, w.batch * H_Q, D,
-                       scale=1.0 / np.sqrt(D)).reshape(w.batch, H_Q, D)
+                       scale=query_scale(w)).reshape(w.batch, H_Q, D)
 
 
 def index_query(w: Workload, layer: int) -> np.ndarray:

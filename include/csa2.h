@@ -20,8 +20,10 @@
  *
  * Conventions
  *  - Every data pointer is a DEVICE pointer owned by the caller unless stated.
- *    The library allocates nothing: scratch comes from a caller workspace of
- *    the size the matching *_workspace() function returns (256-B aligned).
+ *    The library calls no allocator: scratch comes from a caller workspace of
+ *    the size the matching *_workspace() function returns (256-B aligned),
+ *    except for csa2_sparse_attn_noalloc, which uses a fixed 1 MiB device
+ *    array the library declares statically (see there).
  *    A workspace must be zero-filled before its first use (cudaMemset once
  *    after allocating it): part of it holds barrier counters and histograms
  *    that every call leaves zero again.  After a call whose device check
@@ -180,9 +182,18 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
  * 2^-22; softmax and every accumulation are fp32; the softmax weights enter
  * the PV product as fp16 (at most e^2 each, times the window row's fp32
  * scale x 2^8 -- window rows with |x| above ~15,000 would overflow it).
- * Workspace: none (csa2_sparse_attn_workspace() returns 0; `workspace` may
- * be NULL): each (sequence) is one thread-block cluster whose CTAs merge
- * their partial softmax results through distributed shared memory. */
+ * Launch shape and workspace: each sequence is one thread-block cluster
+ * (up to 16 CTAs, a tile of 128 rows each, merged through distributed
+ * shared memory), or several clusters when that is faster; split clusters
+ * each write a partial (running max, sum, normalised output) to the
+ * workspace and the last one to finish merges them.  The plan is the
+ * fastest whose scratch fits `workspace_bytes`; csa2_sparse_attn_workspace()
+ * is the most any plan of these sizes asks for.  `workspace` may be NULL
+ * (with any size): then every sequence is one cluster.  The split path's
+ * ticket counters must be zero before the first use (zero-fill the
+ * workspace once) and every call leaves them zero.  Results are identical
+ * for equal inputs and equal workspace sizes; a different split merges in a
+ * different order, which changes the rounding only. */
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window);
 csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                              int32_t batch, int32_t n_heads, int32_t head_dim,
@@ -197,11 +208,19 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
  * device), or a plugin living inside another runtime's allocator.  The paper
  * has no counterpart; this is a deployment convenience of this library.
  * Arguments, layouts, numerics and error codes are those of
- * csa2_sparse_attn minus the workspace.  The attention kernel keeps all of
- * its intermediate state in shared and tensor memory, so this call uses no
- * device memory beyond its inputs and outputs, holds no library-owned
- * array, and calls no allocator; calls on different streams do not
- * interfere. */
+ * csa2_sparse_attn minus the workspace; the result is bit-identical to
+ * csa2_sparse_attn given a 1 MiB workspace.  Scratch for split clusters
+ * comes from a 1 MiB array the library declares as a static __device__
+ * variable on each device (zero when the module loads; every call leaves
+ * its counters zero again), planned to fit it; no allocator is called.
+ * Its device address is looked up once per device with
+ * cudaGetSymbolAddress (thread-safe); make the first call on each device
+ * before capturing it in a CUDA graph, because the lookup may load the
+ * module.  All calls on a device share the array: calls that overlap in
+ * time (on different streams, or from several threads) race on it and give
+ * wrong results.  A sequence that needs more than the array holds runs as
+ * one cluster, which needs no scratch, so no size is rejected for want of
+ * scratch.  Returns CSA2_ERR_CUDA if the address lookup fails. */
 csa2_status csa2_sparse_attn_noalloc(const csa2_cache *kv, const csa2_cache *swa, const float *q,
                                      int32_t batch, int32_t n_heads, int32_t head_dim,
                                      const int32_t *seq_lens, int32_t max_seq_len,
@@ -270,6 +289,53 @@ csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, i
                               int32_t batch, const int32_t *seq_lens, int32_t max_seq_len,
                               int32_t topk, int32_t pool_len, int32_t swa_window,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---- planning (host only, no GPU work) ---------------------------------- */
+/* Footprint of one session for a schedule `modes` (CSA2_MODE_* per layer) at
+ * a context of `context` tokens: [HC] launch post ("890 bytes go a long
+ * way") and [LB] "Share the cache and the search work" quote the global KV
+ * per token (890 B) and per million tokens (0.89 GB); the pages give neither
+ * widths nor the token compression, so these are this library's layouts'
+ * figures, not a reproduction of 890 B.
+ *   global_bytes_per_token  (288 + 36) B per Full layer (main KV + indexer key)
+ *   cache_bytes             the Full layers' caches (context rounded up to 64
+ *                           tokens) + every layer's FP8 window ring (window
+ *                           rounded up to 4 slots, 516 B each)
+ *   step_bytes              per-step buffers: q, out, lse per layer, indices
+ *                           per indexing layer, pools per Full layer
+ *   sessions                floor(hbm_bytes / (cache_bytes + step_bytes)) */
+typedef struct csa2_footprint {
+    int64_t global_bytes_per_token;
+    int64_t cache_bytes;
+    int64_t step_bytes;
+    int64_t sessions;
+} csa2_footprint;
+csa2_status csa2_plan_footprint(const int32_t *modes, int32_t n_layers, int64_t context, int32_t topk,
+                                int32_t pool_len, int32_t window, int64_t hbm_bytes, csa2_footprint *out);
+
+/* Compute and traffic of one decode token through the schedule at a context
+ * of `context` tokens, [HC] "07 · compute, memory, bill" (decode work weighted
+ * BF16 = 1, FP8 = 0.5, FP4 = 0.25, followed from 4K to 1M), restricted to this
+ * path.  Reindex layers score the pool when pool_len > 0.
+ *   index_flops       2 x 4 heads x 64 per position scored (Full, Reindex)
+ *   attn_flops        4 x 16 heads x 512 per attended row (QK^T + PV):
+ *                     min(topk, context) selected rows (not SWA-only layers)
+ *                     + min(window, context) window rows, every layer
+ *   weighted_flops    index x 0.25 (FP4 keys and query) + selected-row
+ *                     attention x 0.25 (FP4 rows) + window attention x 0.5
+ *                     (FP8 rows)
+ *   bytes_sequential  algorithmic bytes in the layer-sequential order: 36 B
+ *                     per position scored (40 B per pool entry), 288 B per
+ *                     selected row, 516 B per window row, q/out/lse, indexer
+ *                     inputs, indices written and read, appended rows */
+typedef struct csa2_cost {
+    double index_flops;
+    double attn_flops;
+    double weighted_flops;
+    double bytes_sequential;
+} csa2_cost;
+csa2_status csa2_plan_cost(const int32_t *modes, int32_t n_layers, int64_t context, int32_t topk,
+                           int32_t pool_len, int32_t window, csa2_cost *out);
 
 /* ---- diagnostics ------------------------------------------------------ */
 /* Message for the last failure on the calling thread ("" if none). */

@@ -30,6 +30,7 @@ def read_golden(name):
 def orc():
     import oracle
     oracle.build()
+    oracle.set_threads(os.cpu_count() or 1)  # results do not depend on the thread count
     return oracle
 
 

@@ -45,3 +45,39 @@ def oracle_inputs(orc, w: synth.Workload, layers_needed=None):
 def oracle_step(orc, w: synth.Workload):
     caches, per = oracle_inputs(orc, w)
     return orc.decode_step(w.layers, list(w.seq_lens), w.topk, w.pool_len, caches, per), caches, per
+
+
+def oracle_inputs_seq(orc, w: synth.Workload, b: int, chunk=synth.CHUNK_ROWS):
+    """caches[f][0] and per_layer[l] of sequence b alone (a batch of one), from
+    the same streams the GPU path draws sequence b from; the main KV is
+    quantised chunk by chunk so long contexts stay within memory."""
+    L = int(w.seq_lens[b])
+    caches, per = {}, {}
+    for f, ly in enumerate(w.layers):
+        if ly.mode != synth.FULL:
+            continue
+        kc = np.empty((L, 256), np.uint8)
+        ks = np.empty((L, 32), np.uint8)
+        for r0 in range(0, L, chunk):
+            n = min(chunk, L - r0)
+            kc[r0:r0 + n], ks[r0:r0 + n] = orc.quant_fp4(synth.kv_values(w, f, b, r0, n))
+        ic = np.empty((L, 32), np.uint8)
+        isc = np.empty((L, 4), np.uint8)
+        for r0 in range(0, L, chunk):
+            n = min(chunk, L - r0)
+            ic[r0:r0 + n], isc[r0:r0 + n] = orc.quant_fp4(synth.idx_key_values(w, f, b, r0, n))
+        caches[f] = {0: dict(kv_codes=kc, kv_scales=ks, k_codes=ic, k_scales=isc)}
+    for l, ly in enumerate(w.layers):
+        n = min(w.window, L)
+        c, s = orc.quant_fp8(synth.swa_values(w, l, b)[w.window - n:])
+        pl = dict(q=synth.query(w, l)[b:b + 1], swa_codes=[c], swa_scales=[s], q_idx=None, w=None)
+        if ly.mode in (synth.FULL, synth.REINDEX):
+            pl["q_idx"] = synth.index_query(w, l)[b:b + 1]
+            pl["w"] = synth.index_weights(w, l)[b:b + 1]
+        per[l] = pl
+    return caches, per
+
+
+def oracle_step_seq(orc, w: synth.Workload, b: int):
+    caches, per = oracle_inputs_seq(orc, w, b)
+    return orc.decode_step(w.layers, [int(w.seq_lens[b])], w.topk, w.pool_len, caches, per)
