@@ -59,11 +59,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTileBytes = kRows * kDim * 2;     // 131,072: one tile, fp16
 constexpr int kQBytes = 32 * kDim * 2;           // 32,768 per layer: 16 heads x (value, remainder)
 constexpr int kPBytes = kRows * 16 * 2;          // 4,096 per layer
-constexpr int kQStage = kDim * 4 + 16;           // 2,064 B per fp32 query row staged in the idle tile buffer
-static_assert(kMaxNL * 16 * kQStage <= kTileBytes, "query staging fits the tile buffer");
 
 constexpr int kSAcc = 1;                         // QK^T accumulators (partial sums over the channels)
-constexpr int kChunks = 4;                       // channel chunks of a tile: dequantised and multiplied in turn
+constexpr int kChunks = 4;                       // channel chunks of a row (the layout of a thread's gathered bytes)
 
 template <int NL>
 struct Cols {
@@ -95,14 +93,18 @@ struct AttnParams {
     EntryDev entries[kMaxAttnEntries];
     int32_t n_units, batch, topk, window, win_tiles, cs;
     int32_t split;           // clusters per (unit, sequence); > 1 merges through `parts`
+    int32_t inputs_ready;    // indices, caches, rings and lengths predate the previous kernel
     const int32_t *seq_lens;
     float *parts;            // split > 1: [unit][b][part][kPartFloats]
-    uint32_t *tickets;       // split > 1: [unit][b], zero at launch, left zero
+    uint32_t *tickets;       // split > 1: [unit][b][kMaxCS], zero at launch, left zero
 };
 
-// One cluster's merged result in the workspace: (max, sum) per query, then the
-// output normalised by that sum, [query][channel].
-constexpr int kPartFloats = 2 * 16 * kMaxNL + 16 * kMaxNL * kDim;
+// One cluster's merged result in the workspace: per CTA rank a copy of the
+// cluster's (max, sum) per query (each CTA writes its own, so that CTAs need
+// not wait for one another), then the output normalised by that sum,
+// [query][channel] (CTA r writes its slice of the channels).
+constexpr int kHdrFloats = kMaxCS * 2 * 16 * kMaxNL;
+constexpr int kPartFloats = kHdrFloats + 16 * kMaxNL * kDim;
 
 struct Misc {
     uint32_t vmask[4];               // valid rows of the tile in the buffer
@@ -113,13 +115,13 @@ struct Misc {
     float2 mlall[kMaxCS][16 * kMaxNL];  // merge: every CTA's (m, l) per query, pushed by that CTA
     float wall[kMaxCS][16 * kMaxNL];    // merge: every CTA's (or part's) weight per query
     float cm[16 * kMaxNL], cl[16 * kMaxNL];  // merge: the cluster's (max, sum) per query
+    float inv_l[16 * kMaxNL];        // merge: 1 / this CTA's sum per query (0 without rows)
     int32_t last;                    // split: this cluster merges the parts
     float mu[16 * kMaxNL];           // the maximum a tile's weights are taken against
     float alpha[16 * kMaxNL];        // factor moving O^T to that maximum
     __align__(16) uint8_t app[kMaxNL][kDim];  // appended window row per layer slot (E4M3 codes)
     float app_scale[kMaxNL];
-    uint64_t bar_qk, bar_pv, bar_q;
-    uint64_t bar_deq[kChunks];       // every thread has converted its part of channel chunk k
+    uint64_t bar_qk, bar_pv;
     uint32_t tmem_slot;
     int32_t ok;
     int32_t any_resc;
@@ -142,18 +144,15 @@ __host__ __device__ __forceinline__ uint32_t cm_off(uint32_t r, uint32_t c)
 
 __device__ __forceinline__ uint32_t pack_h2(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
 
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count)
-{
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
-}
-
 // Reduces v[0..N) over the 32 lanes of a warp by halving exchanges: after
-// the call v[0] holds the reduction of query qlane(lane) over all lanes,
-// where qlane = lane >> 1 (N = 16) or lane (N = 32).
+// the call v[0] holds the reduction of entry qlane(lane) = lane >> (5 -
+// log2 N) over all lanes (N = 8, 16 or 32).
 template <int N, bool MAX>
 __device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane)
 {
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 entries");
     auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+    constexpr int kStages = N == 8 ? 3 : (N == 16 ? 4 : 5);
 #pragma unroll
     for (int half = N / 2, bit = 4; half >= 1; half >>= 1, --bit) {
         const bool up = (lane >> bit) & 1;
@@ -164,7 +163,9 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane)
             v[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 1 << bit));
         }
     }
-    if (N == 16) v[0] = op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
+    // the lanes that share an entry hold partials over the rest of the lane bits
+#pragma unroll
+    for (int bit = 4 - kStages; bit >= 0; --bit) v[0] = op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1 << bit));
 }
 
 // Raw bytes of one thread's share of a row: row r, channels 128 k + 64 h ..
@@ -304,6 +305,28 @@ __device__ __forceinline__ void dequant_chunk(const Ctx &c, bool window, int r, 
     }
 }
 
+// Dequantises this thread's whole share of its row (every channel chunk).
+__device__ __forceinline__ void dequant(const Ctx &c, bool window, int r, int h, const Raw &raw, uint8_t *T)
+{
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) dequant_chunk(c, window, r, h, k, raw, T);
+}
+
+// Row r of a window tile from the appended codes of layer slot j (one warp,
+// 16 channels per lane), with its row factor.
+__device__ __forceinline__ void dequant_app_row(Misc &M, int j, int r, int lane, uint8_t *T)
+{
+    const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));  // 2^-8
+    const uint4 cw = *reinterpret_cast<const uint4 *>(&M.app[j][16 * lane]);
+    *reinterpret_cast<uint4 *>(T + cm_off(r, 16 * lane)) =
+        make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.x & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.x >> 16), k2m8)),
+                   pack_h2(__hmul2(e4m3x2_half2(cw.y & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.y >> 16), k2m8)));
+    *reinterpret_cast<uint4 *>(T + cm_off(r, 16 * lane + 8)) =
+        make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.z & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.z >> 16), k2m8)),
+                   pack_h2(__hmul2(e4m3x2_half2(cw.w & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.w >> 16), k2m8)));
+    if (lane == 0) M.rowfac[r] = M.app_scale[j] * 256.0f;
+}
+
 // Quantises a layer's appended window row into its ring slot at position
 // L-1 (FP8, scale = absmax / 448) and keeps the codes in shared memory for
 // this CTA's own window tile.  One warp; lane = 16 channels.
@@ -343,48 +366,43 @@ __device__ __forceinline__ void append_window_row(const Ctx &c, const EntryDev &
     if (lane == 0) c.M->app_scale[j] = s;
 }
 
-// Softmax of one tile (warps 0-3, thread = row r = TMEM lane).  Writes P as
-// fp16 into the PV operand, updates the running (m, l) and rescales O^T in
-// tensor memory when a query's maximum moves.
+// Softmax of one tile, all eight warps: thread (row r = TMEM lane, query half
+// qh = warp / 4) takes half of the queries of its row.  Writes P as fp16 into
+// the PV operand, updates the running (m, l) and rescales O^T in tensor
+// memory when a query's maximum moves.
 template <int NL>
 __device__ __forceinline__ void softmax_tile(const Ctx &c, uint32_t tmem, uint8_t *Ps, int tile, bool first)
 {
-    constexpr int NQ = 16 * NL;
+    constexpr int NQ = 16 * NL, NH = NQ / 2;
     Misc &M = *c.M;
     const UnitDev &U = *c.U;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = tid;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp & 3, qh = warp >> 2;
+    const int r = tid & (kRows - 1);
     const bool window = tile_is_window(U, tile);
     const int owner = window ? (tile - U.row_tiles) / c.P->win_tiles : -1;
-    const int qlane = NQ == 16 ? (lane >> 1) : lane;
-    // S^T: per query the value and remainder columns (of each of the kSAcc
-    // partial sums over the channels, added in a fixed order)
-    float s[NQ], v[NQ];
+    const int ql = lane >> (NH == 8 ? 2 : 1);  // this lane's entry after a transpose reduction
+    // S^T: this half's value columns qh NH.. and remainder columns NQ + qh NH..
+    float s[NH], v[NH];
+    {
+        float hv[NH], lv[NH];
+        tc::tmem_ld<NH>(tc::taddr(tmem, 32u * quad, Cols<NL>::S + (uint32_t)(qh * NH)), hv);
+        tc::tmem_ld<NH>(tc::taddr(tmem, 32u * quad, Cols<NL>::S + (uint32_t)(NQ + qh * NH)), lv);
 #pragma unroll
-    for (int a = 0; a < kSAcc; ++a)
-#pragma unroll
-        for (int c0 = 0; c0 < 2 * NQ; c0 += 32) {
-            float t[32];
-            tc::tmem_ld32(tc::taddr(tmem, 32u * warp, Cols<NL>::S + (uint32_t)(a * 2 * NQ + c0)), t);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int col = c0 + i, q = col % NQ;
-                s[q] = (a == 0 && col < NQ) ? t[i] : s[q] + t[i];
-            }
-        }
+        for (int i = 0; i < NH; ++i) s[i] = hv[i] + lv[i];
+    }
     const bool valid = (M.vmask[r >> 5] >> (r & 31)) & 1u;
     const float fac = M.rowfac[r];
     // logits times the row factor
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        const int j = q >> 4;
+    for (int i = 0; i < NH; ++i) {
+        const int q = qh * NH + i, j = q >> 4;
         const bool own = window ? (j == owner) : (j < U.n_layers);
-        s[q] = (valid && own) ? fac * s[q] : -INFINITY;
-        v[q] = s[q];
+        s[i] = (valid && own) ? fac * s[i] : -INFINITY;
+        v[i] = s[i];
     }
-    warp_transpose_reduce<NQ, true>(v, lane);
-    M.red[warp][qlane] = v[0];
-    named_sync(1, 128);
+    warp_transpose_reduce<NH, true>(v, lane);
+    M.red[quad][qh * NH + ql] = v[0];
+    __syncthreads();
     // one thread per query: the tile maximum, the lazy move of the running maximum
     if (tid < NQ) {
         const int q = tid;
@@ -398,26 +416,26 @@ __device__ __forceinline__ void softmax_tile(const Ctx &c, uint32_t tmem, uint8_
         const uint32_t any = __ballot_sync(NQ == 32 ? 0xFFFFFFFFu : 0xFFFFu, resc && al != 0.0f);
         if (q == 0) M.any_resc = any != 0u;
     }
-    named_sync(1, 128);
+    __syncthreads();
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        s[q] = (s[q] == -INFINITY) ? 0.0f : tc::exp2_fast((s[q] - M.mu[q]) * kLog2e);
-        v[q] = s[q];
+    for (int i = 0; i < NH; ++i) {
+        s[i] = (s[i] == -INFINITY) ? 0.0f : tc::exp2_fast((s[i] - M.mu[qh * NH + i]) * kLog2e);
+        v[i] = s[i];
     }
     // P (weights times the row factor) as fp16: core matrices 8 rows x 8 queries,
     // query groups 128 B apart, row groups 256 NL B apart
     uint8_t *prow = Ps + (r >> 3) * (256 * NL) + (r & 7) * 16;
 #pragma unroll
-    for (int g = 0; g < NQ / 8; ++g) {
+    for (int g = 0; g < NH / 8; ++g) {
         uint32_t hv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             hv[i] = pack_h2(__floats2half2_rn(s[8 * g + 2 * i] * fac, s[8 * g + 2 * i + 1] * fac));
-        *reinterpret_cast<uint4 *>(prow + g * 128) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(prow + (qh * (NH / 8) + g) * 128) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
     }
-    warp_transpose_reduce<NQ, false>(v, lane);
-    M.red[warp][qlane] = v[0];  // the maxima in red[][] were read before the last barrier
-    named_sync(1, 128);
+    warp_transpose_reduce<NH, false>(v, lane);
+    M.red[quad][qh * NH + ql] = v[0];  // the maxima in red[][] were read before the last barrier
+    __syncthreads();
     if (tid < NQ) {
         const int q = tid;
         const float lt = (M.red[0][q] + M.red[1][q]) + (M.red[2][q] + M.red[3][q]);
@@ -425,18 +443,85 @@ __device__ __forceinline__ void softmax_tile(const Ctx &c, uint32_t tmem, uint8_
         M.m_run[q] = M.mu[q];
     }
     // O^T holds earlier tiles' PV: scale it where a query's maximum moved
+    // (thread: channel lane 32 quad + lane, columns of its half)
     if (!first && M.any_resc) {
         float o[32];
 #pragma unroll
-        for (int c0 = 0; c0 < 64 * NL; c0 += 32) {
-            tc::tmem_ld32(tc::taddr(tmem, 32u * warp, Cols<NL>::O + c0), o);
+        for (int c0 = qh * 32 * NL; c0 < (qh + 1) * 32 * NL; c0 += 32) {
+            tc::tmem_ld32(tc::taddr(tmem, 32u * quad, Cols<NL>::O + c0), o);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= M.alpha[(c0 + i) % NQ];
-            tc::tmem_st32(tc::taddr(tmem, 32u * warp, Cols<NL>::O + c0), o);
+            tc::tmem_st32(tc::taddr(tmem, 32u * quad, Cols<NL>::O + c0), o);
         }
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
+}
+
+// Weighted sums over `ns` sources for this thread's items of one channel
+// slice: item = (query q, four channels), n4 items per query.  For each item,
+// sum_s wgt[s][q] x load(s, q, ch) in source order.  With few sources, four
+// items go at once; otherwise one item with all its sources: every load of a
+// batch is in flight before the first is used.
+template <int NQ, typename Load, typename Store>
+__device__ __forceinline__ void slice_reduce(int ns, int n4, int c_lo, int n_layers, const float (*wgt)[16 * kMaxNL],
+                                             Load load, Store store)
+{
+    const int total = NQ * n4;
+    const int tid = threadIdx.x;
+    if (ns <= 4) {
+        for (int base = tid; base < total; base += 4 * kThreads) {
+            float4 v[4][4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                const int item = base + ii * kThreads;
+                const int q = item / max(n4, 1), ch = c_lo + 4 * (item - q * n4);
+                if (item < total && (q >> 4) < n_layers) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k < ns) v[ii][k] = load(k, q, ch);
+                }
+            }
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                const int item = base + ii * kThreads;
+                const int q = item / max(n4, 1), ch = c_lo + 4 * (item - q * n4);
+                if (item < total && (q >> 4) < n_layers) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k < ns) {
+                            const float w = wgt[k][q];
+                            acc.x += w * v[ii][k].x;
+                            acc.y += w * v[ii][k].y;
+                            acc.z += w * v[ii][k].z;
+                            acc.w += w * v[ii][k].w;
+                        }
+                    store(q, ch, acc);
+                }
+            }
+        }
+    } else {
+        for (int item = tid; item < total; item += kThreads) {
+            const int q = item / n4, ch = c_lo + 4 * (item % n4);
+            if ((q >> 4) >= n_layers) continue;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 v[kMaxCS];
+#pragma unroll
+            for (int k = 0; k < kMaxCS; ++k)
+                if (k < ns) v[k] = load(k, q, ch);
+#pragma unroll
+            for (int k = 0; k < kMaxCS; ++k)
+                if (k < ns) {
+                    const float w = wgt[k][q];
+                    acc.x += w * v[k].x;
+                    acc.y += w * v[k].y;
+                    acc.z += w * v[k].z;
+                    acc.w += w * v[k].w;
+                }
+            store(q, ch, acc);
+        }
+    }
 }
 
 template <int NL>
@@ -459,8 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (tid == 0) {
         tc::mbar_init(&M.bar_qk, 1);
         tc::mbar_init(&M.bar_pv, 1);
-        tc::mbar_init(&M.bar_q, 1);
-        for (int k = 0; k < kChunks; ++k) tc::mbar_init(&M.bar_deq[k], kThreads);
         tc::mbar_init_fence();
         M.ok = 1;
     }
@@ -474,8 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     tc::fence_after_sync();
     const uint32_t tmem = M.tmem_slot;
     tc::cluster_arrive_relaxed();  // waited for before the first access to a peer's shared memory
-    tc::pdl_wait();
-    tc::pdl_launch_dependents();
 
     Ctx c;
     c.P = &P;
@@ -483,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     c.M = &M;
     c.flags = flags;
     c.b = blockIdx.y;
-    c.L = max(0, __ldcg(P.seq_lens + c.b));
+    c.L = 0;
     c.W = P.window;
     // this cluster's tiles: a contiguous part of the unit's; this CTA's: every cs-th
     const int per_part = (U.n_tiles + P.split - 1) / P.split;
@@ -491,54 +572,88 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int n_my = t_end > t0 ? (t_end - 1 - t0) / cs + 1 : 0;
     const int r = tid & (kRows - 1), h = tid >> 7;
 
-    // the unit's queries go out first, as one bulk copy per (layer, head) into
-    // the idle tile buffer (fp32 rows kQStage apart, so the conversion below
-    // reads them without bank conflicts); the first tile's positions and rows,
-    // the next tile's positions and the appended window rows load meanwhile
-    if (warp == 0) {
-        if (lane == 0) tc::mbar_expect_tx(&M.bar_q, (uint32_t)(U.n_layers * kHeads * kDim * 4));
-        __syncwarp();
-        for (int i = lane; i < U.n_layers * kHeads; i += 32)
-            tc::bulk_g2s(T + i * kQStage, P.entries[U.entry[i >> 4]].q + ((int64_t)c.b * kHeads + (i & 15)) * kDim,
-                         kDim * 4, &M.bar_q);
-    }
     Raw raw;
     int32_t pos_next = -1;
-    if (n_my > 0) {
-        const int32_t pos0 = load_pos(c, t0, r);
+    auto first_gather = [&]() {
+        // the length and the positions are independent loads: both in flight at once
+        const int32_t Lraw = __ldcg(P.seq_lens + c.b);
+        const int32_t pos0 = n_my > 0 ? load_pos(c, t0, r) : -1;
         if (n_my > 1) pos_next = load_pos(c, t0 + cs, r);
-        gather(c, t0, pos0, r, h, raw);
+        c.L = max(0, Lraw);
+        if (n_my > 0) gather(c, t0, pos0, r, h, raw);
+    };
+    auto row_masks = [&](bool window) {
+        if (h == 0) {
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, raw.valid);
+            if (lane == 0) M.vmask[warp] = m;
+            M.rowfac[r] = window ? (raw.app >= 0 ? M.app_scale[raw.app] : raw.scale) * 256.0f : 1.0f;
+        }
+    };
+    // the queries' and appended window rows' lines into L2 while the previous kernel runs
+    for (int i = tid; i < U.n_layers * (kHeads * kDim * 4 / 128); i += kThreads) {
+        const int j = i / (kHeads * kDim * 4 / 128), line = i % (kHeads * kDim * 4 / 128);
+        tc::prefetch_l2(reinterpret_cast<const uint8_t *>(P.entries[U.entry[j]].q + (int64_t)c.b * kHeads * kDim) +
+                        128 * line);
     }
+    if (warp < U.n_layers && P.entries[U.entry[warp]].new_swa && lane < kDim * 4 / 128)
+        tc::prefetch_l2(reinterpret_cast<const uint8_t *>(P.entries[U.entry[warp]].new_swa + (int64_t)c.b * kDim) +
+                        128 * lane);
+    const bool pre = P.inputs_ready && n_my > 0;
+    if (pre) {
+        // nothing the previous kernel writes is read here: the first tile is
+        // gathered and dequantised while that kernel runs (an appended window
+        // row, written after the wait, is patched in below)
+        first_gather();
+        dequant(c, tile_is_window(U, t0), r, h, raw, T);
+        row_masks(tile_is_window(U, t0));
+        if (n_my > 1) {
+            gather(c, t0 + cs, pos_next, r, h, raw);
+            pos_next = n_my > 2 ? load_pos(c, t0 + 2 * cs, r) : -1;
+        }
+    }
+    tc::pdl_wait();
+    tc::pdl_launch_dependents();
+
+    // queries: every load in flight at once (before the first tile's dependent
+    // position and row loads), then the fp16 value and fp16 remainder into
+    // K-major core matrices (query rows n, 8,192 B per 8 rows; remainders at
+    // n + 16 NL)
+    float4 qv[4 * NL][2];
+#pragma unroll
+    for (int k = 0; k < 4 * NL; ++k) {
+        const int item = tid + kThreads * k;
+        const int qi = (item & 7) | ((item >> 9) << 3);
+        const int cg = (item >> 3) & 63;
+        if ((qi >> 4) < U.n_layers) {
+            const float4 *src = reinterpret_cast<const float4 *>(P.entries[U.entry[qi >> 4]].q +
+                                                                 ((int64_t)c.b * kHeads + (qi & 15)) * kDim + 8 * cg);
+            qv[k][0] = __ldcg(src);
+            qv[k][1] = __ldcg(src + 1);
+        } else {
+            qv[k][0] = qv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if (!pre) first_gather();
 
     // appended window rows of this CTA's window tiles (position L-1 of each layer)
     if (P.window > 0 && c.L > 0 && warp < U.n_layers) {
         const int j = warp;
         const EntryDev &E = P.entries[U.entry[j]];
         const int t_app = U.row_tiles + j * P.win_tiles + (P.window - 1) / kRows;
-        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0) append_window_row(c, E, j, lane);
+        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0) {
+            append_window_row(c, E, j, lane);
+            __syncwarp();
+            if (pre && t_app == t0) dequant_app_row(M, j, (P.window - 1) % kRows, lane, T);
+        }
     }
 
-    // queries to fp16 value and fp16 remainder, K-major core matrices (query
-    // rows n, 8,192 B per 8 rows; remainders at n + 16 NL)
-    if (!tc::mbar_wait(&M.bar_q, 0)) {
-        M.ok = 0;
-        tc::mbar_wait(&M.bar_q, 0);  // a last chance for the copies in flight
-    }
 #pragma unroll
     for (int k = 0; k < 4 * NL; ++k) {
         const int item = tid + kThreads * k;
         const int qi = (item & 7) | ((item >> 9) << 3);
         const int cg = (item >> 3) & 63;
-        float x[8];
-        if ((qi >> 4) < U.n_layers) {
-            const float4 *src = reinterpret_cast<const float4 *>(T + qi * kQStage + 32 * cg);
-            const float4 a = src[0], b = src[1];
-            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.0f;
-        }
+        const float x[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                            qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -557,47 +672,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     for (int it = 0; it < n_my; ++it) {
         const int tile = t0 + it * cs;
         const bool window = tile_is_window(U, tile);
-        if (it > 0 && tid == 0 && !tc::mbar_wait(&M.bar_pv, (it - 1) & 1)) M.ok = 0;  // tile and P buffers free
-        __syncthreads();
-        tc::fence_after_sync();
-        if (h == 0) {
-            const uint32_t m = __ballot_sync(0xFFFFFFFFu, raw.valid);
-            if (lane == 0) M.vmask[warp] = m;
-            M.rowfac[r] = window ? (raw.app >= 0 ? M.app_scale[raw.app] : raw.scale) * 256.0f : 1.0f;
-        }
-        // channel chunk by chunk: every thread converts its part of chunk k and
-        // arrives; thread 0 multiplies chunk k - 1 once all have arrived, so the
-        // tensor core works on one chunk while the threads convert the next
-        const uint64_t a0 = tc::sdesc(tc::smem_u32(T), 128, 8192);
-        const uint64_t b0 = tc::sdesc(tc::smem_u32(Qs), 128, 8192);
-        auto issue_chunk = [&](int k) {
-            if (!tc::mbar_wait(&M.bar_deq[k], it & 1)) M.ok = 0;
+        if (it > 0 || !pre) {
+            if (it > 0 && tid == 0 && !tc::mbar_wait(&M.bar_pv, (it - 1) & 1)) M.ok = 0;  // tile and P buffers free
+            __syncthreads();
             tc::fence_after_sync();
-#pragma unroll
-            for (int ks = 8 * k; ks < 8 * k + 8; ++ks)
-                tc::mma_f16(tmem + Cols<NL>::S, a0 + 16 * ks, b0 + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
-        };
-#pragma unroll
-        for (int k = 0; k < kChunks; ++k) {
-            dequant_chunk(c, window, r, h, k, raw, T);
-            tc::fence_async_smem();
-            tc::mbar_arrive(&M.bar_deq[k]);
-            if (tid == 0 && k > 0) issue_chunk(k - 1);
+            dequant(c, window, r, h, raw, T);
+            row_masks(window);
+            if (it + 1 < n_my) {  // in flight during this tile
+                gather(c, tile + cs, pos_next, r, h, raw);
+                pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * cs, r) : -1;
+            }
         }
+        tc::fence_async_smem();
+        __syncthreads();
         if (tid == 0) {
-            issue_chunk(kChunks - 1);
+            tc::fence_after_sync();
+            const uint64_t a0 = tc::sdesc(tc::smem_u32(T), 128, 8192);
+            const uint64_t b0 = tc::sdesc(tc::smem_u32(Qs), 128, 8192);
+#pragma unroll
+            for (int ks = 0; ks < kDim / 16; ++ks)
+                tc::mma_f16(tmem + Cols<NL>::S, a0 + 16 * ks, b0 + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
             tc::mma_commit(&M.bar_qk);
         }
-        if (it + 1 < n_my) {  // in flight during this tile
-            gather(c, tile + cs, pos_next, r, h, raw);
-            pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * cs, r) : -1;
-        }
-        __syncthreads();  // row masks and factors before the softmax
-        if (warp < 4) {
-            if (!tc::mbar_wait(&M.bar_qk, it & 1) && tid == 0) M.ok = 0;
-            tc::fence_after_sync();
-            softmax_tile<NL>(c, tmem, Ps, tile, it == 0);
-        }
+        if (!tc::mbar_wait(&M.bar_qk, it & 1) && tid == 0) M.ok = 0;
+        tc::fence_after_sync();
+        softmax_tile<NL>(c, tmem, Ps, tile, it == 0);
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
@@ -620,6 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0 && !M.ok) raise_flag(flags, kFlagTimeout);
+    if (tid < NQ) M.inv_l[tid] = M.l_run[tid] > 0.0f ? 1.0f / M.l_run[tid] : 0.0f;
+    __syncthreads();
 
     // ---- merge across the cluster: every CTA stages its output normalised by its
     // own sum, with its (max, sum); one cluster barrier; each CTA then weighs
@@ -647,8 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int col = c0 + i, cb = col / NQ, q = col % NQ;
-                const float l = M.l_run[q];
-                stage[q * kDim + 128 * cb + ch_in] = l > 0.0f ? o[i] / l : 0.0f;
+                stage[q * kDim + 128 * cb + ch_in] = o[i] * M.inv_l[q];
             }
         }
     }
@@ -658,18 +758,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Cols<NL>::alloc);
     }
-    if (tid < NQ) {
+    if (tid >= kThreads - NQ) {
         // the cluster's maximum and sum; each CTA's weight l_s exp(m_s - M) / L
-        const int q = tid;
+        // (every table entry loaded at once; sums in source order)
+        const int q = tid - (kThreads - NQ);
+        float2 ml[kMaxCS];
+#pragma unroll
+        for (int s = 0; s < kMaxCS; ++s) ml[s] = s < cs ? M.mlall[s][q] : make_float2(-INFINITY, 0.0f);
         float mx = -INFINITY;
-        for (int s = 0; s < cs; ++s)
-            if (M.mlall[s][q].y > 0.0f) mx = fmaxf(mx, M.mlall[s][q].x);
-        float lsum = 0.0f;
-        for (int s = 0; s < cs; ++s)
-            if (M.mlall[s][q].y > 0.0f) lsum += M.mlall[s][q].y * __expf(M.mlall[s][q].x - mx);
-        for (int s = 0; s < cs; ++s)
-            M.wall[s][q] = (lsum > 0.0f && M.mlall[s][q].y > 0.0f) ? M.mlall[s][q].y * __expf(M.mlall[s][q].x - mx) / lsum
-                                                                   : 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxCS; ++s)
+            if (ml[s].y > 0.0f) mx = fmaxf(mx, ml[s].x);
+        float e[kMaxCS], lsum = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxCS; ++s) {
+            e[s] = ml[s].y > 0.0f ? ml[s].y * __expf(ml[s].x - mx) : 0.0f;
+            lsum += e[s];
+        }
+        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxCS; ++s)
+            if (s < cs) M.wall[s][q] = e[s] * inv;
         M.cm[q] = mx;
         M.cl[q] = lsum;
     }
@@ -682,107 +791,83 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                           : nullptr;
     {
         const uint32_t st_addr = tc::smem_u32(stage);
-        for (int item = tid; item < NQ * n4; item += kThreads) {
-            const int q = item / n4, ch = c_lo + 4 * (item % n4);
-            const int j = q >> 4;
-            if (j >= U.n_layers) continue;
-            const uint32_t off = (uint32_t)(q * kDim + ch) * 4u;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            // eight remote loads in flight, then their weighted sum
-#pragma unroll
-            for (int s0 = 0; s0 < kMaxCS; s0 += 8) {
-                float4 v[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (s0 + k < cs) v[k] = tc::ld_cluster_f4(tc::mapa(st_addr + off, (uint32_t)(s0 + k)));
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (s0 + k < cs) {
-                        const float wgt = M.wall[s0 + k][q];
-                        acc.x += wgt * v[k].x;
-                        acc.y += wgt * v[k].y;
-                        acc.z += wgt * v[k].z;
-                        acc.w += wgt * v[k].w;
-                    }
-            }
-            float *dst = part_rec ? part_rec + 2 * 16 * kMaxNL + q * kDim + ch
-                                  : P.entries[U.entry[j]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch;
-            *reinterpret_cast<float4 *>(dst) = acc;
+        slice_reduce<NQ>(
+            cs, n4, c_lo, U.n_layers, M.wall,
+            [&](int src, int q, int ch) {
+                return tc::ld_cluster_f4(tc::mapa(st_addr + (uint32_t)(q * kDim + ch) * 4u, (uint32_t)src));
+            },
+            [&](int q, int ch, float4 acc) {
+                float *dst = part_rec ? part_rec + kHdrFloats + q * kDim + ch
+                                      : P.entries[U.entry[q >> 4]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch;
+                *reinterpret_cast<float4 *>(dst) = acc;
+            });
+        if (tid < NQ && part_rec) {
+            part_rec[rank * 32 * kMaxNL + tid] = M.cm[tid];
+            part_rec[rank * 32 * kMaxNL + 16 * kMaxNL + tid] = M.cl[tid];
         }
-        if (tid < NQ && rank == 0) {
+        if (tid < NQ && rank == 0 && !part_rec) {
             const int q = tid, j = q >> 4;
-            if (part_rec) {
-                part_rec[q] = M.cm[q];
-                part_rec[16 * kMaxNL + q] = M.cl[q];
-            } else if (j < U.n_layers && P.entries[U.entry[j]].lse) {
+            if (j < U.n_layers && P.entries[U.entry[j]].lse) {
                 P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] =
                     M.cl[q] > 0.0f ? M.cm[q] + logf(M.cl[q]) : -INFINITY;
             }
         }
     }
     if (P.split > 1) {
-        // the unit's clusters meet through a ticket: the last one to arrive sums the
-        // parts (each CTA its slice of the channels) and writes the output
-        __threadfence();
-        tc::fence_before_sync();
-        tc::cluster_sync();  // every part record of this cluster is written
-        if (rank == 0 && tid == 0) {
-            uint32_t *tk = P.tickets + (int64_t)unit * P.batch + c.b;
+        // the parts of each channel slice meet through a ticket per (unit,
+        // sequence, CTA rank): the CTA that arrives last for its slice sums
+        // the parts' slices and writes the output
+        __syncthreads();  // this CTA's slice and header copy are written
+        if (tid == 0) {
+            __threadfence();
+            uint32_t *tk = P.tickets + ((int64_t)unit * P.batch + c.b) * kMaxCS + rank;
             const uint32_t t = atomicAdd(tk, 1u);
             M.last = (t == (uint32_t)P.split - 1) ? 1 : 0;
-            if (M.last) atomicExch(tk, 0u);  // every cluster has arrived: leave it zero
-            __threadfence();
+            if (M.last) {
+                atomicExch(tk, 0u);  // every part has arrived: leave it zero
+                __threadfence();
+            }
         }
-        tc::fence_before_sync();
-        tc::cluster_sync();
-        int last = 0;
-        {
-            const uint32_t a = tc::mapa(tc::smem_u32(&M.last), 0u);
-            asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(last) : "r"(a) : "memory");
-        }
+        __syncthreads();
+        const int last = M.last;
         if (last) {
             __threadfence();
             const float *base = P.parts + ((int64_t)unit * P.batch + c.b) * P.split * (int64_t)kPartFloats;
+            // every part's (m, l) of every query, all loads at once
+            for (int i = tid; i < P.split * NQ; i += kThreads) {
+                const int p2 = i / NQ, q = i % NQ;
+                const float *rec = base + (int64_t)p2 * kPartFloats;
+                M.mlall[p2][q] = make_float2(__ldcg(rec + rank * 32 * kMaxNL + q), __ldcg(rec + rank * 32 * kMaxNL + 16 * kMaxNL + q));
+            }
+            __syncthreads();
             if (tid < NQ) {
                 const int q = tid;
                 float mx = -INFINITY;
-                for (int p2 = 0; p2 < P.split; ++p2) {
-                    const float *rec = base + (int64_t)p2 * kPartFloats;
-                    if (__ldcg(rec + 16 * kMaxNL + q) > 0.0f) mx = fmaxf(mx, __ldcg(rec + q));
-                }
+                for (int p2 = 0; p2 < P.split; ++p2)
+                    if (M.mlall[p2][q].y > 0.0f) mx = fmaxf(mx, M.mlall[p2][q].x);
                 float lsum = 0.0f;
+                for (int p2 = 0; p2 < P.split; ++p2)
+                    if (M.mlall[p2][q].y > 0.0f) lsum += M.mlall[p2][q].y * __expf(M.mlall[p2][q].x - mx);
+                const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
                 for (int p2 = 0; p2 < P.split; ++p2) {
-                    const float *rec = base + (int64_t)p2 * kPartFloats;
-                    const float lp = __ldcg(rec + 16 * kMaxNL + q);
-                    if (lp > 0.0f) lsum += lp * __expf(__ldcg(rec + q) - mx);
-                }
-                for (int p2 = 0; p2 < P.split && p2 < kMaxCS; ++p2) {
-                    const float *rec = base + (int64_t)p2 * kPartFloats;
-                    const float lp = __ldcg(rec + 16 * kMaxNL + q);
-                    M.wall[p2][q] = (lsum > 0.0f && lp > 0.0f) ? lp * __expf(__ldcg(rec + q) - mx) / lsum : 0.0f;
+                    const float2 ml = M.mlall[p2][q];
+                    M.wall[p2][q] = ml.y > 0.0f ? ml.y * __expf(ml.x - mx) * inv : 0.0f;
                 }
                 const int j = q >> 4;
                 if (rank == 0 && j < U.n_layers && P.entries[U.entry[j]].lse)
                     P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
             }
             __syncthreads();
-            for (int item = tid; item < NQ * n4; item += kThreads) {
-                const int q = item / n4, ch = c_lo + 4 * (item % n4);
-                const int j = q >> 4;
-                if (j >= U.n_layers) continue;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int p2 = 0; p2 < P.split && p2 < kMaxCS; ++p2) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (int64_t)p2 * kPartFloats +
-                                                                            2 * 16 * kMaxNL + q * kDim + ch));
-                    const float wgt = M.wall[p2][q];
-                    acc.x += wgt * v.x;
-                    acc.y += wgt * v.y;
-                    acc.z += wgt * v.z;
-                    acc.w += wgt * v.w;
-                }
-                *reinterpret_cast<float4 *>(P.entries[U.entry[j]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch) =
-                    acc;
-            }
+            slice_reduce<NQ>(
+                P.split, n4, c_lo, U.n_layers, M.wall,
+                [&](int src, int q, int ch) {
+                    return __ldcg(reinterpret_cast<const float4 *>(base + (int64_t)src * kPartFloats + kHdrFloats + q * kDim +
+                                                                   ch));
+                },
+                [&](int q, int ch, float4 acc) {
+                    *reinterpret_cast<float4 *>(P.entries[U.entry[q >> 4]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim +
+                                                ch) = acc;
+                });
         }
     }
     tc::cluster_sync();  // no CTA leaves while another reads its shared memory
@@ -880,18 +965,21 @@ size_t split_bytes(int n_units, int batch, int split)
     if (split <= 1) return 0;
     auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
     const size_t groups = (size_t)n_units * batch;
-    return r256(groups * split * kPartFloats * sizeof(float)) + r256(groups * sizeof(uint32_t));
+    return r256(groups * split * kPartFloats * sizeof(float)) + r256(groups * kMaxCS * sizeof(uint32_t));
 }
 
 // Launch shape: the (split, cluster size) with the lowest modelled time whose
-// workspace fits `budget`.  A cluster costs a fixed part (queries in, gathers'
-// latency, merge), its busiest CTA's tiles and a little per CTA; a split adds
-// the partials' round trip through global memory; clusters run `active` at a
-// time.  Costs are in units of one tile's processing.
+// workspace fits `budget`.  A cluster costs a fixed part (queries in, merge),
+// its busiest CTA's tiles and a little per CTA; a split adds the partials'
+// round trip through global memory and, per part, the last arrival's reads;
+// clusters run `active` at a time.  Costs are in microseconds, from global-
+// timer stamps of the L = 131,072 step on B300: a tile's tensor-core work
+// alone is 64 MMAs at about 46 cycles each, so a CTA's second tile costs
+// about 4 us of dequantisation, products and softmax.
 template <int NL>
 Shape choose_shape(int dev, int max_tiles, int n_groups, size_t budget)
 {
-    constexpr double kFixed = 2.0, kPerTile = 1.0, kPerCta = 0.02, kSplit = 0.35;
+    constexpr double kFixed = 6.0, kPerTile = 4.0, kPerCta = 0.05, kSplit = 2.5, kPerPart = 0.3;
     Shape best;
     double best_cost = 1e300;
     for (int split = 1; split <= kMaxCS; ++split) {
@@ -905,7 +993,8 @@ Shape choose_shape(int dev, int max_tiles, int n_groups, size_t budget)
             if (act <= 0) continue;
             const int per = (tiles + cs - 1) / cs;
             const double waves = std::ceil((double)n_groups * split / act);
-            const double cost = waves * (kFixed + kPerTile * per + kPerCta * cs) + (split > 1 ? kSplit : 0.0);
+            const double cost =
+                waves * (kFixed + kPerTile * per + kPerCta * cs) + (split > 1 ? kSplit + kPerPart * split : 0.0);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.split = split;
@@ -968,6 +1057,7 @@ int fill_params(const AttnPlan &plan, AttnParams &p, int &max_tiles)
     p.win_tiles = plan.window > 0 ? (plan.window + kRows - 1) / kRows : 0;
     p.seq_lens = plan.seq_lens;
     p.split = 1;
+    p.inputs_ready = plan.inputs_ready && plan.pdl;
     for (int e = 0; e < plan.n_entries; ++e) {
         const AttnEntry &en = plan.entries[e];
         EntryDev &E = p.entries[e];

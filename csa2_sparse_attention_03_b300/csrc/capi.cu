@@ -235,7 +235,7 @@ LevelWs level_ws(const IdxJob *jobs, int n_jobs, int batch, int max_seq_len)
 
 cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int batch, const int32_t *seq_lens,
                       int max_seq_len, int topk, int pool_out_len, int64_t scores_stride, uint8_t *fused_ws,
-                      uint8_t *old_ws, int *fp, cudaStream_t s)
+                      uint8_t *old_ws, int *fp, cudaStream_t s, int keys_ready = 0)
 {
     if (lw.fused) {
         std::vector<FusedJobDesc> d((size_t)n_jobs);
@@ -271,6 +271,7 @@ cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int bat
         L.pool_out = pool_out_len;
         L.max_len = max_seq_len;
         L.pdl = 1;
+        L.keys_ready = keys_ready;
         return launch_fused(L, lw.plan, fp, s);
     }
     // scan + select, the appends first
@@ -513,6 +514,7 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
     en.has_kv = idx ? 1 : 0;
     en.has_swa = swa_window > 0 ? 1 : 0;
     AttnPlan plan;
+    memset(&plan, 0, sizeof(plan));  // inputs_ready 0: the caller's indices may come from the previous kernel
     plan.entries = &en;
     plan.n_entries = 1;
     plan.batch = batch;
@@ -813,8 +815,10 @@ csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, i
         st = check_ws(workspace, workspace_bytes, lw.fused_bytes + lw.old_bytes);
         if (st) return st;
         uint8_t *ws = static_cast<uint8_t *>(workspace);
+        // the keys were written before the previous layer's attention (a Full
+        // layer's own new key is patched in by the kernel): copies start early
         e = run_level(jobs.data(), 1, lw, batch, seq_lens, max_seq_len, topk, d.mode == CSA2_MODE_FULL ? pool_len : 0, 0,
-                      ws, ws + lw.fused_bytes, fp, s);
+                      ws, ws + lw.fused_bytes, fp, s, 1);
         if (e != cudaSuccess) return cuda_fail(e, "index launch");
     }
     AttnEntry en;
@@ -855,6 +859,10 @@ csa2_status csa2_decode_layer(const csa2_layer_desc *layers, int32_t n_layers, i
     ap.seq_lens = seq_lens;
     ap.max_group = 1;
     ap.pdl = 1;
+    // a Reuse layer's indices come from an earlier layer's call and an SWA-only
+    // layer has none; its caches and ring were written before the previous
+    // layer's attention: the first tile is gathered before the wait for it
+    ap.inputs_ready = (d.mode == CSA2_MODE_REUSE || d.mode == CSA2_MODE_SWA_ONLY) ? 1 : 0;
     ap.workspace = a_bytes ? static_cast<uint8_t *>(workspace) + a_off : nullptr;
     ap.workspace_bytes = a_bytes;
     e = launch_attention(ap, fp, s, nullptr);

@@ -14,10 +14,11 @@
 // two targets (its Top-K and, for a Full layer, its pool).  CTA g owns the
 // contiguous candidates [g chunk, (g+1) chunk):
 //   scan     its key tiles arrive by bulk copy (a two-slot ring of 16 tiles)
-//            or, for a pool, by per-key gathers; each candidate's score
-//            becomes an order-preserving uint32 key kept in shared memory,
-//            and its CTA histogram of the keys' top 11 bits is added into the
-//            group's global histogram;
+//            or, for a pool, by per-key gathers; each thread scores two
+//            candidates at a time (exact integer block products); each
+//            score becomes an order-preserving uint32 key kept in shared
+//            memory and counted in the CTA's histogram of the keys' top 11
+//            bits, added into the group's after the scan;
 //   rounds   after each group barrier every CTA reads the same global state
 //            and takes the same decisions: the threshold bin of each target;
 //            when that bin holds at most CAP candidates, every CTA appends
@@ -55,7 +56,8 @@ constexpr int kBatchKeys = 1024;                    // candidates per bulk-copy 
 constexpr int kBatchTiles = kBatchKeys / kIdxTile;  // 16 tiles
 constexpr int kBatchBytes = kBatchTiles * kIdxTileBytes;
 constexpr int kMaxSel = 4;                          // (row, target) selections per group
-constexpr int kCandCap = 8192;                      // candidate list capacity per selection
+constexpr int kCandCap = 1024;                      // candidate list capacity per selection (every CTA resolves the
+                                                    // whole list: a larger threshold bin takes a refining round)
 constexpr int kMaxG = 1024;
 constexpr int kMaxChunk = 8192;
 
@@ -92,6 +94,7 @@ struct FusedParams {
     int32_t ring_slots;       // bulk-copy ring slots (1 or 2)
     uint32_t spin_limit;      // group-barrier polls before giving up
     uint32_t first_wait_limit;  // polls of the first tile wait (test hook; normally the mbarrier limit)
+    int32_t keys_ready;         // the key caches predate the previous kernel: copies go out before the wait
 };
 
 struct Sel {
@@ -300,7 +303,6 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     M.sk_lut[tid] = e4m3_value((uint32_t)tid);
     for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0u;
     __syncthreads();
-    tc::pdl_wait();
 
     const bool direct = job.pool == nullptr;
     const int64_t c0 = (int64_t)g * P.chunk;
@@ -316,6 +318,9 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     // out before the sequence length is known (positions past it are ignored);
     // paged caches map only the sequence's own pages, so they wait for it
     const bool early = direct && job.keys.page_size == 0;
+    // when the keys predate the previous kernel, the copies go out while it runs
+    const bool pre = early && P.keys_ready;
+    if (!pre) tc::pdl_wait();
     int L = early ? -1 : load_len();
     const int64_t c1_max = min((int64_t)(direct ? (early ? P.max_len : L) : job.pool_len), c0 + P.chunk);
     const int nb_max = (int)max((int64_t)0, (c1_max - c0 + kBatchKeys - 1) / kBatchKeys);
@@ -358,6 +363,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     if (direct && tid == 0) {
         for (int k = 0; k < min(nb_max, P.ring_slots); ++k) issue_batch(k);
     }
+    if (pre) tc::pdl_wait();
     if (L < 0) L = load_len();
     const int64_t n_cand = direct ? L : job.pool_len;
     const int64_t c1 = min(n_cand, c0 + P.chunk);
@@ -453,8 +459,8 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         }
         const uint8_t *tiles = ring + (size_t)slot * kBatchBytes;
         const int base = k * kBatchKeys;  // local index of the batch's first candidate
-#pragma unroll 1
-        for (int i = tid; i < kBatchKeys && base < nk; i += kThreads) {
+        // candidate i of the batch: its codes as int8 words and its block scales; false when absent
+        auto fetch = [&](int i, uint32_t (&kw)[16], float (&sk)[4]) -> bool {
             const int li = base + i;
             bool ok = li < nk;
             uint4 c0v = make_uint4(0u, 0u, 0u, 0u), c1v = c0v;
@@ -483,18 +489,45 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                     }
                 }
             }
-            uint32_t kw[16];
-            float sk[4];
             scan::unpack_key(c0v, c1v, scw, M.sk_lut, kw, sk);
-            for (int q = 0; q < n_rows; ++q) {
-                const float sc = scan::score_key_int(kw, sk, M.qs, q);
-                const uint32_t key = ok ? score_key(sc) : 0u;
-                if (li < nk) keys[(size_t)q * P.chunk + li] = key;
-                // the histogram of the keys' top bits: one atomic per distinct bin of the warp
-                const uint32_t tag = key ? (key >> (32 - kHistBits)) : (0x80000000u | (uint32_t)lane);
-                const uint32_t same = __match_any_sync(__activemask(), tag);
-                if (key && (__ffs(same) - 1) == lane) atomicAdd(&hist[q * kHistBins + (key >> (32 - kHistBits))], __popc(same));
-                if (key && job.out_scores[q]) job.out_scores[q][(int64_t)b * P.scores_stride + c0 + li] = sc;
+            return ok;
+        };
+        // candidate i's score for row q: its key in shared memory and one
+        // shared atomic into the histogram of the keys' top bits
+        auto record = [&](int i, bool ok, float sc, int q) {
+            const int li = base + i;
+            const uint32_t key = ok ? score_key(sc) : 0u;
+            if (li < nk) keys[(size_t)q * P.chunk + li] = key;
+            if (key) atomicAdd(&hist[q * kHistBins + (key >> (32 - kHistBits))], 1u);
+            if (key && job.out_scores[q]) job.out_scores[q][(int64_t)b * P.scores_stride + c0 + li] = sc;
+        };
+        // two candidates per thread at a time (i and i + 256), their scores'
+        // dependent chains interleaved
+        static_assert(kBatchKeys % (2 * kThreads) == 0, "two candidates per step");
+        if (n_rows == 1) {
+            const scan::Query1 q1 = scan::query_of(M.qs, 0);  // registers
+#pragma unroll 1
+            for (int i = tid; i < kBatchKeys && base < nk; i += 2 * kThreads) {
+                uint32_t kwa[16], kwb[16];
+                float ska[4], skb[4];
+                const bool oka = fetch(i, kwa, ska), okb = fetch(i + kThreads, kwb, skb);
+                const float sa = scan::score_words(kwa, ska, q1.qi8, q1.sq, q1.w);
+                const float sb = scan::score_words(kwb, skb, q1.qi8, q1.sq, q1.w);
+                record(i, oka, sa, 0);
+                record(i + kThreads, okb, sb, 0);
+            }
+        } else {
+#pragma unroll 1
+            for (int i = tid; i < kBatchKeys && base < nk; i += 2 * kThreads) {
+                uint32_t kwa[16], kwb[16];
+                float ska[4], skb[4];
+                const bool oka = fetch(i, kwa, ska), okb = fetch(i + kThreads, kwb, skb);
+                for (int q = 0; q < n_rows; ++q) {
+                    const float sa = scan::score_key_int(kwa, ska, M.qs, q);
+                    const float sb = scan::score_key_int(kwb, skb, M.qs, q);
+                    record(i, oka, sa, q);
+                    record(i + kThreads, okb, sb, q);
+                }
             }
         }
         __syncthreads();
@@ -562,7 +595,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                     int nb = S.nb;
                     uint32_t *h = hist;  // scratch histogram (4,096 bins)
                     while (nb < 32) {
-                        const int bits = (nb == 11) ? 11 : (nb == 22 ? 10 : (32 - nb >= 11 ? 11 : 32 - nb));
+                        const int bits = min(11, 32 - nb);
                         const int shift = 32 - nb - bits;
                         const int nbins = 1 << bits;
                         for (int i = tid; i < 2048; i += kThreads) h[i] = 0u;
@@ -709,18 +742,9 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
             pending = true;
             {
                 Sel S = M.sel[si];
-                const uint32_t *gh;
-                int bits;
-                if (S.nb == 0) {
-                    gh = GS.hist1[r];
-                    bits = 11;
-                } else if (S.nb == 11) {
-                    gh = GS.hist2[si];
-                    bits = 11;
-                } else {
-                    gh = GS.hist3[si];
-                    bits = 10;
-                }
+                // digits: 11 bits (the scan's histogram), 11, then the last 10
+                const uint32_t *gh = S.nb == 0 ? GS.hist1[r] : (S.nb <= 11 ? GS.hist2[si] : GS.hist3[si]);
+                const int bits = S.nb == 0 ? kHistBits : min(11, 32 - S.nb);
                 uint32_t *h = reinterpret_cast<uint32_t *>(ring);  // idle after the scan
                 load_to_smem(h, gh, 1 << bits);
                 __syncthreads();
@@ -805,7 +829,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                 }
             } else {
                 // next digit's histogram of the keys at the prefix
-                const int bits = (S.nb == 11) ? 11 : 10;
+                const int bits = min(11, 32 - S.nb);
                 uint32_t *lh = reinterpret_cast<uint32_t *>(ring);
                 for (int i = tid; i < 2048; i += kThreads) lh[i] = 0u;
                 __syncthreads();
@@ -815,7 +839,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                     if (key && prefix_of(key, S.nb) == S.prefix) atomicAdd(&lh[(key >> shift) & ((1u << bits) - 1u)], 1u);
                 }
                 __syncthreads();
-                uint32_t *gh = (S.nb == 11) ? GS.hist2[si] : GS.hist3[si];
+                uint32_t *gh = (S.nb <= 11) ? GS.hist2[si] : GS.hist3[si];
                 for (int i = tid; i < (1 << bits); i += kThreads)
                     if (lh[i]) atomicAdd(gh + i, lh[i]);
             }
@@ -941,6 +965,7 @@ cudaError_t launch_fused(const FusedLaunch &L, const FusedPlan &fp, int *flags, 
     p.topk = L.topk;
     p.pool_out = L.pool_out;
     p.max_len = L.max_len;
+    p.keys_ready = L.keys_ready;
     p.G = fp.G;
     p.chunk = fp.chunk;
     p.cap = fp.cap;

@@ -122,6 +122,7 @@ struct FusedLaunch {
     int64_t scores_stride;
     int batch, topk, pool_out, max_len;
     int pdl;
+    int keys_ready;          // 1: the key caches predate the stream's previous kernel (copies start before the wait)
 };
 
 struct FusedPlan {
@@ -159,6 +160,8 @@ struct AttnPlan {
     const int32_t *seq_lens;
     int max_group;         // layers that may share one gather (1 or 2)
     int pdl;               // 1: the launch may overlap the stream's previous kernel
+    int inputs_ready;      // 1: indices, caches, window rings and lengths were written before the
+                           // stream's previous kernel started, so they are read before the wait for it
     void *workspace;       // optional: lets a (group, sequence) split over several clusters
     size_t workspace_bytes;
 };

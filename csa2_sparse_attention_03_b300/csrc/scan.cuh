@@ -70,20 +70,23 @@ __device__ __forceinline__ void prep_query_set(int tid, int n_q, const float *co
 // Eight doubled E2M1 codes (one 32-bit word of nibbles) -> two int8 x 4 words.
 __device__ __forceinline__ void e2m1_word_to_i8(uint32_t wd, uint32_t &lo4, uint32_t &hi4)
 {
-    // magnitudes {0,1,2,3,4,6,8,12} of the 3-bit codes, picked byte by byte
-    constexpr uint32_t kLo = 0x03020100u, kHi = 0x0C080604u;
-    const uint32_t m0 = __byte_perm(kLo, kHi, wd & 0x7777u);
-    const uint32_t m1 = __byte_perm(kLo, kHi, (wd >> 16) & 0x7777u);
-    // 0xFF for every negative code, then -m = (m ^ 0xFF) - 0xFF per byte
-    const uint32_t s0 = __byte_perm(0x0000FF00u, 0u, (wd >> 3) & 0x1111u);
+    // the 3-bit magnitude codes pick bytes from the tables of +v and -v,
+    // v in {0,1,2,3,4,6,8,12}; the sign bit of each code picks the table
+    constexpr uint32_t kPosLo = 0x03020100u, kPosHi = 0x0C080604u;
+    constexpr uint32_t kNegLo = 0xFDFEFF00u, kNegHi = 0xF4F8FAFCu;
+    const uint32_t sel0 = wd & 0x7777u, sel1 = (wd >> 16) & 0x7777u;
+    const uint32_t s0 = __byte_perm(0x0000FF00u, 0u, (wd >> 3) & 0x1111u);  // 0xFF per negative code
     const uint32_t s1 = __byte_perm(0x0000FF00u, 0u, (wd >> 19) & 0x1111u);
-    lo4 = __vsub4(m0 ^ s0, s0);
-    hi4 = __vsub4(m1 ^ s1, s1);
+    lo4 = (__byte_perm(kPosLo, kPosHi, sel0) & ~s0) | (__byte_perm(kNegLo, kNegHi, sel0) & s0);
+    hi4 = (__byte_perm(kPosLo, kPosHi, sel1) & ~s1) | (__byte_perm(kNegLo, kNegHi, sel1) & s1);
 }
 
-// Score of one key (eight code words, four scale bytes) for query qi.
-__device__ __forceinline__ float score_key_int(const uint32_t (&kw)[16], const float (&sk)[4], const QuerySet &Q,
-                                               int qi)
+// Score of one key (sixteen int8 x 4 words, four scale values) against one
+// query's words qi8[h][w], block scales sq[h][j] and head weights w[h]; the
+// arrays may live in shared memory or in registers.
+template <typename QW, typename QS, typename QH>
+__device__ __forceinline__ float score_words(const uint32_t (&kw)[16], const float (&sk)[4], const QW &qi8,
+                                             const QS &sq, const QH &wt)
 {
     float score = 0.0f;
 #pragma unroll
@@ -93,14 +96,42 @@ __device__ __forceinline__ float score_key_int(const uint32_t (&kw)[16], const f
         for (int blk = 0; blk < 4; ++blk) {
             int P = 0;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) P = __dp4a((int)kw[4 * blk + w], (int)Q.qi8[qi][h][4 * blk + w], P);
-            const float t = __fmul_rn(__fmul_rn(__fmul_rn(Q.sq[qi][h][blk], sk[blk]), (float)P), 0.25f);
+            for (int w = 0; w < 4; ++w) P = __dp4a((int)kw[4 * blk + w], (int)qi8[h][4 * blk + w], P);
+            const float t = __fmul_rn(__fmul_rn(__fmul_rn(sq[h][blk], sk[blk]), (float)P), 0.25f);
             s = blk == 0 ? t : __fadd_rn(s, t);
         }
         const float r = s > 0.0f ? s : 0.0f;
-        score = h == 0 ? __fmul_rn(Q.w[qi][0], r) : __fmaf_rn(Q.w[qi][h], r, score);
+        score = h == 0 ? __fmul_rn(wt[0], r) : __fmaf_rn(wt[h], r, score);
     }
     return score == 0.0f ? 0.0f : score;
+}
+
+// Score of one key for query qi of a QuerySet in shared memory.
+__device__ __forceinline__ float score_key_int(const uint32_t (&kw)[16], const float (&sk)[4], const QuerySet &Q,
+                                               int qi)
+{
+    return score_words(kw, sk, Q.qi8[qi], Q.sq[qi], Q.w[qi]);
+}
+
+// One query of a QuerySet, copied out (into registers when indexed statically).
+struct Query1 {
+    uint32_t qi8[kIdxHeads][kIdxDim / 4];
+    float sq[kIdxHeads][kIdxDim / 16];
+    float w[kIdxHeads];
+};
+
+__device__ __forceinline__ Query1 query_of(const QuerySet &Q, int qi)
+{
+    Query1 r;
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; ++h) {
+#pragma unroll
+        for (int w = 0; w < kIdxDim / 4; ++w) r.qi8[h][w] = Q.qi8[qi][h][w];
+#pragma unroll
+        for (int j = 0; j < kIdxDim / 16; ++j) r.sq[h][j] = Q.sq[qi][h][j];
+        r.w[h] = Q.w[qi][h];
+    }
+    return r;
 }
 
 // The 64 channels of a key as int8 x 4 words, and its four block scales.

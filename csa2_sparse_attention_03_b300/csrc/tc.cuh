@@ -119,6 +119,10 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t caddr, float x, float y)
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};\n" ::"r"(caddr), "f"(x), "f"(y) : "memory");
 }
 
+// Brings the 128-B line holding p into L2 (no value is read, so it may run
+// before the data's writer has finished; later loads see the written data).
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
+
 // ---- programmatic dependent launch -----------------------------------------
 // Waits until the grids this one depends on have completed and their memory
 // is visible (a no-op when the launch has no programmatic dependency).
@@ -235,6 +239,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float v[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// N (8 or 16) consecutive 32-bit columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t addr, float (&v)[N])
+{
+    static_assert(N == 8 || N == 16, "8 or 16 columns");
+    uint32_t r[N];
+    if constexpr (N == 8) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(addr));
+    } else {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(addr));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t addr, const float v[32])

@@ -278,8 +278,16 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
  * A model calls it for layer 0, 1, ... with its own work in between; the
  * layers a call reads (kv_src's caches and pool, idx_src's indices) must
  * have run before on the same stream.  Launches may overlap the tail of
- * the stream's previous kernel (programmatic dependent launch); they read
- * nothing that kernel writes before it completes.  Workspace: the size of
+ * the stream's previous kernel (programmatic dependent launch).  What that
+ * kernel may write (this layer's queries, indexer query and weights, its
+ * appended rows) is read only after it completes.  Read before that, so
+ * that their loads overlap the previous kernel: a FULL or REINDEX layer's
+ * indexer keys (contiguous caches; a FULL layer's own new key is patched
+ * in), and a REUSE or SWA_ONLY layer's indices, sequence lengths, kv_src's
+ * cache and window ring.  These must have been written before the stream's
+ * previous kernel started, as they are when the layers run in order
+ * through this call: do not rewrite them with a kernel launched right
+ * before this call.  Workspace: the size of
  * csa2_decode_layer_workspace() (zero-filled before its first use, see
  * the conventions above), shared by every layer's call. */
 size_t csa2_decode_layer_workspace(const csa2_layer_desc *layers, int32_t n_layers, int32_t batch,

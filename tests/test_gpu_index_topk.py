@@ -114,6 +114,28 @@ def test_all_equal_scores_take_lowest_positions(cuda, orc):
     assert np.array_equal(idx2[0].cpu().numpy(), np.arange(K2))
 
 
+@pytest.mark.parametrize("K", [3000, 7777])
+def test_few_distinct_scores_over_many_keys(cuda, orc, K):
+    """60,000 keys drawn from 40 distinct rows: each score value is shared by
+    ~1,500 keys, so the threshold bin overflows the candidate list at every
+    digit (coarse, 16-bit, the refining digits) and the ties at the
+    threshold are split by position."""
+    L = 60000
+    rows = synth.normal_rows(15, "tk", (0,), 0, 40, 64)
+    pick = np.random.default_rng(15).integers(0, 40, L)
+    x = rows[pick]
+    cache, ref = _keys(cuda, orc, [x], 60032)
+    q, w = _queries(1, 8)
+    seq = torch.tensor([L], dtype=torch.int32, device="cuda")
+    idx, _, sc = cuda.csa2_index_topk(cuda.MODE_FULL, cache, torch.from_numpy(q).cuda(), torch.from_numpy(w).cuda(),
+                                      seq, L, K, with_scores=True)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags)
+    s = orc.index_scores(q[0], w[0], ref[0][0], ref[0][1])
+    assert np.array_equal(sc[0].cpu().numpy().view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(idx[0].cpu().numpy(), orc.topk(s, np.arange(L, dtype=np.int32), K))
+
+
 def test_extreme_codes_are_exact(cuda, orc):
     """Keys and queries at the E2M1 extremes (every code +-6, the largest and
     smallest E4M3 scales): the tensor-core block sums stay exact."""
