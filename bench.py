@@ -73,6 +73,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work budget of the oracle baseline")
+    ap.add_argument("--only-sequential", action="store_true",
+                    help="time the layer-sequential step alone and print its time (no other measurements; "
+                         "the command the committed launch-list and kernel profiles were taken with)")
     return ap.parse_args()
 
 
@@ -469,7 +472,7 @@ def run_csa2(args):
     from csa2_sparse_attention_03_b300 import synth
     w = synth.workload(args.config)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only_sequential:
         cpu = cpu_baseline(w, args.cpu_seconds)
 
     torch.cuda.set_device(local)
@@ -518,6 +521,12 @@ def run_csa2(args):
     ms = ms_total / args.steps
     value = whole_job_value(world, w.batch, ms)
     n_small = max(1, min(args.steps, 100))
+    if args.only_sequential:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": ms, "steps": args.steps,
+                              "warmup": args.warmup, "launches_per_step": int(seq_launches),
+                              "note": "layer-sequential step only (profiling run)"}))
+        return 0
 
     # the phased step (csa2_decode_layers), same timing
     n0 = csa2.csa2_launch_count()

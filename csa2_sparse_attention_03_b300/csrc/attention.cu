@@ -23,9 +23,10 @@
 //                  memory), so every weight P = exp(z - m) <= e^2 as fp16;
 //   O^T += V^T P   M 128 channels (four blocks), N 16 NL queries, K the rows.
 // The CTAs of a cluster then merge their partials through distributed shared
-// memory: each publishes its running (max, sum) per query, scales its O^T by
-// its share of the cluster's softmax denominator, and each CTA sums one slice
-// of the output channels over the cluster and writes it.  When one (unit,
+// memory: each pushes its running (max, sum) per query into every peer,
+// stages its O^T normalised by its own sum, and sends each CTA, by one bulk
+// copy, its block of that CTA's slice of the channels; each CTA weighs and
+// sums its slice over the cluster and writes it.  When one (unit,
 // sequence) has more tiles than a cluster takes well, it is split over
 // several clusters, each a contiguous part of the tiles: each writes its
 // merged partial (max, sum, normalised output) to the workspace, and the last
@@ -121,7 +122,8 @@ struct Misc {
     float alpha[16 * kMaxNL];        // factor moving O^T to that maximum
     __align__(16) uint8_t app[kMaxNL][kDim];  // appended window row per layer slot (E4M3 codes)
     float app_scale[kMaxNL];
-    uint64_t bar_qk, bar_pv;
+    float app_max[kMaxNL][4];        // per-warp maxima of an appended row
+    uint64_t bar_qk, bar_pv, bar_rx;
     uint32_t tmem_slot;
     int32_t ok;
     int32_t any_resc;
@@ -133,6 +135,11 @@ constexpr size_t smem_bytes()
     return (size_t)kTileBytes + (size_t)NL * (kQBytes + kPBytes) + sizeof(Misc);
 }
 static_assert(smem_bytes<2>() <= 232448, "attention shared memory over the 227 KB limit");
+// the merge's staged and received blocks (cs x cpc <= 512 + 4 cs <= 576 channels)
+// fit the tile and query buffers
+static_assert(2 * 16 * kMaxNL * 576 * 4 <= kTileBytes + kMaxNL * kQBytes &&
+                  2 * 16 * 1 * 576 * 4 <= kTileBytes + 1 * kQBytes,
+              "merge blocks fit");
 
 // Byte offset of fp16 element (row r, channel c) of a 512-channel operand in
 // the no-swizzle core-matrix layout: 8-row groups 8,192 B apart, 8-channel
@@ -312,58 +319,46 @@ __device__ __forceinline__ void dequant(const Ctx &c, bool window, int r, int h,
     for (int k = 0; k < kChunks; ++k) dequant_chunk(c, window, r, h, k, raw, T);
 }
 
-// Row r of a window tile from the appended codes of layer slot j (one warp,
-// 16 channels per lane), with its row factor.
-__device__ __forceinline__ void dequant_app_row(Misc &M, int j, int r, int lane, uint8_t *T)
-{
-    const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));  // 2^-8
-    const uint4 cw = *reinterpret_cast<const uint4 *>(&M.app[j][16 * lane]);
-    *reinterpret_cast<uint4 *>(T + cm_off(r, 16 * lane)) =
-        make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.x & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.x >> 16), k2m8)),
-                   pack_h2(__hmul2(e4m3x2_half2(cw.y & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.y >> 16), k2m8)));
-    *reinterpret_cast<uint4 *>(T + cm_off(r, 16 * lane + 8)) =
-        make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.z & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.z >> 16), k2m8)),
-                   pack_h2(__hmul2(e4m3x2_half2(cw.w & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(cw.w >> 16), k2m8)));
-    if (lane == 0) M.rowfac[r] = M.app_scale[j] * 256.0f;
-}
-
 // Quantises a layer's appended window row into its ring slot at position
 // L-1 (FP8, scale = absmax / 448) and keeps the codes in shared memory for
-// this CTA's own window tile.  One warp; lane = 16 channels.
-__device__ __forceinline__ void append_window_row(const Ctx &c, const EntryDev &E, int j, int lane)
+// this CTA's own window tile.  128 threads (four warps, named barrier 1 + j);
+// thread t: channels 4t .. 4t+3.  With `patch`, also writes the row's fp16
+// values into row r_app of the (already dequantised) tile buffer.
+__device__ __forceinline__ void append_window_row(const Ctx &c, const EntryDev &E, int j, int t, bool patch, int r_app,
+                                                  uint8_t *T)
 {
-    const float4 *src = reinterpret_cast<const float4 *>(E.new_swa + (int64_t)c.b * kDim + lane * 16);
-    float x[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float4 v = __ldcg(src + k);
-        x[4 * k] = v.x;
-        x[4 * k + 1] = v.y;
-        x[4 * k + 2] = v.z;
-        x[4 * k + 3] = v.w;
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    Misc &M = *c.M;
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(E.new_swa + (int64_t)c.b * kDim) + t);
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((t & 31) == 0) M.app_max[j][t >> 5] = amax;
+    if (j == 0)
+        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    else
+        asm volatile("bar.sync 2, 128;\n" ::: "memory");
+    amax = fmaxf(fmaxf(M.app_max[j][0], M.app_max[j][1]), fmaxf(M.app_max[j][2], M.app_max[j][3]));
     const float s = __fdiv_rn(amax, 448.0f);
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (s != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i >> 2] |= e4m3_code(__fdiv_rn(x[i], s)) << (8 * (i & 3));
-    }
-    const uint4 cw = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(&c.M->app[j][lane * 16]) = cw;
-    const int64_t pos = (int64_t)c.L - 1;
-    const int64_t slot = slot_of(E.swa, c.b, pos);
+    uint32_t w = 0u;
+    if (s != 0.0f)
+        w = e4m3_code(__fdiv_rn(v.x, s)) | (e4m3_code(__fdiv_rn(v.y, s)) << 8) | (e4m3_code(__fdiv_rn(v.z, s)) << 16) |
+            (e4m3_code(__fdiv_rn(v.w, s)) << 24);
+    reinterpret_cast<uint32_t *>(M.app[j])[t] = w;
+    const int64_t slot = slot_of(E.swa, c.b, (int64_t)c.L - 1);
     if (slot < 0) {
-        if (lane == 0) raise_flag(c.flags, kFlagBounds);
+        if (t == 0) raise_flag(c.flags, kFlagBounds);
     } else {
-        *reinterpret_cast<uint4 *>(E.swa.data + slot * kDim + lane * 16) = cw;
-        if (lane == 0) reinterpret_cast<float *>(E.swa.data + E.swa.n_slots * kDim)[slot] = s;
+        reinterpret_cast<uint32_t *>(E.swa.data + slot * kDim)[t] = w;
+        if (t == 0) reinterpret_cast<float *>(E.swa.data + E.swa.n_slots * kDim)[slot] = s;
     }
-    if (lane == 0) c.M->app_scale[j] = s;
+    if (t == 0) M.app_scale[j] = s;
+    if (patch) {
+        // the row in the tile buffer: codes x 2^-8 (exact in fp16), its row factor
+        const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));
+        *reinterpret_cast<uint2 *>(T + cm_off(r_app, 4 * t)) =
+            make_uint2(pack_h2(__hmul2(e4m3x2_half2(w & 0xFFFFu), k2m8)), pack_h2(__hmul2(e4m3x2_half2(w >> 16), k2m8)));
+        if (t == 0) M.rowfac[r_app] = s * 256.0f;
+    }
 }
 
 // Softmax of one tile, all eight warps: thread (row r = TMEM lane, query half
@@ -458,69 +453,63 @@ __device__ __forceinline__ void softmax_tile(const Ctx &c, uint32_t tmem, uint8_
     tc::fence_before_sync();
 }
 
+// From the (max, sum) table M.mlall[0..ns) of each query: the merged maximum
+// and sum (M.cm, M.cl) and each source's weight l_s exp(m_s - max) / sum
+// (M.wall).  All 256 threads: sixteen lanes per query, lane = source.
+template <int NQ>
+__device__ __forceinline__ void merge_weights(Misc &M, int ns)
+{
+    static_assert((NQ * 16) % kThreads == 0, "whole warps per pass");
+#pragma unroll 1
+    for (int i = threadIdx.x; i < NQ * 16; i += kThreads) {
+        const int q = i >> 4, src = i & 15, lead = threadIdx.x & 16;  // lane of source 0 of this query
+        const float2 ml = src < ns ? M.mlall[src][q] : make_float2(-INFINITY, 0.0f);
+        float mx = ml.y > 0.0f ? ml.x : -INFINITY;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        const float e = ml.y > 0.0f ? ml.y * __expf(ml.x - mx) : 0.0f;
+        float lsum = e;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+        lsum = __shfl_sync(0xFFFFFFFFu, lsum, lead);  // one sum for every source of the query
+        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+        if (src < ns) M.wall[src][q] = e * inv;
+        if (src == 0) {
+            M.cm[q] = mx;
+            M.cl[q] = lsum;
+        }
+    }
+}
+
 // Weighted sums over `ns` sources for this thread's items of one channel
 // slice: item = (query q, four channels), n4 items per query.  For each item,
-// sum_s wgt[s][q] x load(s, q, ch) in source order.  With few sources, four
-// items go at once; otherwise one item with all its sources: every load of a
-// batch is in flight before the first is used.
+// sum_s wgt[s][q] x load(s, q, ch) in source order, every source's load in
+// flight before the first is used.  (The launch shapes the host picks give a
+// thread at most one or two items.)
 template <int NQ, typename Load, typename Store>
 __device__ __forceinline__ void slice_reduce(int ns, int n4, int c_lo, int n_layers, const float (*wgt)[16 * kMaxNL],
                                              Load load, Store store)
 {
     const int total = NQ * n4;
-    const int tid = threadIdx.x;
-    if (ns <= 4) {
-        for (int base = tid; base < total; base += 4 * kThreads) {
-            float4 v[4][4];
+#pragma unroll 1
+    for (int item = threadIdx.x; item < total; item += kThreads) {
+        const int q = item / n4, ch = c_lo + 4 * (item % n4);
+        if ((q >> 4) >= n_layers) continue;
+        float4 v[kMaxCS];
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const int item = base + ii * kThreads;
-                const int q = item / max(n4, 1), ch = c_lo + 4 * (item - q * n4);
-                if (item < total && (q >> 4) < n_layers) {
+        for (int k = 0; k < kMaxCS; ++k)
+            if (k < ns) v[k] = load(k, q, ch);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (k < ns) v[ii][k] = load(k, q, ch);
-                }
+        for (int k = 0; k < kMaxCS; ++k)
+            if (k < ns) {
+                const float w = wgt[k][q];
+                acc.x += w * v[k].x;
+                acc.y += w * v[k].y;
+                acc.z += w * v[k].z;
+                acc.w += w * v[k].w;
             }
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const int item = base + ii * kThreads;
-                const int q = item / max(n4, 1), ch = c_lo + 4 * (item - q * n4);
-                if (item < total && (q >> 4) < n_layers) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (k < ns) {
-                            const float w = wgt[k][q];
-                            acc.x += w * v[ii][k].x;
-                            acc.y += w * v[ii][k].y;
-                            acc.z += w * v[ii][k].z;
-                            acc.w += w * v[ii][k].w;
-                        }
-                    store(q, ch, acc);
-                }
-            }
-        }
-    } else {
-        for (int item = tid; item < total; item += kThreads) {
-            const int q = item / n4, ch = c_lo + 4 * (item % n4);
-            if ((q >> 4) >= n_layers) continue;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 v[kMaxCS];
-#pragma unroll
-            for (int k = 0; k < kMaxCS; ++k)
-                if (k < ns) v[k] = load(k, q, ch);
-#pragma unroll
-            for (int k = 0; k < kMaxCS; ++k)
-                if (k < ns) {
-                    const float w = wgt[k][q];
-                    acc.x += w * v[k].x;
-                    acc.y += w * v[k].y;
-                    acc.z += w * v[k].z;
-                    acc.w += w * v[k].w;
-                }
-            store(q, ch, acc);
-        }
+        store(q, ch, acc);
     }
 }
 
@@ -544,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (tid == 0) {
         tc::mbar_init(&M.bar_qk, 1);
         tc::mbar_init(&M.bar_pv, 1);
+        tc::mbar_init(&M.bar_rx, 1);
         tc::mbar_init_fence();
         M.ok = 1;
     }
@@ -635,16 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     }
     if (!pre) first_gather();
 
-    // appended window rows of this CTA's window tiles (position L-1 of each layer)
-    if (P.window > 0 && c.L > 0 && warp < U.n_layers) {
-        const int j = warp;
+    // appended window rows of this CTA's window tiles (position L-1 of each
+    // layer): layer slot j by threads 128 j .. 128 j + 127
+    if (P.window > 0 && c.L > 0 && (tid >> 7) < U.n_layers) {
+        const int j = tid >> 7;
         const EntryDev &E = P.entries[U.entry[j]];
         const int t_app = U.row_tiles + j * P.win_tiles + (P.window - 1) / kRows;
-        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0) {
-            append_window_row(c, E, j, lane);
-            __syncwarp();
-            if (pre && t_app == t0) dequant_app_row(M, j, (P.window - 1) % kRows, lane, T);
-        }
+        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0)
+            append_window_row(c, E, j, tid & 127, pre && t_app == t0, (P.window - 1) % kRows, T);
     }
 
 #pragma unroll
@@ -689,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             tc::fence_after_sync();
             const uint64_t a0 = tc::sdesc(tc::smem_u32(T), 128, 8192);
             const uint64_t b0 = tc::sdesc(tc::smem_u32(Qs), 128, 8192);
-#pragma unroll
+            // rolled: the issue rate of the tensor core, not the loop, bounds these
+#pragma unroll 1
             for (int ks = 0; ks < kDim / 16; ++ks)
                 tc::mma_f16(tmem + Cols<NL>::S, a0 + 16 * ks, b0 + 16 * ks, kIdescQK, ks > 0 ? 1u : 0u);
             tc::mma_commit(&M.bar_qk);
@@ -701,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         if (tid == 0) {
             tc::fence_after_sync();
             // the four channel blocks are independent accumulators: interleaved
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < kRows / 16; ++ks)
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb)
@@ -725,7 +714,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     // ---- merge across the cluster: every CTA stages its output normalised by its
     // own sum, with its (max, sum); one cluster barrier; each CTA then weighs
     // and sums one slice of the channels over the cluster
-    float *stage = reinterpret_cast<float *>(T);  // [query][channel] fp32, in the idle tile buffer
+    // channel slices: CTA r owns channels [r cpc, min(512, (r + 1) cpc))
+    const int cpc = ((kDim + cs - 1) / cs + 3) & ~3;
+    const int c_lo = rank * cpc, c_hi = min(kDim, c_lo + cpc);
+    const int n4 = max(0, (c_hi - c_lo) / 4);
+    const uint32_t blk_bytes = (uint32_t)(NQ * cpc * 4);  // one owner's block: [query][cpc] fp32
+    // staged output, [owner][query][channel of the owner's slice], in the idle
+    // tile buffer; the blocks this CTA receives follow it (into the query
+    // buffer, idle too, for two layers)
+    float *stage = reinterpret_cast<float *>(T);
+    float *recv = reinterpret_cast<float *>(T + ((cs * blk_bytes + 127u) & ~127u));
     // this CTA's (m, l) of every query into every CTA's table (remote stores,
     // visible after the cluster barrier; every peer has started by now)
     tc::cluster_wait();
@@ -733,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const int q = i % NQ, dst = i / NQ;
         tc::st_cluster_f2(tc::mapa(tc::smem_u32(&M.mlall[rank][q]), (uint32_t)dst), M.m_run[q], M.l_run[q]);
     }
+    if (tid == 0) tc::mbar_expect_tx(&M.bar_rx, (uint32_t)cs * blk_bytes);  // every peer's block for this slice
     {
         const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32 quad.., column half
         const int ch_in = 32 * quad + lane;
@@ -748,53 +747,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int col = c0 + i, cb = col / NQ, q = col % NQ;
-                stage[q * kDim + 128 * cb + ch_in] = o[i] * M.inv_l[q];
+                const int ch = 128 * cb + ch_in, own = ch / cpc;
+                stage[(own * NQ + q) * cpc + (ch - own * cpc)] = o[i] * M.inv_l[q];
             }
         }
     }
+    tc::fence_async_smem();  // the staged blocks are read by bulk copies
     tc::fence_before_sync();
     tc::cluster_sync();
     if (warp == 0) {  // O^T is staged: tensor memory is done
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, Cols<NL>::alloc);
     }
-    if (tid >= kThreads - NQ) {
-        // the cluster's maximum and sum; each CTA's weight l_s exp(m_s - M) / L
-        // (every table entry loaded at once; sums in source order)
-        const int q = tid - (kThreads - NQ);
-        float2 ml[kMaxCS];
-#pragma unroll
-        for (int s = 0; s < kMaxCS; ++s) ml[s] = s < cs ? M.mlall[s][q] : make_float2(-INFINITY, 0.0f);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < kMaxCS; ++s)
-            if (ml[s].y > 0.0f) mx = fmaxf(mx, ml[s].x);
-        float e[kMaxCS], lsum = 0.0f;
-#pragma unroll
-        for (int s = 0; s < kMaxCS; ++s) {
-            e[s] = ml[s].y > 0.0f ? ml[s].y * __expf(ml[s].x - mx) : 0.0f;
-            lsum += e[s];
-        }
-        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-#pragma unroll
-        for (int s = 0; s < kMaxCS; ++s)
-            if (s < cs) M.wall[s][q] = e[s] * inv;
-        M.cm[q] = mx;
-        M.cl[q] = lsum;
+    // one bulk copy per owner: this CTA's block of its slice, into the owner's
+    // receive area at this CTA's rank, completing on the owner's barrier
+    if (tid < cs) {
+        const uint32_t dst = tc::mapa(tc::smem_u32(recv) + (uint32_t)rank * blk_bytes, (uint32_t)tid);
+        tc::bulk_s2peer(dst, reinterpret_cast<const uint8_t *>(stage) + (size_t)tid * blk_bytes, blk_bytes,
+                        tc::mapa(tc::smem_u32(&M.bar_rx), (uint32_t)tid));
+    }
+    merge_weights<NQ>(M, cs);
+    if (!tc::mbar_wait(&M.bar_rx, 0)) {
+        M.ok = 0;
+        tc::mbar_wait(&M.bar_rx, 0);  // a last chance for the copies in flight
     }
     __syncthreads();
-    const int cpc = ((kDim + cs - 1) / cs + 3) & ~3;
-    const int c_lo = rank * cpc, c_hi = min(kDim, c_lo + cpc);
-    const int n4 = max(0, (c_hi - c_lo) / 4);
+    if (tid == 0 && !M.ok) raise_flag(flags, kFlagTimeout);
     float *part_rec = P.split > 1
                           ? P.parts + (((int64_t)unit * P.batch + c.b) * P.split + part) * (int64_t)kPartFloats
                           : nullptr;
     {
-        const uint32_t st_addr = tc::smem_u32(stage);
         slice_reduce<NQ>(
             cs, n4, c_lo, U.n_layers, M.wall,
             [&](int src, int q, int ch) {
-                return tc::ld_cluster_f4(tc::mapa(st_addr + (uint32_t)(q * kDim + ch) * 4u, (uint32_t)src));
+                return *reinterpret_cast<const float4 *>(recv + (src * NQ + q) * cpc + (ch - c_lo));
             },
             [&](int q, int ch, float4 acc) {
                 float *dst = part_rec ? part_rec + kHdrFloats + q * kDim + ch
@@ -840,24 +826,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 M.mlall[p2][q] = make_float2(__ldcg(rec + rank * 32 * kMaxNL + q), __ldcg(rec + rank * 32 * kMaxNL + 16 * kMaxNL + q));
             }
             __syncthreads();
-            if (tid < NQ) {
-                const int q = tid;
-                float mx = -INFINITY;
-                for (int p2 = 0; p2 < P.split; ++p2)
-                    if (M.mlall[p2][q].y > 0.0f) mx = fmaxf(mx, M.mlall[p2][q].x);
-                float lsum = 0.0f;
-                for (int p2 = 0; p2 < P.split; ++p2)
-                    if (M.mlall[p2][q].y > 0.0f) lsum += M.mlall[p2][q].y * __expf(M.mlall[p2][q].x - mx);
-                const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-                for (int p2 = 0; p2 < P.split; ++p2) {
-                    const float2 ml = M.mlall[p2][q];
-                    M.wall[p2][q] = ml.y > 0.0f ? ml.y * __expf(ml.x - mx) * inv : 0.0f;
-                }
-                const int j = q >> 4;
-                if (rank == 0 && j < U.n_layers && P.entries[U.entry[j]].lse)
-                    P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] = lsum > 0.0f ? mx + logf(lsum) : -INFINITY;
-            }
+            merge_weights<NQ>(M, P.split);
             __syncthreads();
+            if (tid < NQ && rank == 0 && (tid >> 4) < U.n_layers && P.entries[U.entry[tid >> 4]].lse)
+                P.entries[U.entry[tid >> 4]].lse[(int64_t)c.b * kHeads + (tid & 15)] =
+                    M.cl[tid] > 0.0f ? M.cm[tid] + logf(M.cl[tid]) : -INFINITY;
             slice_reduce<NQ>(
                 P.split, n4, c_lo, U.n_layers, M.wall,
                 [&](int src, int q, int ch) {

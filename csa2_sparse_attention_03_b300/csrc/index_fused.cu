@@ -504,30 +504,17 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         // two candidates per thread at a time (i and i + 256), their scores'
         // dependent chains interleaved
         static_assert(kBatchKeys % (2 * kThreads) == 0, "two candidates per step");
-        if (n_rows == 1) {
-            const scan::Query1 q1 = scan::query_of(M.qs, 0);  // registers
 #pragma unroll 1
-            for (int i = tid; i < kBatchKeys && base < nk; i += 2 * kThreads) {
-                uint32_t kwa[16], kwb[16];
-                float ska[4], skb[4];
-                const bool oka = fetch(i, kwa, ska), okb = fetch(i + kThreads, kwb, skb);
-                const float sa = scan::score_words(kwa, ska, q1.qi8, q1.sq, q1.w);
-                const float sb = scan::score_words(kwb, skb, q1.qi8, q1.sq, q1.w);
-                record(i, oka, sa, 0);
-                record(i + kThreads, okb, sb, 0);
-            }
-        } else {
+        for (int i = tid; i < kBatchKeys && base < nk; i += 2 * kThreads) {
+            uint32_t kwa[16], kwb[16];
+            float ska[4], skb[4];
+            const bool oka = fetch(i, kwa, ska), okb = fetch(i + kThreads, kwb, skb);
 #pragma unroll 1
-            for (int i = tid; i < kBatchKeys && base < nk; i += 2 * kThreads) {
-                uint32_t kwa[16], kwb[16];
-                float ska[4], skb[4];
-                const bool oka = fetch(i, kwa, ska), okb = fetch(i + kThreads, kwb, skb);
-                for (int q = 0; q < n_rows; ++q) {
-                    const float sa = scan::score_key_int(kwa, ska, M.qs, q);
-                    const float sb = scan::score_key_int(kwb, skb, M.qs, q);
-                    record(i, oka, sa, q);
-                    record(i + kThreads, okb, sb, q);
-                }
+            for (int q = 0; q < n_rows; ++q) {
+                float sa, sb;
+                scan::score_pair(kwa, ska, kwb, skb, M.qs, q, sa, sb);
+                record(i, oka, sa, q);
+                record(i + kThreads, okb, sb, q);
             }
         }
         __syncthreads();

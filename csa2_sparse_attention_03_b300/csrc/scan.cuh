@@ -34,7 +34,7 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
 
 // The queries of one scan in shared memory: doubled codes as int8 x 4
 // (channels 4w..4w+3 in word w of a head), block scales, head weights.
-struct QuerySet {
+struct __align__(16) QuerySet {
     uint32_t qi8[2][kIdxHeads][kIdxDim / 4];
     float sq[2][kIdxHeads][kIdxDim / 16];
     float w[2][kIdxHeads];
@@ -113,25 +113,43 @@ __device__ __forceinline__ float score_key_int(const uint32_t (&kw)[16], const f
     return score_words(kw, sk, Q.qi8[qi], Q.sq[qi], Q.w[qi]);
 }
 
-// One query of a QuerySet, copied out (into registers when indexed statically).
-struct Query1 {
-    uint32_t qi8[kIdxHeads][kIdxDim / 4];
-    float sq[kIdxHeads][kIdxDim / 16];
-    float w[kIdxHeads];
-};
-
-__device__ __forceinline__ Query1 query_of(const QuerySet &Q, int qi)
+// Scores of two keys against query qi of a QuerySet in shared memory, with
+// the same rounding points as score_words.  The heads run in a rolled loop
+// and share their query loads between the two keys: the code stays small (a
+// scan runs it once per launch, from a cold instruction cache) and the two
+// keys' dependent chains interleave.
+__device__ __forceinline__ void score_pair(const uint32_t (&ka)[16], const float (&sa)[4], const uint32_t (&kb)[16],
+                                           const float (&sb)[4], const QuerySet &Q, int qi, float &out_a, float &out_b)
 {
-    Query1 r;
-#pragma unroll
+    float score_a = 0.0f, score_b = 0.0f;
+#pragma unroll 1
     for (int h = 0; h < kIdxHeads; ++h) {
+        const uint4 *qw = reinterpret_cast<const uint4 *>(Q.qi8[qi][h]);
+        const float4 sq4 = *reinterpret_cast<const float4 *>(Q.sq[qi][h]);
+        const float sq[4] = {sq4.x, sq4.y, sq4.z, sq4.w};
+        float s_a = 0.0f, s_b = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kIdxDim / 4; ++w) r.qi8[h][w] = Q.qi8[qi][h][w];
-#pragma unroll
-        for (int j = 0; j < kIdxDim / 16; ++j) r.sq[h][j] = Q.sq[qi][h][j];
-        r.w[h] = Q.w[qi][h];
+        for (int blk = 0; blk < 4; ++blk) {
+            const uint4 q4 = qw[blk];
+            int pa = __dp4a((int)ka[4 * blk], (int)q4.x, 0), pb = __dp4a((int)kb[4 * blk], (int)q4.x, 0);
+            pa = __dp4a((int)ka[4 * blk + 1], (int)q4.y, pa);
+            pb = __dp4a((int)kb[4 * blk + 1], (int)q4.y, pb);
+            pa = __dp4a((int)ka[4 * blk + 2], (int)q4.z, pa);
+            pb = __dp4a((int)kb[4 * blk + 2], (int)q4.z, pb);
+            pa = __dp4a((int)ka[4 * blk + 3], (int)q4.w, pa);
+            pb = __dp4a((int)kb[4 * blk + 3], (int)q4.w, pb);
+            const float ta = __fmul_rn(__fmul_rn(__fmul_rn(sq[blk], sa[blk]), (float)pa), 0.25f);
+            const float tb = __fmul_rn(__fmul_rn(__fmul_rn(sq[blk], sb[blk]), (float)pb), 0.25f);
+            s_a = blk == 0 ? ta : __fadd_rn(s_a, ta);
+            s_b = blk == 0 ? tb : __fadd_rn(s_b, tb);
+        }
+        // fma(w, r, +0) rounds w r once, as the first head's product does
+        const float wh = Q.w[qi][h];
+        score_a = __fmaf_rn(wh, s_a > 0.0f ? s_a : 0.0f, score_a);
+        score_b = __fmaf_rn(wh, s_b > 0.0f ? s_b : 0.0f, score_b);
     }
-    return r;
+    out_a = score_a == 0.0f ? 0.0f : score_a;
+    out_b = score_b == 0.0f ? 0.0f : score_b;
 }
 
 // The 64 channels of a key as int8 x 4 words, and its four block scales.
