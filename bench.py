@@ -92,6 +92,45 @@ def peaks():
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
+KERNEL_SOURCES = {  # the device code a kernel is compiled from (a change voids its ncu counters)
+    "attn_kernel": ("attention.cu", "tc.cuh", "common.cuh"),
+    "index_fused_kernel": ("index_fused.cu", "scan.cuh", "tc.cuh", "common.cuh"),
+}
+
+
+def kernel_source_sha16(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "csa2_sparse_attention_03_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, pdir=None):
+    """DRAM bytes (read + write) per launch of ``kernel`` from the committed ncu
+    summaries: a line ``traffic-record: kernel=K workload=W launches=N
+    dram_bytes_per_launch=B source_sha16=S`` (W with '_' for ' ').  None when
+    no record matches the workload or the kernel's sources changed since."""
+    pdir = pdir or os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None, None
+    want = kernel_source_sha16(kernel)
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as f:
+            for line in f:
+                if not line.strip().startswith("traffic-record:"):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split(":", 1)[1].split() if "=" in t)
+                if kv.get("kernel") == kernel and kv.get("workload", "").replace("_", " ") == workload:
+                    if kv.get("source_sha16") != want:
+                        return None, f"profiles/{fn}: kernel sources changed since the capture"
+                    return float(kv["dram_bytes_per_launch"]), f"profiles/{fn}"
+    return None, None
+
+
 def _layer_parts(w, ly):
     """Bytes one layer moves in the layer-sequential order, by part: its key
     pass (36 B per position scored, or 36 B + 4 B per pool entry), its
@@ -458,6 +497,39 @@ class GraphTimer:
         return out
 
 
+def multi_query_timing(csa2, torch, step, w, timer, stream, dev, n_small):
+    """csa2_index_topk_multi at n_q = 8 and 32 causal query rows per sequence
+    over the first Full layer's indexer keys (Top-K = the workload's).
+    Useful tensor work: 2 x 4 heads x 64 channels per (row, candidate)."""
+    if not step.caches:
+        return None
+    ik = step.caches[min(step.caches)][1]
+    B, L, K = w.batch, int(w.max_len), int(w.topk)
+    lens = [int(x) for x in w.seq_lens]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed + 7)
+    res = {}
+    for nq in (8, 32):
+        q = torch.randn((B, nq, 4, 64), generator=gen, device=dev) * 0.125
+        wt = torch.rand((B, nq, 4), generator=gen, device=dev)
+        idx = torch.empty((B, nq, K), dtype=torch.int32, device=dev)
+        ws = csa2.new_workspace(csa2.csa2_index_topk_multi_workspace(B, nq, L), dev)
+        n0 = csa2.csa2_launch_count()
+        g = timer.capture(lambda: csa2.csa2_index_topk_multi(ik, q, wt, step.seq_lens, L, K, out_idx=idx,
+                                                             workspace=ws, stream=stream))
+        launches = (csa2.csa2_launch_count() - n0) // 2
+        t = statistics.mean(timer.time(g, n_small))
+        cand = sum(max(0, min(Lb, Lb - nq + i + 1)) for Lb in lens for i in range(nq))
+        flops = 2 * 4 * 64 * cand
+        nbytes = sum(lens) * IDX_ROW + B * nq * (4 * 64 * 4 + 16 + K * 4)
+        res[f"n_q={nq}"] = {"ms": t, "query_tokens_per_s": B * nq / (t * 1e-3), "launches": int(launches),
+                            "useful_tflops": flops / (t * 1e-3) / 1e12, "keys_gbs": nbytes / (t * 1e-3) / 1e9}
+        del g
+    res["how"] = ("csa2_index_topk_multi (tcgen05 kind::f16 scoring, one MMA per 16-channel block, then the "
+                  "cluster select), causal rows, CUDA events around a graph of the call, L2 flushed before each")
+    return res
+
+
 def run_csa2(args):
     import torch
 
@@ -572,14 +644,23 @@ def run_csa2(args):
                          "achieved_gbs": by / (t * 1e-3) / 1e9, "frac": by / (t * 1e-3) / 1e9 / peak}
         del g
     check("the kernel timings")
+
+    # many queries per sequence (a speculative verification, a prefill chunk):
+    # the tensor-core multi-query scoring and its Top-K over the first Full
+    # layer's indexer keys, causal rows
+    multi = multi_query_timing(csa2, torch, step, w, timer, stream, dev, n_small)
+    check("the multi-query indexing")
     # dominant kernel: the larger share of the step (its launches x their time)
     top = max(kernels, key=lambda k: kernels[k]["ms_all_launches"]) if kernels else None
     roof = None
     if top:
         kd = kernels[top]
+        kname = top.split("(")[-1].rstrip(")")
+        traffic, traffic_src = recorded_traffic(kname, w.name)
         roof = {"kernel": top, "bound": "hbm", "unit": "GB/s", "peak": peak,
                 "peak_source": f"{peak_kind} copy bandwidth", "achieved": kd["achieved_gbs"], "frac": kd["frac"],
-                "traffic": None, "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"],
+                "traffic": traffic, "traffic_source": traffic_src,
+                "algorithmic_bytes_per_launch": kd["algorithmic_bytes_per_launch"],
                 "ms_per_launch": kd["ms_per_launch"],
                 "timing": "CUDA events around a graph of this kernel's launches for every layer of the step, "
                           "L2 flushed before each replay"}
@@ -662,6 +743,7 @@ def run_csa2(args):
                     "peak_source": f"{peak_kind} copy bandwidth"},
             "phased": phased,
             "kernels": kernels,
+            "multi_query_index": multi,
             "cache_build": build,
             "roofline": roof,
             "gpu_launches": int(seq_launches) * args.steps,

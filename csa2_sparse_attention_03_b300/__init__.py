@@ -76,6 +76,10 @@ def load():
     L.csa2_index_topk_workspace.argtypes = [i32, i32, i32, i32, i32]
     L.csa2_index_topk.restype = i32
     L.csa2_index_topk.argtypes = [i32, C, P, P, i32, i32, i32, P, i32, P, i32, i32, P, P, i32, P, P, sz, P]
+    L.csa2_index_topk_multi_workspace.restype = sz
+    L.csa2_index_topk_multi_workspace.argtypes = [i32, i32, i32]
+    L.csa2_index_topk_multi.restype = i32
+    L.csa2_index_topk_multi.argtypes = [C, P, P, i32, i32, i32, i32, P, i32, i32, i32, P, P, P, sz, P]
     L.csa2_sparse_attn_workspace.restype = sz
     L.csa2_sparse_attn_workspace.argtypes = [i32, i32, i32]
     L.csa2_sparse_attn.restype = i32
@@ -202,6 +206,34 @@ def csa2_index_topk(mode, keys: Cache, q_idx, w, seq_lens, max_seq_len, topk, po
                              _ptr(out_pool), P, _ptr(scores), _ptr(workspace), workspace.numel(),
                              _stream(stream)))
     return out_idx, out_pool, scores
+
+
+def csa2_index_topk_multi_workspace(batch, n_q, max_seq_len) -> int:
+    return int(load().csa2_index_topk_multi_workspace(batch, n_q, max_seq_len))
+
+
+def csa2_index_topk_multi(keys: Cache, q_idx, w, seq_lens, max_seq_len, topk, causal=True, out_idx=None,
+                          with_idx=True, with_scores=False, workspace=None, stream=None):
+    """Many queries per sequence: q_idx [B, n_q, 4, 64], w [B, n_q, 4].
+    Returns (idx [B, n_q, topk] or None, scores [B, n_q, max_seq_len] or None)."""
+    import torch
+    L = load()
+    B, nq = q_idx.shape[0], q_idx.shape[1]
+    dev = q_idx.device
+    if with_idx and out_idx is None:
+        out_idx = torch.empty((B, nq, topk), dtype=torch.int32, device=dev)
+    if not with_idx:
+        out_idx = None
+    scores = None
+    if with_scores:
+        scores = torch.full((B, nq, max_seq_len), float("nan"), dtype=torch.float32, device=dev)
+    need = L.csa2_index_topk_multi_workspace(B, nq, max_seq_len)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    _check(L.csa2_index_topk_multi(keys.ref, _ptr(q_idx), _ptr(w), B, nq, q_idx.shape[2], q_idx.shape[3],
+                                   _ptr(seq_lens), max_seq_len, 1 if causal else 0, topk, _ptr(out_idx),
+                                   _ptr(scores), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_idx, scores
 
 
 def csa2_sparse_attn(kv, swa, q, seq_lens, max_seq_len, idx, topk, swa_window, out=None, lse=None,

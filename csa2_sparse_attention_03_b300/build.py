@@ -9,7 +9,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcsa2.so")
-SOURCES = ["quantize.cu", "index_topk.cu", "index_fused.cu", "attention.cu", "capi.cu", "noalloc.cu", "plan.cu"]
+SOURCES = ["quantize.cu", "index_topk.cu", "index_fused.cu", "index_multi.cu", "attention.cu", "capi.cu", "noalloc.cu", "plan.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]

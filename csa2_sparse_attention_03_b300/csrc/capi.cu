@@ -472,6 +472,39 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
     return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "index launch");
 }
 
+size_t csa2_index_topk_multi_workspace(int32_t batch, int32_t n_q, int32_t max_seq_len)
+{
+    if (batch <= 0 || n_q <= 0 || max_seq_len < 1 || (int64_t)batch * n_q > 65535) return 0;
+    return index_multi_bytes(batch, n_q, max_seq_len);
+}
+
+csa2_status csa2_index_topk_multi(const csa2_cache *keys, const float *q_idx, const float *w, int32_t batch,
+                                  int32_t n_q, int32_t n_heads, int32_t head_dim, const int32_t *seq_lens,
+                                  int32_t max_seq_len, int32_t causal, int32_t topk, int32_t *out_idx,
+                                  float *out_scores, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (n_heads != kIdxHeads || head_dim != kIdxDim)
+        return fail(CSA2_ERR_UNSUPPORTED, "indexer must be 4 heads x 64 channels (got %d x %d)", n_heads, head_dim);
+    if (batch <= 0 || n_q <= 0 || n_q > 4096 || (int64_t)batch * n_q > 65535)
+        return fail(CSA2_ERR_INVALID_ARG, "need batch >= 1, n_q in [1, 4096] and batch * n_q <= 65535");
+    if (max_seq_len < 1 || max_seq_len > (1 << 24)) return fail(CSA2_ERR_INVALID_ARG, "max_seq_len must be in [1, 2^24]");
+    if (causal != 0 && causal != 1) return fail(CSA2_ERR_INVALID_ARG, "causal must be 0 or 1");
+    if (!q_idx || !w || !seq_lens) return fail(CSA2_ERR_INVALID_ARG, "q_idx, w, seq_lens are required");
+    if (!out_idx && !out_scores) return fail(CSA2_ERR_INVALID_ARG, "nothing to compute: out_idx and out_scores are NULL");
+    if (out_idx && (topk < 1 || topk > 65536)) return fail(CSA2_ERR_INVALID_ARG, "topk must be in [1, 65536]");
+    if (!aligned(q_idx, 16)) return fail(CSA2_ERR_INVALID_ARG, "q_idx must be 16-byte aligned");
+    csa2_status st = check_cache(keys, CSA2_FMT_FP4_IDX, batch, max_seq_len, "keys");
+    if (st) return st;
+    st = check_ws(workspace, workspace_bytes, index_multi_bytes(batch, n_q, max_seq_len));
+    if (st) return st;
+    int *fp = flags_ptr();
+    if (!fp) return fail(CSA2_ERR_CUDA, "no CUDA device");
+    cudaError_t e = run_index_multi(view_of(*keys), q_idx, w, batch, n_q, seq_lens, max_seq_len, causal, topk, out_idx,
+                                    out_scores, static_cast<uint8_t *>(workspace), fp,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CSA2_OK : cuda_fail(e, "multi-query index launch");
+}
+
 size_t csa2_sparse_attn_workspace(int32_t batch, int32_t topk, int32_t swa_window)
 {
     return csa2::sparse_attn_workspace_within(batch, topk, swa_window, SIZE_MAX);

@@ -98,6 +98,17 @@ size_t select_bytes(int n_rows, int64_t cand_cap, int max_seq_len);
 size_t select_hist_bytes(int n_rows);  // the leading part of the region to zero before a scan
 SelectBufs carve_select(uint8_t *base, int n_rows, int64_t cand_cap, int max_seq_len);
 
+// ---- step 2, many queries per sequence: tensor-core scoring + Top-K --------
+// Workspace of run_index_multi: the selection rows (batch * n_q of them) and
+// their candidate counts.
+size_t index_multi_bytes(int batch, int n_q, int max_seq_len);
+// Scores every query row against its candidates (its causal prefix when
+// `causal`, else every position < seq_lens[b]) and, when out_idx is given,
+// selects each row's Top-K (two launches, plus a memset of the histograms).
+cudaError_t run_index_multi(const CacheView &keys, const float *q_idx, const float *w, int batch, int n_q,
+                            const int32_t *seq_lens, int max_seq_len, int causal, int topk, int32_t *out_idx,
+                            float *out_scores, uint8_t *ws, int *flags, cudaStream_t stream);
+
 // ---- step 2, fused: scan + Top-K in one co-resident launch ------------------
 struct FusedJobDesc {
     CacheView keys;

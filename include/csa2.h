@@ -164,6 +164,43 @@ csa2_status csa2_index_topk(int32_t mode, const csa2_cache *keys, const float *q
                             float *out_scores, void *workspace, size_t workspace_bytes,
                             void *stream);
 
+/* ---- step 2 with many queries per sequence ----------------------------- */
+/* Several tokens of one sequence index at once: a speculative verification
+ * ([HC] "10 · other changes": DSpark checks drafted tokens together) or a
+ * chunk of prefill ([HC] "03 · CSA2": the Reuse layers' kernel path in
+ * prefill).  Query row i of sequence b is scored exactly as
+ * csa2_index_topk(CSA2_MODE_FULL) scores one query (same quantisation, same
+ * fp32 rounding points, bit-identical scores and index sets) over its
+ * candidates: with causal = 1 the positions 0 .. L_b - n_q + i (the n_q
+ * queries are the sequence's last n_q tokens, L_b = seq_lens[b]; rows with
+ * no position have no candidates), with causal = 0 every position < L_b.
+ * The scores are a dense contraction here, computed on the tensor cores
+ * (tcgen05 kind::f16, one MMA per 16-channel block with the E4M3 scales
+ * folded exactly into the fp16 operands; the epilogue adds the blocks in the
+ * fixed order).
+ *   keys        FP4_IDX cache holding positions 0..seq_lens[b]-1
+ *   q_idx, w    device fp32 [batch][n_q][4][64] (16-byte aligned), [batch][n_q][4]
+ *   seq_lens    device int32 [batch], each in [0, max_seq_len]
+ *   causal      1: row i sees its causal prefix; 0: every position
+ *   out_idx     device int32 [batch][n_q][topk]: ascending positions of the
+ *               row's Top-K (order: score desc, position asc), -1 padded; or
+ *               NULL (scores only, topk ignored)
+ *   out_scores  optional device fp32 [batch][n_q][max_seq_len], written at
+ *               the row's candidate positions only
+ * Limits: n_q in [1, 4096], batch * n_q <= 65535, topk in [1, 65536],
+ * max_seq_len <= 2^24; at least one of out_idx, out_scores.
+ * Workspace: csa2_index_topk_multi_workspace() bytes, 256-byte aligned
+ * (batch * n_q * (max_seq_len rounded up to 64) * 4 B of selection keys plus
+ * 8 KB of histogram per row); the call zeroes what it needs.
+ * Launches: a memset, the scoring kernel, and (with out_idx) the cluster
+ * select. */
+size_t csa2_index_topk_multi_workspace(int32_t batch, int32_t n_q, int32_t max_seq_len);
+csa2_status csa2_index_topk_multi(const csa2_cache *keys, const float *q_idx, const float *w,
+                                  int32_t batch, int32_t n_q, int32_t n_heads, int32_t head_dim,
+                                  const int32_t *seq_lens, int32_t max_seq_len, int32_t causal,
+                                  int32_t topk, int32_t *out_idx, float *out_scores,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---- step 3: gather + dequantise + sparse attention with the SWA branch - */
 /* [LB] "Share the cache and the search work": the selected global entries
  * beside the local 128-token window; [HC] "04 · FP4": FP4 global rows, FP8

@@ -236,6 +236,26 @@ def topk(scores: np.ndarray, positions: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def index_topk_multi(q_idx: np.ndarray, w: np.ndarray, k_codes: np.ndarray, k_scales: np.ndarray, L: int,
+                     K: int, causal: bool = True):
+    """Several indexer queries of one sequence ([HC] "10 · other changes": a
+    speculative verification checks several drafted tokens together; [HC]
+    "03 · CSA2": the indexing path also runs in prefill): q_idx [n_q, Hi, Di],
+    w [n_q, Hi], keys of positions 0..L-1.  Query row i is an ordinary indexer
+    query whose candidates are its causal prefix 0 .. L - n_q + i (the queries
+    are the sequence's last n_q tokens), or every position < L when not
+    causal.  Returns (scores: list of per-row fp32 arrays over the row's
+    candidates, idx [n_q, K] ascending positions, -1 padded)."""
+    n_q = q_idx.shape[0]
+    scores, idx = [], np.full((n_q, K), -1, np.int32)
+    for i in range(n_q):
+        n = max(0, min(L, L - n_q + i + 1)) if causal else L
+        s = index_scores(q_idx[i], w[i], k_codes[:n], k_scales[:n]) if n else np.zeros(0, np.float32)
+        scores.append(s)
+        idx[i] = topk(s, np.arange(n, dtype=np.int32), K)
+    return scores, idx
+
+
 def attend(q: np.ndarray, rows: np.ndarray):
     """q [H, D] fp32, rows [n, D] fp64 -> (out [H, D] fp64, lse [H] fp64)."""
     q = np.ascontiguousarray(q, np.float32)

@@ -62,3 +62,24 @@ def test_launch_bytes_l131072():
     assert bench.attention_launch_bytes(w, reuse) == K * KV + W * SWA + Q + OUT + LSE + K * 4
     full = w.layers[0]
     assert bench.index_launch_bytes(w, full) == L * IDX + IDXQ + K * 4 + 512 * 4 + KV + 64 * 4 + IDX
+
+
+def test_traffic_record_is_read_only_for_unchanged_kernel_sources(tmp_path):
+    """roofline.traffic comes from a committed ncu summary line, and is null
+    once the kernel's sources differ from those the counters were taken on."""
+    import bench
+
+    sha = bench.kernel_source_sha16("attn_kernel")
+    wl = "B1 L131072 40-layer 4F/4R/30U/2S K2048"
+    (tmp_path / "a.md").write_text(
+        "some text\n"
+        f"traffic-record: kernel=attn_kernel workload={wl.replace(' ', '_')} launches=40 "
+        f"dram_bytes_per_launch=123456.5 source_sha16={sha}\n")
+    v, src = bench.recorded_traffic("attn_kernel", wl, str(tmp_path))
+    assert v == 123456.5 and src.endswith("a.md")
+    assert bench.recorded_traffic("attn_kernel", "another workload", str(tmp_path)) == (None, None)
+    (tmp_path / "a.md").write_text(
+        f"traffic-record: kernel=attn_kernel workload={wl.replace(' ', '_')} launches=40 "
+        "dram_bytes_per_launch=1 source_sha16=0000000000000000\n")
+    v, src = bench.recorded_traffic("attn_kernel", wl, str(tmp_path))
+    assert v is None and "changed" in src

@@ -364,6 +364,30 @@ def test_topk_ties_take_lower_positions(orc):
     assert orc.topk(scores, pos, 5).tolist() == [0, 1, 2, 3, 5]
 
 
+@pytest.mark.parametrize("L,n_q,K,causal", [(40, 6, 5, True), (40, 6, 5, False), (7, 12, 3, True), (1, 1, 2, True)])
+def test_multi_query_rows_brute_force(orc, L, n_q, K, causal):
+    """Each query row of a multi-query call is an ordinary indexer query over
+    its candidates: the causal prefix 0 .. L - n_q + i (rows before position 0
+    have none), or all L positions.  Scores per key from the single-query
+    function (pinned above); masks and selection by brute force."""
+    x = synth.normal_rows(5, "mqk", (L,), 0, L, 64)
+    kc, ks = orc.quant_fp4(x)
+    q = synth.normal_rows(5, "mqq", (n_q,), 0, n_q * 4, 64, scale=0.125).reshape(n_q, 4, 64)
+    w = synth.uniform(5, "mqw", (n_q,), (n_q, 4)).astype(np.float32)
+    scores, idx = orc.index_topk_multi(q, w, kc, ks, L, K, causal)
+    for i in range(n_q):
+        full = orc.index_scores(q[i], w[i], kc, ks)
+        last = (L - n_q + i) if causal else (L - 1)
+        n = max(0, last + 1)
+        assert scores[i].shape == (n,)
+        assert np.array_equal(scores[i].view(np.uint32), full[:n].view(np.uint32))
+        assert idx[i].tolist() == _brute_topk(full[:n], np.arange(n, dtype=np.int32), K), i
+    if causal and n_q <= L:
+        # the last row sees every position: the single-query call over all L
+        assert idx[-1].tolist() == orc.topk(orc.index_scores(q[-1], w[-1], kc, ks),
+                                            np.arange(L, dtype=np.int32), K).tolist()
+
+
 # ---------------------------------------------------------------- attention
 
 def _dense(q, rows):
