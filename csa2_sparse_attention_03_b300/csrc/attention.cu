@@ -27,11 +27,16 @@
 // stages its O^T normalised by its own sum, and sends each CTA, by one bulk
 // copy, its block of that CTA's slice of the channels; each CTA weighs and
 // sums its slice over the cluster and writes it.  When one (unit,
-// sequence) has more tiles than a cluster takes well, it is split over
-// several clusters, each a contiguous part of the tiles: each writes its
-// merged partial (max, sum, normalised output) to the workspace, and the last
-// cluster to finish (a ticket counter, left zero again) merges the parts the
-// same way.  With no workspace every (unit, sequence) is one cluster.
+// sequence) has more tiles than a cluster takes well, it is split over two
+// clusters, the tiles dealt round-robin over all their CTAs: the second
+// cluster's CTAs (satellites) skip the cluster merge and write their partial
+// (max, sum, normalised output) to the workspace, then count themselves into
+// a counter per owner of a channel slice of the first cluster; each owner
+// waits for its counter (bounded, left zero again), and sums the satellites'
+// share of its slice with the cluster's.  A split is only planned when every
+// cluster of the launch fits on the device at once, so the satellites are
+// resident while the owners wait.  With no workspace every (unit, sequence)
+// is one cluster.
 //
 // Value precision: E2M1 x E4M3 values and E4M3 codes x 2^-8 are exact in
 // fp16; an FP8 window row's fp32 scale (x 2^8) multiplies its logit in fp32
@@ -93,19 +98,17 @@ struct AttnParams {
     UnitDev units[kMaxUnits];
     EntryDev entries[kMaxAttnEntries];
     int32_t n_units, batch, topk, window, win_tiles, cs;
-    int32_t split;           // clusters per (unit, sequence); > 1 merges through `parts`
+    int32_t split;           // clusters per (unit, sequence): 1, or 2 (the second one's CTAs are satellites)
     int32_t inputs_ready;    // indices, caches, rings and lengths predate the previous kernel
     const int32_t *seq_lens;
-    float *parts;            // split > 1: [unit][b][part][kPartFloats]
-    uint32_t *tickets;       // split > 1: [unit][b][kMaxCS], zero at launch, left zero
+    float *parts;            // split 2: satellite partials [unit][b][satellite rank < cs][kSatFloats]
+    uint32_t *tickets;       // split 2: satellite counters per owner rank [unit][b][kMaxCS], zero at launch, left zero
 };
 
-// One cluster's merged result in the workspace: per CTA rank a copy of the
-// cluster's (max, sum) per query (each CTA writes its own, so that CTAs need
-// not wait for one another), then the output normalised by that sum,
-// [query][channel] (CTA r writes its slice of the channels).
-constexpr int kHdrFloats = kMaxCS * 2 * 16 * kMaxNL;
-constexpr int kPartFloats = kHdrFloats + 16 * kMaxNL * kDim;
+// One satellite's partial in the workspace: its running maximum and sum per
+// query, then its output normalised by that sum, [query][channel].
+constexpr int kSatHdr = 2 * 16 * kMaxNL;
+constexpr int kSatFloats = kSatHdr + 16 * kMaxNL * kDim;
 
 struct Misc {
     uint32_t vmask[4];               // valid rows of the tile in the buffer
@@ -117,7 +120,9 @@ struct Misc {
     float wall[kMaxCS][16 * kMaxNL];    // merge: every CTA's (or part's) weight per query
     float cm[16 * kMaxNL], cl[16 * kMaxNL];  // merge: the cluster's (max, sum) per query
     float inv_l[16 * kMaxNL];        // merge: 1 / this CTA's sum per query (0 without rows)
-    int32_t last;                    // split: this cluster merges the parts
+    float2 mlsat[kMaxCS][16 * kMaxNL];  // merge: every satellite's (m, l) per query
+    float wsat[kMaxCS][16 * kMaxNL];    // merge: every satellite's final weight per query
+    float w0[16 * kMaxNL];              // merge: the final weight of the cluster's merged result
     float mu[16 * kMaxNL];           // the maximum a tile's weights are taken against
     float alpha[16 * kMaxNL];        // factor moving O^T to that maximum
     __align__(16) uint8_t app[kMaxNL][kDim];  // appended window row per layer slot (E4M3 codes)
@@ -481,21 +486,25 @@ __device__ __forceinline__ void merge_weights(Misc &M, int ns)
     }
 }
 
-// Weighted sums over `ns` sources for this thread's items of one channel
-// slice: item = (query q, four channels), n4 items per query.  For each item,
-// sum_s wgt[s][q] x load(s, q, ch) in source order, every source's load in
-// flight before the first is used.  (The launch shapes the host picks give a
-// thread at most one or two items.)
-template <int NQ, typename Load, typename Store>
-__device__ __forceinline__ void slice_reduce(int ns, int n4, int c_lo, int n_layers, const float (*wgt)[16 * kMaxNL],
-                                             Load load, Store store)
+// Weighted sums for this thread's items of one channel slice: item = (query
+// q, four channels), n4 items per query.  For each item, the cluster's
+// sources in order, sum_k wall[k][q] x load(k, q, ch); with satellites, that
+// sum times w0[q] plus sum_s wsat[s][q] x load_sat(s, q, ch) in order.  Every
+// load is in flight before the first is used (the satellites' global loads
+// first).  (The launch shapes the host picks give a thread one or two items.)
+template <int NQ, typename Load, typename LoadSat, typename Store>
+__device__ __forceinline__ void slice_reduce(int ns, int n_sat, int n4, int c_lo, int n_layers, const Misc &M,
+                                             Load load, LoadSat load_sat, Store store)
 {
     const int total = NQ * n4;
 #pragma unroll 1
     for (int item = threadIdx.x; item < total; item += kThreads) {
         const int q = item / n4, ch = c_lo + 4 * (item % n4);
         if ((q >> 4) >= n_layers) continue;
-        float4 v[kMaxCS];
+        float4 u[kMaxCS], v[kMaxCS];
+#pragma unroll
+        for (int k = 0; k < kMaxCS; ++k)
+            if (k < n_sat) u[k] = load_sat(k, q, ch);
 #pragma unroll
         for (int k = 0; k < kMaxCS; ++k)
             if (k < ns) v[k] = load(k, q, ch);
@@ -503,12 +512,25 @@ __device__ __forceinline__ void slice_reduce(int ns, int n4, int c_lo, int n_lay
 #pragma unroll
         for (int k = 0; k < kMaxCS; ++k)
             if (k < ns) {
-                const float w = wgt[k][q];
+                const float w = M.wall[k][q];
                 acc.x += w * v[k].x;
                 acc.y += w * v[k].y;
                 acc.z += w * v[k].z;
                 acc.w += w * v[k].w;
             }
+        if (n_sat > 0) {
+            const float w0 = M.w0[q];
+            acc = make_float4(w0 * acc.x, w0 * acc.y, w0 * acc.z, w0 * acc.w);
+#pragma unroll
+            for (int k = 0; k < kMaxCS; ++k)
+                if (k < n_sat) {
+                    const float w = M.wsat[k][q];
+                    acc.x += w * u[k].x;
+                    acc.y += w * u[k].y;
+                    acc.z += w * u[k].z;
+                    acc.w += w * u[k].w;
+                }
+        }
         store(q, ch, acc);
     }
 }
@@ -556,10 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     c.b = blockIdx.y;
     c.L = 0;
     c.W = P.window;
-    // this cluster's tiles: a contiguous part of the unit's; this CTA's: every cs-th
-    const int per_part = (U.n_tiles + P.split - 1) / P.split;
-    const int t0 = part * per_part + rank, t_end = min(U.n_tiles, (part + 1) * per_part);
-    const int n_my = t_end > t0 ? (t_end - 1 - t0) / cs + 1 : 0;
+    // this CTA's tiles: every (split cs)-th of the unit's, from its index in
+    // the (unit, sequence): the first cluster's CTAs, then the satellites'
+    const int gc = part * cs + rank, stride = P.split * cs;
+    const int t0 = gc, t_end = U.n_tiles;
+    const int n_my = t_end > t0 ? (t_end - 1 - t0) / stride + 1 : 0;
     const int r = tid & (kRows - 1), h = tid >> 7;
 
     Raw raw;
@@ -568,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         // the length and the positions are independent loads: both in flight at once
         const int32_t Lraw = __ldcg(P.seq_lens + c.b);
         const int32_t pos0 = n_my > 0 ? load_pos(c, t0, r) : -1;
-        if (n_my > 1) pos_next = load_pos(c, t0 + cs, r);
+        if (n_my > 1) pos_next = load_pos(c, t0 + stride, r);
         c.L = max(0, Lraw);
         if (n_my > 0) gather(c, t0, pos0, r, h, raw);
     };
@@ -597,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         dequant(c, tile_is_window(U, t0), r, h, raw, T);
         row_masks(tile_is_window(U, t0));
         if (n_my > 1) {
-            gather(c, t0 + cs, pos_next, r, h, raw);
-            pos_next = n_my > 2 ? load_pos(c, t0 + 2 * cs, r) : -1;
+            gather(c, t0 + stride, pos_next, r, h, raw);
+            pos_next = n_my > 2 ? load_pos(c, t0 + 2 * stride, r) : -1;
         }
     }
     tc::pdl_wait();
@@ -631,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const int j = tid >> 7;
         const EntryDev &E = P.entries[U.entry[j]];
         const int t_app = U.row_tiles + j * P.win_tiles + (P.window - 1) / kRows;
-        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % cs == 0)
+        if (E.new_swa && t_app >= t0 && t_app < t_end && (t_app - t0) % stride == 0)
             append_window_row(c, E, j, tid & 127, pre && t_app == t0, (P.window - 1) % kRows, T);
     }
 
@@ -658,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     constexpr uint32_t kIdescQK = tc::idesc_f16(128, 2 * NQ, false, false);
     constexpr uint32_t kIdescPV = tc::idesc_f16(128, NQ, true, true);
     for (int it = 0; it < n_my; ++it) {
-        const int tile = t0 + it * cs;
+        const int tile = t0 + it * stride;
         const bool window = tile_is_window(U, tile);
         if (it > 0 || !pre) {
             if (it > 0 && tid == 0 && !tc::mbar_wait(&M.bar_pv, (it - 1) & 1)) M.ok = 0;  // tile and P buffers free
@@ -667,8 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
             dequant(c, window, r, h, raw, T);
             row_masks(window);
             if (it + 1 < n_my) {  // in flight during this tile
-                gather(c, tile + cs, pos_next, r, h, raw);
-                pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * cs, r) : -1;
+                gather(c, tile + stride, pos_next, r, h, raw);
+                pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * stride, r) : -1;
             }
         }
         tc::fence_async_smem();
@@ -711,9 +734,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     if (tid < NQ) M.inv_l[tid] = M.l_run[tid] > 0.0f ? 1.0f / M.l_run[tid] : 0.0f;
     __syncthreads();
 
+    // ---- a satellite (a CTA of the second cluster of a split (unit,
+    // sequence)) hands its partial to the first cluster through the
+    // workspace: its running (max, sum) per query and O^T normalised by that
+    // sum, then one counter increment per owner of a channel slice
+    if (part > 0) {
+        if (n_my > 0) {
+            float *rec = P.parts + (((int64_t)unit * P.batch + c.b) * cs + rank) * (int64_t)kSatFloats;
+            if (tid < NQ) {
+                rec[tid] = M.m_run[tid];
+                rec[16 * kMaxNL + tid] = M.l_run[tid];
+            }
+            const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32 quad.., column half
+            const int ch_in = 32 * quad + lane;
+#pragma unroll 1
+            for (int c0 = half * 32 * NL; c0 < (half + 1) * 32 * NL; c0 += 32) {
+                float o[32];
+                tc::tmem_ld32(tc::taddr(tmem, 32u * quad, Cols<NL>::O + c0), o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = c0 + i, q = col % NQ;
+                    rec[kSatHdr + q * kDim + 128 * (col / NQ) + ch_in] = o[i] * M.inv_l[q];
+                }
+            }
+            tc::fence_before_sync();
+            __syncthreads();  // the record is written
+            if (tid < cs) {
+                __threadfence();
+                atomicAdd(P.tickets + ((int64_t)unit * P.batch + c.b) * kMaxCS + tid, 1u);
+            }
+        }
+        if (warp == 0) {
+            tc::fence_after_sync();
+            tc::tmem_dealloc(tmem, Cols<NL>::alloc);
+        }
+        tc::cluster_wait();  // pairs with the prologue's arrival
+        return;
+    }
+
     // ---- merge across the cluster: every CTA stages its output normalised by its
     // own sum, with its (max, sum); one cluster barrier; each CTA then weighs
-    // and sums one slice of the channels over the cluster
+    // and sums one slice of the channels over the cluster (and over the
+    // satellites' partials of that slice, when the (unit, sequence) is split)
     // channel slices: CTA r owns channels [r cpc, min(512, (r + 1) cpc))
     const int cpc = ((kDim + cs - 1) / cs + 3) & ~3;
     const int c_lo = rank * cpc, c_hi = min(kDim, c_lo + cpc);
@@ -767,80 +829,74 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                         tc::mapa(tc::smem_u32(&M.bar_rx), (uint32_t)tid));
     }
     merge_weights<NQ>(M, cs);
+    // the satellites with a tile wrote their partials while this cluster was
+    // still computing: wait (bounded) for this slice's counter
+    const int n_sat = P.split > 1 ? max(0, min(cs, U.n_tiles - cs)) : 0;
+    const float *sat = n_sat > 0 ? P.parts + ((int64_t)unit * P.batch + c.b) * cs * (int64_t)kSatFloats : nullptr;
+    if (n_sat > 0 && tid == 0) {
+        uint32_t *cnt = P.tickets + ((int64_t)unit * P.batch + c.b) * kMaxCS + rank;
+        bool got = false;
+        for (uint32_t i = 0; i < tc::kWaitLimit && !got; ++i) got = tc::ld_acquire_gpu(cnt) >= (uint32_t)n_sat;
+        if (got) {
+            *cnt = 0u;  // only this CTA reads it: left zero for the next launch
+        } else {
+            M.ok = 0;
+        }
+    }
     if (!tc::mbar_wait(&M.bar_rx, 0)) {
         M.ok = 0;
         tc::mbar_wait(&M.bar_rx, 0);  // a last chance for the copies in flight
     }
     __syncthreads();
     if (tid == 0 && !M.ok) raise_flag(flags, kFlagTimeout);
-    float *part_rec = P.split > 1
-                          ? P.parts + (((int64_t)unit * P.batch + c.b) * P.split + part) * (int64_t)kPartFloats
-                          : nullptr;
-    {
-        slice_reduce<NQ>(
-            cs, n4, c_lo, U.n_layers, M.wall,
-            [&](int src, int q, int ch) {
-                return *reinterpret_cast<const float4 *>(recv + (src * NQ + q) * cpc + (ch - c_lo));
-            },
-            [&](int q, int ch, float4 acc) {
-                float *dst = part_rec ? part_rec + kHdrFloats + q * kDim + ch
-                                      : P.entries[U.entry[q >> 4]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim + ch;
-                *reinterpret_cast<float4 *>(dst) = acc;
-            });
-        if (tid < NQ && part_rec) {
-            part_rec[rank * 32 * kMaxNL + tid] = M.cm[tid];
-            part_rec[rank * 32 * kMaxNL + 16 * kMaxNL + tid] = M.cl[tid];
-        }
-        if (tid < NQ && rank == 0 && !part_rec) {
-            const int q = tid, j = q >> 4;
-            if (j < U.n_layers && P.entries[U.entry[j]].lse) {
-                P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] =
-                    M.cl[q] > 0.0f ? M.cm[q] + logf(M.cl[q]) : -INFINITY;
-            }
-        }
-    }
-    if (P.split > 1) {
-        // the parts of each channel slice meet through a ticket per (unit,
-        // sequence, CTA rank): the CTA that arrives last for its slice sums
-        // the parts' slices and writes the output
-        __syncthreads();  // this CTA's slice and header copy are written
-        if (tid == 0) {
-            __threadfence();
-            uint32_t *tk = P.tickets + ((int64_t)unit * P.batch + c.b) * kMaxCS + rank;
-            const uint32_t t = atomicAdd(tk, 1u);
-            M.last = (t == (uint32_t)P.split - 1) ? 1 : 0;
-            if (M.last) {
-                atomicExch(tk, 0u);  // every part has arrived: leave it zero
-                __threadfence();
-            }
+    if (n_sat > 0) {
+        // every satellite's (m, l); the cluster's merged (max, sum) is one more
+        // source: the final weights of the cluster's CTAs are their cluster
+        // weights times w0, a satellite's its own
+        for (int i = tid; i < n_sat * NQ; i += kThreads) {
+            const int sidx = i / NQ, q = i % NQ;
+            const float *rec = sat + (int64_t)sidx * kSatFloats;
+            M.mlsat[sidx][q] = make_float2(__ldcg(rec + q), __ldcg(rec + 16 * kMaxNL + q));
         }
         __syncthreads();
-        const int last = M.last;
-        if (last) {
-            __threadfence();
-            const float *base = P.parts + ((int64_t)unit * P.batch + c.b) * P.split * (int64_t)kPartFloats;
-            // every part's (m, l) of every query, all loads at once
-            for (int i = tid; i < P.split * NQ; i += kThreads) {
-                const int p2 = i / NQ, q = i % NQ;
-                const float *rec = base + (int64_t)p2 * kPartFloats;
-                M.mlall[p2][q] = make_float2(__ldcg(rec + rank * 32 * kMaxNL + q), __ldcg(rec + rank * 32 * kMaxNL + 16 * kMaxNL + q));
+        if (tid < NQ) {
+            const int q = tid;
+            float mx = M.cl[q] > 0.0f ? M.cm[q] : -INFINITY;
+            for (int k = 0; k < n_sat; ++k)
+                if (M.mlsat[k][q].y > 0.0f) mx = fmaxf(mx, M.mlsat[k][q].x);
+            const float w0 = M.cl[q] > 0.0f ? M.cl[q] * __expf(M.cm[q] - mx) : 0.0f;
+            float tot = w0;
+            for (int k = 0; k < n_sat; ++k) {
+                const float2 ml = M.mlsat[k][q];
+                const float e = ml.y > 0.0f ? ml.y * __expf(ml.x - mx) : 0.0f;
+                M.wsat[k][q] = e;
+                tot += e;
             }
-            __syncthreads();
-            merge_weights<NQ>(M, P.split);
-            __syncthreads();
-            if (tid < NQ && rank == 0 && (tid >> 4) < U.n_layers && P.entries[U.entry[tid >> 4]].lse)
-                P.entries[U.entry[tid >> 4]].lse[(int64_t)c.b * kHeads + (tid & 15)] =
-                    M.cl[tid] > 0.0f ? M.cm[tid] + logf(M.cl[tid]) : -INFINITY;
-            slice_reduce<NQ>(
-                P.split, n4, c_lo, U.n_layers, M.wall,
-                [&](int src, int q, int ch) {
-                    return __ldcg(reinterpret_cast<const float4 *>(base + (int64_t)src * kPartFloats + kHdrFloats + q * kDim +
-                                                                   ch));
-                },
-                [&](int q, int ch, float4 acc) {
-                    *reinterpret_cast<float4 *>(P.entries[U.entry[q >> 4]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim +
-                                                ch) = acc;
-                });
+            const float inv = tot > 0.0f ? 1.0f / tot : 0.0f;
+            for (int k = 0; k < n_sat; ++k) M.wsat[k][q] *= inv;
+            M.w0[q] = w0 * inv;
+            M.cm[q] = mx;
+            M.cl[q] = tot;
+        }
+        __syncthreads();
+    }
+    slice_reduce<NQ>(
+        cs, n_sat, n4, c_lo, U.n_layers, M,
+        [&](int src, int q, int ch) {
+            return *reinterpret_cast<const float4 *>(recv + (src * NQ + q) * cpc + (ch - c_lo));
+        },
+        [&](int sidx, int q, int ch) {
+            return __ldcg(reinterpret_cast<const float4 *>(sat + (int64_t)sidx * kSatFloats + kSatHdr + q * kDim + ch));
+        },
+        [&](int q, int ch, float4 acc) {
+            *reinterpret_cast<float4 *>(P.entries[U.entry[q >> 4]].out + ((int64_t)c.b * kHeads + (q & 15)) * kDim +
+                                        ch) = acc;
+        });
+    if (tid < NQ && rank == 0) {
+        const int q = tid, j = q >> 4;
+        if (j < U.n_layers && P.entries[U.entry[j]].lse) {
+            P.entries[U.entry[j]].lse[(int64_t)c.b * kHeads + (q & 15)] =
+                M.cl[q] > 0.0f ? M.cm[q] + logf(M.cl[q]) : -INFINITY;
         }
     }
     tc::cluster_sync();  // no CTA leaves while another reads its shared memory
@@ -932,42 +988,46 @@ struct Shape {
     size_t ws = 0;
 };
 
-// Workspace of a launch that splits each (unit, sequence) over `split` clusters.
-size_t split_bytes(int n_units, int batch, int split)
+// Workspace of a launch that splits each (unit, sequence) over two clusters
+// of `cs`: a partial per satellite and a counter per owner rank.
+size_t split_bytes(int n_units, int batch, int split, int cs)
 {
     if (split <= 1) return 0;
     auto r256 = [](size_t n) { return (n + 255) & ~(size_t)255; };
     const size_t groups = (size_t)n_units * batch;
-    return r256(groups * split * kPartFloats * sizeof(float)) + r256(groups * kMaxCS * sizeof(uint32_t));
+    return r256(groups * cs * kSatFloats * sizeof(float)) + r256(groups * kMaxCS * sizeof(uint32_t));
 }
 
 // Launch shape: the (split, cluster size) with the lowest modelled time whose
 // workspace fits `budget`.  A cluster costs a fixed part (queries in, merge),
-// its busiest CTA's tiles and a little per CTA; a split adds the partials'
-// round trip through global memory and, per part, the last arrival's reads;
-// clusters run `active` at a time.  Costs are in microseconds, from global-
-// timer stamps of the L = 131,072 step on B300: a tile's tensor-core work
-// alone is 64 MMAs at about 46 cycles each, so a CTA's second tile costs
-// about 4 us of dequantisation, products and softmax.
+// its busiest CTA's tiles and a little per CTA; clusters run `active` at a
+// time.  A split (two clusters per (unit, sequence), the second one's CTAs
+// handing their partials to the first through the workspace) adds the
+// satellites' reads to the merge; the first cluster waits for the second, so
+// a split is only planned when every cluster of the launch fits on the
+// device at once.  Costs are in microseconds, from global-timer stamps of the
+// L = 131,072 step on B300: a tile's tensor-core work alone is 64 MMAs at
+// about 46 cycles each, so a CTA's second tile costs about 4 us of
+// dequantisation, products and softmax.
 template <int NL>
 Shape choose_shape(int dev, int max_tiles, int n_groups, size_t budget)
 {
-    constexpr double kFixed = 6.0, kPerTile = 4.0, kPerCta = 0.05, kSplit = 2.5, kPerPart = 0.3;
+    constexpr double kFixed = 6.0, kPerTile = 4.0, kPerCta = 0.05, kSat = 1.0;
     Shape best;
     double best_cost = 1e300;
-    for (int split = 1; split <= kMaxCS; ++split) {
+    for (int split = 1; split <= 2; ++split) {
         if (split > 1 && split > max_tiles) break;
-        const size_t ws = split_bytes(1, n_groups, split);
-        if (ws > budget) continue;
         const int tiles = (max_tiles + split - 1) / split;
         for (int cs = 1; cs <= kMaxCS; ++cs) {
             if (cs > 1 && cs > tiles) break;
+            const size_t ws = split_bytes(1, n_groups, split, cs);
+            if (ws > budget) continue;
             const int act = active_clusters<NL>(dev, cs);
             if (act <= 0) continue;
-            const int per = (tiles + cs - 1) / cs;
+            if (split > 1 && (int64_t)n_groups * split > act) continue;  // one wave: the satellites are resident
+            const int per = (max_tiles + split * cs - 1) / (split * cs);
             const double waves = std::ceil((double)n_groups * split / act);
-            const double cost =
-                waves * (kFixed + kPerTile * per + kPerCta * cs) + (split > 1 ? kSplit + kPerPart * split : 0.0);
+            const double cost = waves * (kFixed + kPerTile * per + kPerCta * cs) + (split > 1 ? kSat : 0.0);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best.split = split;
@@ -994,7 +1054,7 @@ cudaError_t launch_nl(AttnParams &p, int max_tiles, const AttnPlan &plan, int *f
         uint8_t *ws = static_cast<uint8_t *>(plan.workspace);
         const size_t groups = (size_t)p.n_units * plan.batch;
         p.parts = reinterpret_cast<float *>(ws);
-        p.tickets = reinterpret_cast<uint32_t *>(ws + (((groups * sh.split * kPartFloats * sizeof(float)) + 255) &
+        p.tickets = reinterpret_cast<uint32_t *>(ws + (((groups * sh.cs * kSatFloats * sizeof(float)) + 255) &
                                                       ~(size_t)255));
     }
     log_plan("attention NL=%d: %d units x %d sequences, %d tiles at most, %d cluster(s) of %d each (%d fit at once)",
@@ -1074,7 +1134,7 @@ size_t attn_workspace_bytes(const AttnPlan &plan, size_t budget)
     if ((nl == 1 ? prepare_kernel<1>(dev) : prepare_kernel<2>(dev)) != cudaSuccess) return 0;
     const Shape sh = nl == 1 ? choose_shape<1>(dev, std::max(1, max_tiles), p.n_units * plan.batch, budget)
                              : choose_shape<2>(dev, std::max(1, max_tiles), p.n_units * plan.batch, budget);
-    return split_bytes(p.n_units, plan.batch, sh.split);
+    return split_bytes(p.n_units, plan.batch, sh.split, sh.cs);
 }
 
 cudaError_t launch_attention(const AttnPlan &plan, int *flags, cudaStream_t stream, cudaEvent_t mid_event)

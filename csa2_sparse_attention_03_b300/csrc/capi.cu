@@ -200,6 +200,7 @@ struct IdxJob {
     float *out_scores[2];
     const csa2_cache *kv;    // appends of a Full layer
     const float *new_kv, *new_key;
+    const csa2_cache *warm;  // main-KV cache the selected rows are gathered from next, or null
 };
 
 int64_t level_max_cand(const IdxJob *jobs, int n_jobs, int max_seq_len)
@@ -259,6 +260,10 @@ cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int bat
                 D.new_kv = J.new_kv;
             }
             D.new_key = J.new_key;
+            if (J.warm) {
+                D.warm = view_of(*J.warm);
+                D.has_warm = 1;
+            }
         }
         FusedLaunch L;
         L.jobs = d.data();
@@ -693,6 +698,7 @@ void add_index_job(const csa2_layer_desc *layers, int l, int32_t pool_len, std::
         j.new_kv = d.new_kv;
         j.new_key = d.new_idx_key;
     }
+    j.warm = layers[f].kv;  // every query of the job gathers from the keys' Full layer
     jobs.push_back(j);
 }
 

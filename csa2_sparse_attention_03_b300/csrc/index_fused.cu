@@ -39,6 +39,9 @@
 // group barriers are bounded spins that raise the timeout flag when they
 // give up.  The Full layer's appended main-KV row and indexer key (position
 // L-1) are quantised here, the key patched into the scanning CTA's copy.
+// Inside a decode step each winner's main-KV row is brought into L2 as its
+// index is written: the attention launch that follows gathers those rows
+// right after its wait for this kernel.
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -277,6 +280,20 @@ __device__ __forceinline__ void group_barrier(uint32_t *bar, uint32_t target, ui
 __device__ __forceinline__ uint32_t prefix_of(uint32_t key, int nb) { return nb >= 32 ? key : key >> (32 - nb); }
 
 // ---- the kernel ------------------------------------------------------------------------
+
+// Brings the main-KV row of (sequence b, position pos) into L2: the attention
+// launch that follows gathers it, and its gather waits on the index kernel.
+__device__ __forceinline__ void warm_row(const CacheView &kv, int b, int32_t pos)
+{
+    if (pos < 0) return;
+    const int64_t slot = slot_of(kv, b, pos);
+    if (slot < 0) return;
+    const uint8_t *row = kv.data + slot * kKvRow;
+    tc::prefetch_l2(row);
+    tc::prefetch_l2(row + 128);
+    tc::prefetch_l2(row + 256);
+    tc::prefetch_l2(row + kKvRow - 1);
+}
 
 __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_constant__ FusedParams P, int *flags)
 {
@@ -713,7 +730,11 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
                     const uint32_t sm = __ballot_sync(0xFFFFFFFFu, sel);
                     if (sel) {
                         const uint32_t at = sel_before + written + __popc(sm & lt);
-                        if (at < K) out[at] = direct ? (int32_t)(c0 + i) : __ldcg(pool + c0 + i);
+                        if (at < K) {
+                            const int32_t pos = direct ? (int32_t)(c0 + i) : __ldcg(pool + c0 + i);
+                            out[at] = pos;
+                            if (tg == 0 && job.has_warm) warm_row(job.warm, b, pos);
+                        }
                     }
                     written += __popc(sm);
                     ties_seen += __popc(tm);
@@ -944,6 +965,8 @@ cudaError_t launch_fused(const FusedLaunch &L, const FusedPlan &fp, int *flags, 
         J.kv = d.kv;
         J.new_kv = d.new_kv;
         J.new_key = d.new_key;
+        J.warm = d.warm;
+        J.has_warm = d.has_warm;
     }
     p.seq_lens = L.seq_lens;
     p.state = L.state;

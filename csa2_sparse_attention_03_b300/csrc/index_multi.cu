@@ -28,7 +28,7 @@
 // gridDim.x-th tile of 128 keys.  Per tile: two 64-key tiles by bulk copy
 // (double-buffered), unpacked to fp16 core matrices (A: 128 keys x 64
 // channels), four MMAs (M = 128 keys, N = 4 heads x 32 queries, K = 16) into
-// 512 tensor-memory columns, then the epilogue: thread = key x 16 queries.  The
+// 512 tensor-memory columns, then the epilogue: thread = key x 8 queries.  The
 // epilogue writes each query row's order-preserving keys (0 = not a
 // candidate) and adds them to a shared 2,048-bin histogram of 16-bit counts,
 // added into the row's global histogram at the end; the cluster radix select
@@ -43,7 +43,7 @@
 namespace csa2 {
 namespace {
 
-constexpr int kMqThreads = 256;
+constexpr int kMqThreads = 512;                       // 16 warps: the epilogue is latency-bound
 constexpr int kMqKeys = 128;                          // keys per tile: the MMA's M
 constexpr int kMqQueries = 32;                        // queries per CTA
 constexpr int kMqN = kIdxHeads * kMqQueries;          // 128 B rows: (head, query)
@@ -87,33 +87,26 @@ __device__ __forceinline__ uint32_t cm64(int row, int k)
     return (uint32_t)((row >> 3) * 1024 + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2);
 }
 
-// Four loads of 16 consecutive columns of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, float (&v)[4][16])
+// Four loads of 8 consecutive columns of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld8x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, float (&v)[4][8])
 {
-    uint32_t r[64];
+    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%64];\n"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
-        "[%65];\n"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, "
-        "[%66];\n"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, "
-        "[%67];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n"
         "tcgen05.wait::ld.sync.aligned;\n"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
         : "memory");
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[j][i] = __uint_as_float(r[16 * j + i]);
+        for (int i = 0; i < 8; ++i) v[j][i] = __uint_as_float(r[8 * j + i]);
 }
 
 __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_constant__ MqParams P, int *flags)
@@ -220,7 +213,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
     if (tid == 0 && n_my > 0) issue(0);
 
     constexpr uint32_t kIdesc = tc::idesc_f16(kMqKeys, kMqN, false, false);
-    const int quad = warp & 3, qh = warp >> 2;  // lanes 32 quad.., queries 16 qh..
+    const int quad = warp & 3, qo = warp >> 2;  // lanes 32 quad.., queries 8 qo..
     const int r = 32 * quad + lane;             // this thread's key in the tile
     uint32_t ok = 1;
 #pragma unroll 1
@@ -231,9 +224,10 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
             ok = 0;
             tc::mbar_wait(&S.bar_ld[s], (uint32_t)(k >> 1) & 1u);  // a last chance for copies in flight
         }
-        // keys -> fp16: item = (key, block); sk * e2m1 is exact in fp16
+        // keys -> fp16: item = (key, block), eight consecutive keys per block
+        // in a quarter warp (conflict-free 16-B stores); sk * e2m1 is exact in fp16
         for (int item = tid; item < kMqKeys * kMqBlocks; item += kMqThreads) {
-            const int kr = item >> 2, j = item & 3, hf = kr >> 6, rr = kr & 63;
+            const int kr = (item & 7) | ((item >> 5) << 3), j = (item >> 3) & 3, hf = kr >> 6, rr = kr & 63;
             uint32_t hv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (S.tile_ok[s][hf]) {
                 const uint8_t *t = S.stage[s] + hf * kIdxTileBytes;
@@ -268,26 +262,26 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
         }
         tc::fence_after_sync();
 
-        // epilogue: key r of the tile, queries 16 qh .. 16 qh + 15
+        // epilogue: key r of the tile, queries 8 qo .. 8 qo + 7
         const int64_t pos = (int64_t)tile * kMqKeys + r;
         const bool key_ok = pos < L && S.tile_ok[s][r >> 6];
-        float sc[16];
+        float sc[8];
 #pragma unroll 1
         for (int h = 0; h < kIdxHeads; ++h) {
-            float t[4][16];
-            const uint32_t base = tc::taddr(tmem, 32u * quad, (uint32_t)(h * kMqQueries + 16 * qh));
-            tmem_ld16x4(base, base + kMqN, base + 2 * kMqN, base + 3 * kMqN, t);
+            float t[4][8];
+            const uint32_t base = tc::taddr(tmem, 32u * quad, (uint32_t)(h * kMqQueries + 8 * qo));
+            tmem_ld8x4(base, base + kMqN, base + 2 * kMqN, base + 3 * kMqN, t);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const float sh = __fadd_rn(__fadd_rn(__fadd_rn(t[0][i], t[1][i]), t[2][i]), t[3][i]);
                 const float rl = sh > 0.0f ? sh : 0.0f;
-                const float wh = S.wq[16 * qh + i][h];
+                const float wh = S.wq[8 * qo + i][h];
                 sc[i] = h == 0 ? __fmul_rn(wh, rl) : __fmaf_rn(wh, rl, sc[i]);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int qi = 16 * qh + i, gq = g0 + qi;
+        for (int i = 0; i < 8; ++i) {
+            const int qi = 8 * qo + i, gq = g0 + qi;
             if (gq >= P.n_q || pos >= S.ncand[qi]) continue;
             const int64_t row = (int64_t)b * P.n_q + gq;
             const float score = sc[i] == 0.0f ? 0.0f : sc[i];

@@ -123,6 +123,8 @@ struct FusedJobDesc {
     CacheView kv;            // Full layer appends: main-KV cache written when new_kv
     const float *new_kv;     // [B][512] or null: quantised to position L-1 of kv
     const float *new_key;    // [B][64] or null: quantised to position L-1 of keys
+    CacheView warm;          // main-KV cache the Top-K rows are gathered from next (has_warm)
+    int32_t has_warm;        // 1: bring each selected row into L2 as its index is written
 };
 
 struct FusedLaunch {

@@ -6,8 +6,8 @@
 // then fails, and it would synchronise the device anyway), or a plugin that
 // runs inside another runtime's allocator and has no way to ask it for
 // scratch.  The attention kernel needs scratch only to split one (layer
-// group, sequence) over several clusters (each cluster's merged partial and
-// a ticket naming the last cluster to finish); this variant takes that
+// group, sequence) over two clusters (the second cluster's per-CTA partials
+// and a counter per owner in the first); this variant takes that
 // scratch from a fixed array the library owns for the life of the process,
 // planned to fit it, instead of from a caller workspace.
 #include <atomic>

@@ -123,6 +123,15 @@ __device__ __forceinline__ void st_cluster_f2(uint32_t caddr, float x, float y)
 // before the data's writer has finished; later loads see the written data).
 __device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
+// Load with acquire semantics at GPU scope: pairs with another CTA's
+// __threadfence() and atomic update of the same word.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ---- programmatic dependent launch -----------------------------------------
 // Waits until the grids this one depends on have completed and their memory
 // is visible (a no-op when the launch has no programmatic dependency).

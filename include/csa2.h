@@ -221,13 +221,14 @@ csa2_status csa2_index_topk_multi(const csa2_cache *keys, const float *q_idx, co
  * scale x 2^8 -- window rows with |x| above ~15,000 would overflow it).
  * Launch shape and workspace: each sequence is one thread-block cluster
  * (up to 16 CTAs, a tile of 128 rows each, merged through distributed
- * shared memory), or several clusters when that is faster; split clusters
- * each write a partial (running max, sum, normalised output) to the
- * workspace and the last one to finish merges them.  The plan is the
+ * shared memory), or two clusters when that is faster: the second
+ * cluster's CTAs each write a partial (running max, sum, normalised output)
+ * to the workspace and the first cluster folds them into its merge (planned
+ * only when every cluster of the launch fits on the device at once).  The plan is the
  * fastest whose scratch fits `workspace_bytes`; csa2_sparse_attn_workspace()
  * is the most any plan of these sizes asks for.  `workspace` may be NULL
  * (with any size): then every sequence is one cluster.  The split path's
- * ticket counters must be zero before the first use (zero-fill the
+ * counters must be zero before the first use (zero-fill the
  * workspace once) and every call leaves them zero.  Results are identical
  * for equal inputs and equal workspace sizes; a different split merges in a
  * different order, which changes the rounding only. */
