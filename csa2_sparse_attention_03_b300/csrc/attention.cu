@@ -848,6 +848,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         tc::mbar_wait(&M.bar_rx, 0);  // a last chance for the copies in flight
     }
     __syncthreads();
+    // every block for this CTA has landed, so its peers' copies out of their
+    // shared memory are done: arrive now, wait only before leaving
+    tc::cluster_arrive();
     if (tid == 0 && !M.ok) raise_flag(flags, kFlagTimeout);
     if (n_sat > 0) {
         // every satellite's (m, l); the cluster's merged (max, sum) is one more
@@ -899,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
                 M.cl[q] > 0.0f ? M.cm[q] + logf(M.cl[q]) : -INFINITY;
         }
     }
-    tc::cluster_sync();  // no CTA leaves while another reads its shared memory
+    tc::cluster_wait();  // no CTA leaves while a copy out of its shared memory may be in flight
 }
 
 }  // namespace

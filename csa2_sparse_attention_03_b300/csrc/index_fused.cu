@@ -908,7 +908,11 @@ bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp)
     const int n_groups = n_jobs * batch;
     if (n_groups <= 0 || n_jobs > kMaxFusedJobs) return false;
     const int64_t cand = std::max<int64_t>(1, max_cand);
-    int G = (int)std::max<int64_t>(1, std::min<int64_t>((cand + 63) / 64, n_sm / n_groups));
+    // 20 SMs are left to the attention launch of the previous layer (18 CTAs
+    // at batch 1), which still runs when this launch starts: every CTA of the
+    // group becomes resident at once and issues its tile copies before the
+    // wait, instead of the last ones starting when that launch ends
+    int G = (int)std::max<int64_t>(1, std::min<int64_t>((cand + 63) / 64, std::max(1, n_sm - 20) / n_groups));
     if (G < 1) G = 1;
     int64_t chunk = ((cand + G - 1) / G + 63) / 64 * 64;
     if (chunk > kMaxChunk) {
