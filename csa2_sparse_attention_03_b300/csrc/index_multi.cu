@@ -26,7 +26,7 @@
 //
 // Shape: a CTA takes one sequence, a group of up to 32 queries and every
 // gridDim.x-th tile of 128 keys.  Per tile: two 64-key tiles by bulk copy
-// (double-buffered), unpacked to fp16 core matrices (A: 128 keys x 64
+// (a ring of 8 tiles in flight), unpacked to fp16 core matrices (A: 128 keys x 64
 // channels), four MMAs (M = 128 keys, N = 4 heads x 32 queries, K = 16) into
 // 512 tensor-memory columns, then the epilogue: thread = key x 8 queries.  The
 // epilogue writes each query row's order-preserving keys (0 = not a
@@ -50,6 +50,7 @@ constexpr int kMqN = kIdxHeads * kMqQueries;          // 128 B rows: (head, quer
 constexpr int kMqBlocks = kIdxDim / 16;               // 4 channel blocks
 constexpr uint32_t kMqCols = kMqBlocks * kMqN;        // 512 tensor-memory columns: (block, head, query)
 constexpr int kMqStage = 2 * kIdxTileBytes;           // one tile of 128 keys as two 64-key tiles
+constexpr int kMqRing = 8;                            // tiles in flight per CTA
 constexpr int kMqMaxTilesPerCta = 511;                // < 65,536 keys: 16-bit histogram counts
 
 struct MqParams {
@@ -68,16 +69,18 @@ struct MqParams {
 struct __align__(128) MqSmem {
     uint8_t a[kMqKeys * kIdxDim * 2];      // keys as fp16, K-major core matrices
     uint8_t bq[kMqN * kIdxDim * 2];        // queries as fp16, K-major core matrices
-    uint8_t stage[2][kMqStage];            // raw key tiles
+    uint8_t stage[kMqRing][kMqStage];      // raw key tiles, a ring
     uint32_t hist[kMqQueries][kHistBins / 2];  // two 16-bit counts per word (bin 2i low)
     float wq[kMqQueries][kIdxHeads];
     int32_t ncand[kMqQueries];
-    int32_t tile_ok[2][2];
-    uint64_t bar_ld[2];
+    int32_t tile_ok[kMqRing][2];
+    uint64_t bar_ld[kMqRing];
     uint64_t bar_mma;
     uint32_t tmem_slot;
     int32_t ok;
 };
+
+static_assert(sizeof(MqSmem) <= 232448, "multi-query scoring shared memory over the 227 KB limit");
 
 // Byte offset of element (row, k) in a K-major operand of 64 fp16 channels:
 // core matrices of 8 rows x 8 channels, 128 B apart along K, 1,024 B apart
@@ -123,8 +126,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
     const int n_tiles = (L + kMqKeys - 1) / kMqKeys;
 
     if (tid == 0) {
-        tc::mbar_init(&S.bar_ld[0], 1);
-        tc::mbar_init(&S.bar_ld[1], 1);
+        for (int i = 0; i < kMqRing; ++i) tc::mbar_init(&S.bar_ld[i], 1);
         tc::mbar_init(&S.bar_mma, 1);
         tc::mbar_init_fence();
         S.ok = 1;
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
     const int my_first = blockIdx.x;
     const int n_my = my_first < n_tiles ? (n_tiles - 1 - my_first) / (int)gridDim.x + 1 : 0;
     auto issue = [&](int k) {  // thread 0: the two 64-key tiles of this CTA's k-th tile
-        const int tile = my_first + k * (int)gridDim.x, s = k & 1;
+        const int tile = my_first + k * (int)gridDim.x, s = k % kMqRing;
         uint32_t bytes = 0;
         const uint8_t *src[2] = {nullptr, nullptr};
         for (int hf = 0; hf < 2; ++hf) {
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem_slot;
-    if (tid == 0 && n_my > 0) issue(0);
+    if (tid == 0)
+        for (int k = 0; k < min(kMqRing, n_my); ++k) issue(k);
 
     constexpr uint32_t kIdesc = tc::idesc_f16(kMqKeys, kMqN, false, false);
     const int quad = warp & 3, qo = warp >> 2;  // lanes 32 quad.., queries 8 qo..
@@ -218,11 +221,13 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
     uint32_t ok = 1;
 #pragma unroll 1
     for (int k = 0; k < n_my; ++k) {
-        const int tile = my_first + k * (int)gridDim.x, s = k & 1;
-        if (tid == 0 && k + 1 < n_my) issue(k + 1);  // its stage was released at the end of iteration k - 1
-        if (!tc::mbar_wait(&S.bar_ld[s], (uint32_t)(k >> 1) & 1u)) {
+        const int tile = my_first + k * (int)gridDim.x, s = k % kMqRing;
+        // the stage of tile k - 1 was released at the end of the last iteration
+        if (tid == 0 && k > 0 && k - 1 + kMqRing < n_my) issue(k - 1 + kMqRing);
+        const uint32_t parity = (uint32_t)(k / kMqRing) & 1u;
+        if (!tc::mbar_wait(&S.bar_ld[s], parity)) {
             ok = 0;
-            tc::mbar_wait(&S.bar_ld[s], (uint32_t)(k >> 1) & 1u);  // a last chance for copies in flight
+            tc::mbar_wait(&S.bar_ld[s], parity);  // a last chance for copies in flight
         }
         // keys -> fp16: item = (key, block), eight consecutive keys per block
         // in a quarter warp (conflict-free 16-B stores); sk * e2m1 is exact in fp16
@@ -262,35 +267,38 @@ __global__ void __launch_bounds__(kMqThreads, 1) mq_score_kernel(const __grid_co
         }
         tc::fence_after_sync();
 
-        // epilogue: key r of the tile, queries 8 qo .. 8 qo + 7
-        const int64_t pos = (int64_t)tile * kMqKeys + r;
-        const bool key_ok = pos < L && S.tile_ok[s][r >> 6];
-        float sc[8];
+        // epilogue: key r of the tile, queries 8 qo .. 8 qo + 7 (warps whose
+        // eight query rows are all past n_q have nothing to do)
+        if (g0 + 8 * qo < P.n_q) {
+            const int64_t pos = (int64_t)tile * kMqKeys + r;
+            const bool key_ok = pos < L && S.tile_ok[s][r >> 6];
+            float sc[8];
 #pragma unroll 1
-        for (int h = 0; h < kIdxHeads; ++h) {
-            float t[4][8];
-            const uint32_t base = tc::taddr(tmem, 32u * quad, (uint32_t)(h * kMqQueries + 8 * qo));
-            tmem_ld8x4(base, base + kMqN, base + 2 * kMqN, base + 3 * kMqN, t);
+            for (int h = 0; h < kIdxHeads; ++h) {
+                float t[4][8];
+                const uint32_t base = tc::taddr(tmem, 32u * quad, (uint32_t)(h * kMqQueries + 8 * qo));
+                tmem_ld8x4(base, base + kMqN, base + 2 * kMqN, base + 3 * kMqN, t);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sh = __fadd_rn(__fadd_rn(__fadd_rn(t[0][i], t[1][i]), t[2][i]), t[3][i]);
+                    const float rl = sh > 0.0f ? sh : 0.0f;
+                    const float wh = S.wq[8 * qo + i][h];
+                    sc[i] = h == 0 ? __fmul_rn(wh, rl) : __fmaf_rn(wh, rl, sc[i]);
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float sh = __fadd_rn(__fadd_rn(__fadd_rn(t[0][i], t[1][i]), t[2][i]), t[3][i]);
-                const float rl = sh > 0.0f ? sh : 0.0f;
-                const float wh = S.wq[8 * qo + i][h];
-                sc[i] = h == 0 ? __fmul_rn(wh, rl) : __fmaf_rn(wh, rl, sc[i]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int qi = 8 * qo + i, gq = g0 + qi;
-            if (gq >= P.n_q || pos >= S.ncand[qi]) continue;
-            const int64_t row = (int64_t)b * P.n_q + gq;
-            const float score = sc[i] == 0.0f ? 0.0f : sc[i];
-            const uint32_t key = key_ok ? score_key(score) : 0u;
-            P.bufs.keys[row * P.bufs.cand_cap + pos] = key;
-            if (key) {
-                const uint32_t bin = key >> (32 - kHistBits);
-                atomicAdd(&S.hist[qi][bin >> 1], (bin & 1u) ? 0x10000u : 1u);
-                if (P.out_scores) P.out_scores[row * (int64_t)P.max_len + pos] = score;
+                const int qi = 8 * qo + i, gq = g0 + qi;
+                if (gq >= P.n_q || pos >= S.ncand[qi]) continue;
+                const int64_t row = (int64_t)b * P.n_q + gq;
+                const float score = sc[i] == 0.0f ? 0.0f : sc[i];
+                const uint32_t key = key_ok ? score_key(score) : 0u;
+                P.bufs.keys[row * P.bufs.cand_cap + pos] = key;
+                if (key) {
+                    const uint32_t bin = key >> (32 - kHistBits);
+                    atomicAdd(&S.hist[qi][bin >> 1], (bin & 1u) ? 0x10000u : 1u);
+                    if (P.out_scores) P.out_scores[row * (int64_t)P.max_len + pos] = score;
+                }
             }
         }
         // tensor memory read and the stage consumed before the next tile's MMAs and copy

@@ -530,25 +530,34 @@ cudaError_t launch_select_cs(const SelectPlan &plan, int64_t cap, size_t smem, i
 
 // Stages up to 160 KB of keys per CTA.  Eight CTAs per row: 16-CTA clusters
 // were measured slower (the cross-rank histogram sums grow with the cluster).
+// When the rows' 8-CTA clusters would take two waves of the device but
+// 4-CTA clusters fit in one (and still stage their slices), 4 are used.
 cudaError_t launch_select(const SelectPlan &plan, int max_cand, int *flags, cudaStream_t stream,
                           cudaEvent_t mid_event)
 {
     (void)mid_event;
-    constexpr int kCS = 8;
     constexpr int64_t kStageMax = 40960;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool attr_set[64] = {};
+    static int n_sms_of[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(select_kernel<kCS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kStageMax * 4));
+    if (!n_sms_of[dev]) {
+        e = cudaFuncSetAttribute(select_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kStageMax * 4));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(select_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kStageMax * 4));
+        int n = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        n_sms_of[dev] = n > 0 ? n : 1;
     }
-    const int64_t slice = ceil_div(ceil_div(max_cand > 0 ? max_cand : 1, kCS), 32) * 32;
+    const int64_t rows = (int64_t)plan.n_row_blocks * plan.batch;
+    auto slice_of = [&](int cs) { return ceil_div(ceil_div(max_cand > 0 ? max_cand : 1, cs), 32) * 32; };
+    const bool four = rows * 8 > n_sms_of[dev] && rows * 4 <= n_sms_of[dev] && slice_of(4) <= kStageMax;
+    const int64_t slice = slice_of(four ? 4 : 8);
     const int64_t cap = slice <= kStageMax ? slice : 0;
-    e = launch_select_cs<kCS>(plan, cap, (size_t)cap * 4, flags, stream);
+    e = four ? launch_select_cs<4>(plan, cap, (size_t)cap * 4, flags, stream)
+             : launch_select_cs<8>(plan, cap, (size_t)cap * 4, flags, stream);
     count_launches(1);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
