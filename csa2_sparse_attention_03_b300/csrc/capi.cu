@@ -265,6 +265,14 @@ cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int bat
                 D.has_warm = 1;
             }
         }
+        // a layer of a decode step follows the previous layer's attention launch
+        // (18 CTAs at batch 1), which still runs when this one starts: leave it
+        // 20 SMs so that every CTA of this grid starts at once
+        FusedPlan plan = lw.plan;
+        if (keys_ready) {
+            FusedPlan p2;
+            if (fused_plan(n_jobs, batch, level_max_cand(jobs, n_jobs, max_seq_len), p2, 20)) plan = p2;
+        }
         FusedLaunch L;
         L.jobs = d.data();
         L.n_jobs = n_jobs;
@@ -277,7 +285,7 @@ cudaError_t run_level(const IdxJob *jobs, int n_jobs, const LevelWs &lw, int bat
         L.max_len = max_seq_len;
         L.pdl = 1;
         L.keys_ready = keys_ready;
-        return launch_fused(L, lw.plan, fp, s);
+        return launch_fused(L, plan, fp, s);
     }
     // scan + select, the appends first
     std::vector<QuantJob> qjobs;

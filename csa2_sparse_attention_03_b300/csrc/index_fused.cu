@@ -900,7 +900,7 @@ int g_first_wait_limit = -1;  // test hook: polls of the first tile wait, < 0 = 
 
 void fused_set_first_wait_limit(int polls) { g_first_wait_limit = polls; }
 
-bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp)
+bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp, int reserve_sms)
 {
     int dev = 0, n_sm = 148;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -908,11 +908,12 @@ bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp)
     const int n_groups = n_jobs * batch;
     if (n_groups <= 0 || n_jobs > kMaxFusedJobs) return false;
     const int64_t cand = std::max<int64_t>(1, max_cand);
-    // 20 SMs are left to the attention launch of the previous layer (18 CTAs
-    // at batch 1), which still runs when this launch starts: every CTA of the
-    // group becomes resident at once and issues its tile copies before the
-    // wait, instead of the last ones starting when that launch ends
-    int G = (int)std::max<int64_t>(1, std::min<int64_t>((cand + 63) / 64, std::max(1, n_sm - 20) / n_groups));
+    // `reserve_sms` SMs are left to a kernel that still runs when this launch
+    // starts (in a decode step, the previous layer's attention): every CTA of
+    // the grid becomes resident at once and issues its tile copies before the
+    // wait, instead of the last ones starting when that kernel ends
+    int G = (int)std::max<int64_t>(
+        1, std::min<int64_t>((cand + 63) / 64, std::max(1, n_sm - std::max(0, reserve_sms)) / n_groups));
     if (G < 1) G = 1;
     int64_t chunk = ((cand + G - 1) / G + 63) / 64 * 64;
     if (chunk > kMaxChunk) {

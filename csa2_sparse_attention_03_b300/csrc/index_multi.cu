@@ -21,8 +21,10 @@
 // fp32 accumulator holds t_hj exactly whatever order the tensor core adds in.
 // Each block gets its own accumulator columns and the epilogue adds the four
 // blocks in the fixed order, so the scores equal the single-query scan's bit
-// for bit.  (A block-scaled FP4 MMA would sum a head's four blocks inside the
-// instruction, in an order and with roundings the library cannot fix.)
+// for bit.  (A block-scaled FP4 MMA with unit scale factors and a block-
+// diagonal query operand, one column per (head, block), would be exact as
+// well and would read the codes without the unpack; this kernel folds the
+// scales into exact fp16 operands of kind::f16 instead.)
 //
 // Shape: a CTA takes one sequence, a group of up to 32 queries and every
 // gridDim.x-th tile of 128 keys.  Per tile: two 64-key tiles by bulk copy

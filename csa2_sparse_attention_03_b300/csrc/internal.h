@@ -144,7 +144,7 @@ struct FusedPlan {
 };
 
 // Whether the fused launch fits (every CTA co-resident); fills the plan.
-bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp);
+bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp, int reserve_sms = 0);
 size_t fused_state_bytes(int n_groups);
 cudaError_t launch_fused(const FusedLaunch &L, const FusedPlan &fp, int *flags, cudaStream_t stream);
 // Test hook: polls of each CTA's first tile wait (< 0: the normal limit).
