@@ -62,6 +62,8 @@ def _check_rows(orc, q, w, ref, lens, K, causal, idx, sc):
     ([10], 16, 4, True),               # more queries than positions: early rows have none
     ([0, 200], 3, 8, True),            # an empty sequence
     ([70000], 32, 2048, True),         # several tiles per CTA
+    ([1500, 999], 100, 64, False),     # four query groups per sequence, every position
+    ([4097], 33, 4097, True),          # Top-K as large as the context, a one-row second group
 ])
 def test_multi_query_scores_and_topk(cuda, orc, lens, n_q, K, causal):
     B, Lmax = len(lens), max(lens)
