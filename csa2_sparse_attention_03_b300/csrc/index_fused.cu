@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     // when the keys predate the previous kernel, the copies go out while it runs
     const bool pre = early && P.keys_ready;
     if (!pre) tc::pdl_wait();
-    int L = early ? -1 : load_len();
+    int L = (early && !pre) ? -1 : load_len();  // with pre, the lengths predate the previous kernel too
     const int64_t c1_max = min((int64_t)(direct ? (early ? P.max_len : L) : job.pool_len), c0 + P.chunk);
     const int nb_max = (int)max((int64_t)0, (c1_max - c0 + kBatchKeys - 1) / kBatchKeys);
 

@@ -252,9 +252,10 @@ csa2_status csa2_sparse_attn(const csa2_cache *kv, const csa2_cache *swa, const 
  * variable on each device (zero when the module loads; every call leaves
  * its counters zero again), planned to fit it; no allocator is called.
  * Its device address is looked up once per device with
- * cudaGetSymbolAddress (thread-safe); make the first call on each device
- * before capturing it in a CUDA graph, because the lookup may load the
- * module.  All calls on a device share the array: calls that overlap in
+ * cudaGetSymbolAddress (thread-safe) and kept for the life of the
+ * process (a cudaDeviceReset invalidates it: reload the library after
+ * one); make the first call on each device before capturing it in a CUDA
+ * graph, because the lookup may load the module.  All calls on a device share the array: calls that overlap in
  * time (on different streams, or from several threads) race on it and give
  * wrong results.  A sequence that needs more than the array holds runs as
  * one cluster, which needs no scratch, so no size is rejected for want of
@@ -321,8 +322,8 @@ csa2_status csa2_decode_layers(const csa2_layer_desc *layers, int32_t n_layers, 
  * appended rows) is read only after it completes.  Read before that, so
  * that their loads overlap the previous kernel: a FULL or REINDEX layer's
  * indexer keys (contiguous caches; a FULL layer's own new key is patched
- * in), and a REUSE or SWA_ONLY layer's indices, sequence lengths, kv_src's
- * cache and window ring.  These must have been written before the stream's
+ * in) and sequence lengths, and a REUSE or SWA_ONLY layer's indices,
+ * sequence lengths, kv_src's cache and window ring.  These must have been written before the stream's
  * previous kernel started, as they are when the layers run in order
  * through this call: do not rewrite them with a kernel launched right
  * before this call.  Workspace: the size of
