@@ -53,7 +53,7 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;                       // 16 warps: the scoring loop is latency-bound
 constexpr int kWarps = kThreads / 32;
 constexpr int kBatchKeys = 1024;                    // candidates per bulk-copy batch
 constexpr int kBatchTiles = kBatchKeys / kIdxTile;  // 16 tiles
@@ -125,11 +125,11 @@ struct Misc {
     uint64_t bar[2];
 };
 
-// ---- block-wide helpers (256 threads) --------------------------------------------------
+// ---- block-wide helpers (kThreads threads) ---------------------------------------------
 
 // Finds bin d with above(d) < need <= above(d) + h[d] (above = count in bins
 // > d, bins taken from the top).  Returns bin -1 (above = total) when the
-// total is below need.  nbins % 256 == 0.
+// total is below need.  nbins % kThreads == 0.
 struct Thresh {
     int bin;
     uint32_t above;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         M.ok = 1;
         M.app_local = -1;
     }
-    M.sk_lut[tid] = e4m3_value((uint32_t)tid);
+    if (tid < 256) M.sk_lut[tid] = e4m3_value((uint32_t)tid);
     for (int i = tid; i < 2 * kHistBins; i += kThreads) hist[i] = 0u;
     __syncthreads();
 
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
         }
     }
 
-    scan::prep_query_set(tid, job.n_q, job.q_idx, job.w, b, M.qs);
+    if (tid < 256) scan::prep_query_set(tid, job.n_q, job.q_idx, job.w, b, M.qs);  // 256 threads
     __syncthreads();
 
     // ---- scan: one thread scores whole keys (all of this job's queries)
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
             if (key) atomicAdd(&hist[q * kHistBins + (key >> (32 - kHistBits))], 1u);
             if (key && job.out_scores[q]) job.out_scores[q][(int64_t)b * P.scores_stride + c0 + li] = sc;
         };
-        // two candidates per thread at a time (i and i + 256), their scores'
+        // two candidates per thread at a time (i and i + kThreads), their scores'
         // dependent chains interleaved
         static_assert(kBatchKeys % (2 * kThreads) == 0, "two candidates per step");
 #pragma unroll 1
