@@ -700,7 +700,12 @@ def run_csa2(args):
             step.run_sequential(stream=stream)
             h_out.copy_(step.arena_out, non_blocking=True)
 
-        g_e2e = timer.capture(serve)
+        # the serving step as DecodeStep.capture_sequential builds it: groups of
+        # layers' inputs copied in on a side stream ahead of the layers that
+        # need them, groups of outputs copied back as soon as they are done
+        with torch.cuda.stream(stream):
+            g_e2e = step.capture_sequential(stream, h_in, h_out)
+        torch.cuda.synchronize()
         et = timer.time(g_e2e, args.e2e_steps)
 
         dt = []
@@ -717,10 +722,14 @@ def run_csa2(args):
         e_ms, d_ms = max_over_ranks(pg, [statistics.mean(et), statistics.mean(dt)], dev)
         e2e = {"value": whole_job_value(world, w.batch, e_ms), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": e_ms,
-               "how": "one CUDA graph per step: the pinned host input arena (queries, indexer queries, "
-                      "weights, appended rows) copied in, the layer-sequential step (csa2_decode_layer per "
-                      "layer), the output arena (out, lse, indices) copied back; all inside the CUDA events",
-               "direct_call_ms_per_step": d_ms}
+               "how": "one CUDA graph per step (DecodeStep.capture_sequential): the pinned host input arena "
+                      "(queries, indexer queries, weights, appended rows) copied in by groups of layers on a "
+                      "second stream, each layer waiting only for its group; the layer-sequential step "
+                      "(csa2_decode_layer per layer); the output arena (out, lse, indices) copied back by "
+                      "groups of layers on a third stream as they finish; all inside the CUDA events",
+               "direct_call_ms_per_step": d_ms,
+               "direct_call_how": "the same step as direct calls, one whole-arena copy in, then every layer, "
+                                  "then one whole-arena copy out, no graph"}
         check("the end-to-end steps")
 
     if rank == 0:

@@ -189,29 +189,54 @@ class DecodeStep:
         """Place the per-step inputs (queries, indexer queries and weights, the
         appended rows) in one contiguous device buffer and the per-step outputs
         (out, lse, indices, pools) in another, so a caller moves each direction
-        with a single copy."""
+        with a single copy.  Both are laid out layer by layer (every input of
+        layer l before any of layer l + 1), so that a prefix of layers is a
+        prefix of bytes: ``in_ranges[l]`` / ``out_ranges[l]`` are layer l's
+        byte ranges."""
         import torch
 
-        def pack(groups):
-            tensors = [t for g in groups for t in g.values()]
-            offs, total = [], 0
-            for t in tensors:
-                offs.append(total)
-                total += (t.numel() * t.element_size() + 255) // 256 * 256
+        def pack(per_layer):
+            offs, total, ranges = [], 0, []
+            for ts in per_layer:
+                start = total
+                for t in ts:
+                    offs.append(total)
+                    total += (t.numel() * t.element_size() + 255) // 256 * 256
+                ranges.append((start, total))
             arena = torch.zeros(max(total, 256), dtype=torch.uint8, device=self.device)
-            k = 0
-            for g in groups:
-                for key in list(g.keys()):
-                    t = g[key]
+            views, k = [], 0
+            for ts in per_layer:
+                vs = []
+                for t in ts:
                     n = t.numel() * t.element_size()
                     view = arena[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
                     view.copy_(t)
-                    g[key] = view
+                    vs.append(view)
                     k += 1
-            return arena
+                views.append(vs)
+            return arena, views, ranges
 
-        self.arena_in = pack([self.q, self.q_idx, self.wts, self.new_rows])
-        self.arena_out = pack([self.out, self.lse, self.idx, self.pool])
+        L = len(self.w.layers)
+        in_groups = [self.q, self.q_idx, self.wts]
+        in_keys = [[(g, l) for g in range(3) if l in in_groups[g]] +
+                   [("row", key) for key in self.new_rows if key[1] == l] for l in range(L)]
+
+        def fetch(ref):
+            return in_groups[ref[0]][ref[1]] if ref[0] != "row" else self.new_rows[ref[1]]
+
+        self.arena_in, views, self.in_ranges = pack([[fetch(r) for r in keys] for keys in in_keys])
+        for keys, vs in zip(in_keys, views):
+            for r, v in zip(keys, vs):
+                if r[0] == "row":
+                    self.new_rows[r[1]] = v
+                else:
+                    in_groups[r[0]][r[1]] = v
+        out_groups = [self.out, self.lse, self.idx, self.pool]
+        out_keys = [[(g, l) for g in range(4) if l in out_groups[g]] for l in range(L)]
+        self.arena_out, views, self.out_ranges = pack([[out_groups[g][l] for g, l in keys] for keys in out_keys])
+        for keys, vs in zip(out_keys, views):
+            for (g, l), v in zip(keys, vs):
+                out_groups[g][l] = v
         torch.cuda.synchronize(self.device)
 
     def _descs(self):
@@ -262,6 +287,76 @@ class DecodeStep:
             self.run(stream=stream)
             if host_out is not None:
                 host_out.copy_(self.arena_out, non_blocking=True)
+        return g
+
+    def capture_sequential(self, stream, host_in, host_out, in_groups=None, out_groups=None):
+        """Capture one serving step in the layer-sequential order in a CUDA
+        graph on `stream`: the step's inputs copied in from the pinned host
+        buffer `host_in`, every layer's ``csa2_decode_layer`` call, its
+        outputs copied back to the pinned `host_out`.  The copies overlap the
+        kernels: groups of layers' inputs are copied on a second stream, in
+        layer order, and a layer waits only for its own group; each group of
+        layers' outputs goes back on a third stream as soon as its last layer
+        is done.  `in_groups` / `out_groups` are the first layers of each
+        group (default: growing groups in, shrinking groups out, so that the
+        first layer waits for little and the last copy is short)."""
+        import torch
+
+        L = len(self.w.layers)
+        in_groups = sorted(set(in_groups if in_groups is not None else [0, 1, 4, 12])) or [0]
+        out_groups = sorted(set(out_groups if out_groups is not None else [0, L - 8, L - 3, L - 1]))
+        in_groups = [l for l in in_groups if 0 <= l < L]
+        out_groups = [l for l in out_groups if 0 <= l < L]
+        if not in_groups or in_groups[0] != 0:
+            in_groups = [0] + in_groups
+        if not out_groups or out_groups[0] != 0:
+            out_groups = [0] + out_groups
+        if not hasattr(self, "_seq_ws"):
+            need = csa2_decode_layer_workspace(self.descs, self.B, self.Lmax, self.topk, self.pool_len, self.window)
+            self._seq_ws = new_workspace(need, self.device)
+        dev = self.device
+        s_in = torch.cuda.Stream(device=dev)
+        s_out = torch.cuda.Stream(device=dev)
+
+        def span(ranges, l0, l1):
+            return ranges[l0][0], ranges[l1 - 1][1]
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            start = torch.cuda.Event()
+            start.record(stream)
+            s_in.wait_event(start)
+            bounds = in_groups + [L]
+            ready = []
+            with torch.cuda.stream(s_in):
+                for k in range(len(in_groups)):
+                    a, b = span(self.in_ranges, bounds[k], bounds[k + 1])
+                    if b > a:
+                        self.arena_in[a:b].copy_(host_in[a:b], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(s_in)
+                    ready.append(e)
+            obounds = out_groups + [L]
+            ends = set(b - 1 for b in obounds[1:])
+            k_in = 0
+            for l in range(L):
+                if k_in < len(in_groups) and l == in_groups[k_in]:
+                    stream.wait_event(ready[k_in])
+                    k_in += 1
+                csa2_decode_layer(self.descs, l, self.B, self.seq_lens, self.Lmax, self.topk, self.pool_len,
+                                  self.window, self._seq_ws, stream=stream, arr=self.arr)
+                if l in ends:
+                    k = obounds.index(l + 1) - 1
+                    done = torch.cuda.Event()
+                    done.record(stream)
+                    s_out.wait_event(done)
+                    a, b = span(self.out_ranges, obounds[k], l + 1)
+                    if b > a:
+                        with torch.cuda.stream(s_out):
+                            host_out[a:b].copy_(self.arena_out[a:b], non_blocking=True)
+            joined = torch.cuda.Event()
+            joined.record(s_out)
+            stream.wait_event(joined)
         return g
 
     def run_sequential(self, stream=None):

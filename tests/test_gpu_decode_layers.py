@@ -107,3 +107,34 @@ def test_layer_sequential_graph_replays_identically(cuda, orc):
             assert torch.equal(a, b)
     st, flags = cuda.csa2_check_device()
     assert st == 0, (st, flags)
+
+
+def test_pipelined_serving_step_copies_every_output(cuda, orc):
+    """DecodeStep.capture_sequential: the inputs come in from pinned host memory
+    by groups of layers and the outputs go back by groups, overlapping the
+    kernels.  The host copy of the outputs equals what the plain layer-
+    sequential step writes on the device, bit for bit, and matches the oracle;
+    the device inputs equal the host inputs."""
+    w = synth.workload(2, small=True)
+    step = DecodeStep(w, fill="host")
+    ref, _, _ = oracle_step(orc, w)
+    h_in = step.arena_in.detach().cpu().pin_memory()
+    step.run_sequential()
+    torch.cuda.synchronize()
+    want = step.arena_out.detach().cpu().clone()
+    h_out = torch.zeros(step.arena_out.shape, dtype=step.arena_out.dtype, pin_memory=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = step.capture_sequential(s, h_in, h_out)
+    for _ in range(2):
+        step.arena_in.zero_()
+        step.arena_out.zero_()
+        h_out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(step.arena_in.cpu(), h_in)
+        assert torch.equal(h_out, want)
+    _compare(step, ref, w)
+    st, flags = cuda.csa2_check_device()
+    assert st == 0, (st, flags, cuda.csa2_last_error())
