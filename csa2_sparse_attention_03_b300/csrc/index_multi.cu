@@ -17,8 +17,9 @@
 // most 6 significant bits and lies in [2^-10, 2688], so it is exact in fp16:
 // the keys enter the MMA as sk_j * e_k and the queries as sq_hj * e_q.  A
 // 16-channel block is one kind::f16 MMA step (K = 16); every partial sum of
-// its 16 products is sq_hj sk_j / 4 times an integer of at most 576, so the
-// fp32 accumulator holds t_hj exactly whatever order the tensor core adds in.
+// its 16 products is sq_hj sk_j / 4 times an integer of magnitude at most
+// 2,304 (the doubled codes are integers up to 12), so the fp32 accumulator
+// holds t_hj exactly whatever order the tensor core adds in.
 // Each block gets its own accumulator columns and the epilogue adds the four
 // blocks in the fixed order, so the scores equal the single-query scan's bit
 // for bit.  (A block-scaled FP4 MMA with unit scale factors and a block-
