@@ -13,7 +13,7 @@
 // over the same keys share the pass), each query a selection row with up to
 // two targets (its Top-K and, for a Full layer, its pool).  CTA g owns the
 // contiguous candidates [g chunk, (g+1) chunk):
-//   scan     its key tiles arrive by bulk copy (a two-slot ring of 16 tiles)
+//   scan     its key tiles arrive by bulk copy (a ring of up to 4 batches of 16 tiles)
 //            or, for a pool, by per-key gathers; each thread scores two
 //            candidates at a time (exact integer block products); each
 //            score becomes an order-preserving uint32 key kept in shared
@@ -63,6 +63,8 @@ constexpr int kCandCap = 1024;                      // candidate list capacity p
                                                     // whole list: a larger threshold bin takes a refining round)
 constexpr int kMaxG = 1024;
 constexpr int kMaxChunk = 8192;
+constexpr int kMaxRing = 4;                          // bulk-copy ring slots at most
+constexpr size_t kMaxSmem = 232448;                  // dynamic shared memory per CTA at most
 
 enum : int32_t { kRefine = 0, kPubCand = 1, kPubCount = 2, kDone = 3 };
 
@@ -94,7 +96,7 @@ struct FusedParams {
     int64_t scores_stride;
     int32_t batch, topk, pool_out, max_len;
     int32_t G, chunk, cap;    // CTAs per group, candidates per CTA, candidate capacity
-    int32_t ring_slots;       // bulk-copy ring slots (1 or 2)
+    int32_t ring_slots;       // bulk-copy ring slots (1 .. kMaxRing)
     uint32_t spin_limit;      // group-barrier polls before giving up
     uint32_t first_wait_limit;  // polls of the first tile wait (test hook; normally the mbarrier limit)
     int32_t keys_ready;         // the key caches predate the previous kernel: copies go out before the wait
@@ -121,8 +123,8 @@ struct Misc {
     int32_t app_local;         // its candidate index within this CTA's range, or -1
     int32_t ok;
     uint32_t bcast[8];
-    uint32_t tile_ok[2];       // per ring slot: tiles whose copy was issued
-    uint64_t bar[2];
+    uint32_t tile_ok[kMaxRing];  // per ring slot: tiles whose copy was issued
+    uint64_t bar[kMaxRing];
 };
 
 // ---- block-wide helpers (kThreads threads) ---------------------------------------------
@@ -311,8 +313,7 @@ __global__ void __launch_bounds__(kThreads) index_fused_kernel(const __grid_cons
     GroupState &GS = *reinterpret_cast<GroupState *>(P.state + ((size_t)jz * P.batch + b) * sizeof(GroupState));
 
     if (tid == 0) {
-        tc::mbar_init(&M.bar[0], 1);
-        tc::mbar_init(&M.bar[1], 1);
+        for (int i = 0; i < kMaxRing; ++i) tc::mbar_init(&M.bar[i], 1);
         tc::mbar_init_fence();
         M.ok = 1;
         M.app_local = -1;
@@ -921,12 +922,15 @@ bool fused_plan(int n_jobs, int batch, int64_t max_cand, FusedPlan &fp, int rese
         return false;
     }
     const int batches = (int)((chunk + kBatchKeys - 1) / kBatchKeys);
-    const int slots = batches > 1 ? 2 : 1;
+    // every batch of the CTA in flight at once, up to kMaxRing, as shared memory allows: the copies are
+    // latency-bound, and a CTA of the phased launch (four groups) scans 3.5 batches
+    int slots = batches > 1 ? 2 : 1;
+    while (slots < std::min(batches, kMaxRing) && fused_smem(slots + 1, (int)chunk) <= kMaxSmem) ++slots;
     const size_t smem = fused_smem(slots, (int)chunk);
     static bool attr[64] = {};
     if (dev >= 0 && dev < 64 && !attr[dev]) {
         if (cudaFuncSetAttribute(index_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)fused_smem(2, kMaxChunk)) != cudaSuccess)
+                                 (int)kMaxSmem) != cudaSuccess)
             return false;
         attr[dev] = true;
     }
