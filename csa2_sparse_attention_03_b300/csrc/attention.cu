@@ -180,14 +180,28 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[N], int lane)
     for (int bit = 4 - kStages; bit >= 0; --bit) v[0] = op(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1 << bit));
 }
 
-// Raw bytes of one thread's share of a row: row r, channels 128 k + 64 h ..
-// 128 k + 64 h + 63 of every chunk k (so that each channel chunk of the tile
-// is complete once every thread has converted its part of it).
+// A thread's share of a tile, in registers between its loads and its
+// dequantisation.
+//  - Row tile (FP4 main KV) by quarter rows, when a CTA takes more than one
+//    tile: rows 16 w + i and 16 w + 8 + i (w = tid / 32, i = tid % 8), a
+//    quarter of each: lane quarter q = (tid / 8) % 4 holds the row's code
+//    bytes 64 q + 16 s (s = 0..3: channels 128 q + 32 s .. + 31) and its
+//    block scales 8 q .. 8 q + 7.  One load of a warp so reads a 16-byte
+//    piece of 8 rows, four lanes to a row (8 cache lines, not 32), and the
+//    dequantised 16-byte stores of a warp fill four whole 128-byte
+//    core-matrix rows.  The loads of the next tile then issue in about a
+//    quarter of the time.
+//  - Otherwise by half rows, like a window tile: row r = tid % 128, channels
+//    128 k + 64 h .. + 63 of every chunk k (h = tid / 128); one position
+//    load per row, the shortest chain for a CTA's only tile.
 struct Raw {
-    uint4 g[16];     // FP4: chunk k's codes in g[2k], g[2k+1], its 4 scales in word k of g[8]; FP8: g[4k..4k+3]
-    float scale;     // FP8: the row's fp32 scale
-    int32_t app;     // FP8: layer slot whose appended row this is, or -1
-    bool valid;
+    uint4 g[16];     // quarter rows: row g's piece s in g[4 g + s], its scales in words 2 g, 2 g + 1 of g[8];
+                     // half rows, FP4: chunk k's codes in g[2 k], g[2 k + 1], its 4 scales in word k of g[8];
+                     // window tile: chunk k in g[4 k .. 4 k + 3]
+    float scale;     // window tile: the row's fp32 scale
+    int32_t app;     // window tile: layer slot whose appended row this is, or -1
+    bool valid;      // the thread's (first) row
+    bool valid1;     // quarter rows: the thread's second row
 };
 
 struct Ctx {
@@ -196,46 +210,125 @@ struct Ctx {
     Misc *M;
     int *flags;
     int b, L, W;
+    bool quarter;    // row tiles by quarter rows
 };
 
 __device__ __forceinline__ bool tile_is_window(const UnitDev &U, int tile) { return tile >= U.row_tiles; }
 
-// Selected position of row r of a row tile (-1: none, or a window tile).
-// Loaded a tile ahead of the row gather so that the gather never waits on it.
-__device__ __forceinline__ int32_t load_pos(const Ctx &c, int tile, int r)
+// Row g (0, 1) of thread tid in a row tile, and the thread's quarter of it.
+__device__ __forceinline__ int quarter_row(int tid, int g) { return 16 * (tid >> 5) + 8 * g + (tid & 7); }
+__device__ __forceinline__ int row_quarter(int tid) { return (tid >> 3) & 3; }
+
+// Selected positions of a thread's rows of a row tile (-1: none, or a
+// window tile): two rows by quarters, or row tid % 128 (and none) by halves.
+// Loaded a tile ahead of the row gather so that the gather never waits on
+// them.
+struct RowPos {
+    int32_t p[2];
+};
+
+__device__ __forceinline__ RowPos no_rows() { return RowPos{{-1, -1}}; }
+
+__device__ __forceinline__ RowPos load_pos(const Ctx &c, int tile)
 {
     const UnitDev &U = *c.U;
-    if (tile_is_window(U, tile)) return -1;
-    const int v = tile * kRows + r;
-    return v < c.P->topk ? __ldcg(U.idx + (int64_t)c.b * c.P->topk + v) : -1;
+    RowPos rp = no_rows();
+    if (tile_is_window(U, tile)) return rp;
+    const int32_t *sel = U.idx + (int64_t)c.b * c.P->topk;
+    if (!c.quarter) {
+        const int v = tile * kRows + (threadIdx.x & (kRows - 1));
+        if (v < c.P->topk) rp.p[0] = __ldcg(sel + v);
+        return rp;
+    }
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        const int v = tile * kRows + quarter_row(threadIdx.x, g);
+        if (v < c.P->topk) rp.p[g] = __ldcg(sel + v);
+    }
+    return rp;
 }
 
-// Issues the loads of this thread's half row of `tile` into registers (`pos`:
-// load_pos of the row for a row tile).
-__device__ __forceinline__ void gather(const Ctx &c, int tile, int32_t pos, int r, int h, Raw &raw)
+// The selected rows' places in the main-KV cache, found in two steps so that
+// a paged cache's page-table loads are in flight while other work runs:
+// row_issue() starts the loads of the physical pages, row_slot() forms a
+// slot (the same slot as slot_of: -1 when the page is unmapped or out of
+// range, or the position is not below the sequence length).
+struct RowRef {
+    int32_t pos[2];   // selected positions, -1 for none
+    int32_t phys[2];  // paged cache: physical page of pos, -1 when unmapped or out of range
+};
+
+__device__ __forceinline__ RowRef row_issue(const Ctx &c, RowPos rp)
+{
+    const CacheView &kv = c.U->kv;
+    RowRef ref;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        ref.pos[g] = rp.p[g];
+        ref.phys[g] = -1;
+        if (kv.page_size != 0 && rp.p[g] >= 0 && rp.p[g] < c.L) {
+            const int32_t pg = rp.p[g] / kv.page_size;  // p >= 0, page_size > 0
+            if (pg < kv.max_pages) ref.phys[g] = __ldg(kv.page_table + (int64_t)c.b * kv.max_pages + pg);
+        }
+    }
+    return ref;
+}
+
+__device__ __forceinline__ int64_t row_slot(const Ctx &c, int32_t pos, int32_t phys)
+{
+    const CacheView &kv = c.U->kv;
+    if (pos < 0 || pos >= c.L) return -1;
+    int64_t s;
+    if (kv.page_size == 0) {
+        s = (int64_t)c.b * kv.seq_stride + pos;
+    } else {
+        if (phys < 0) return -1;
+        s = (int64_t)phys * kv.page_size + pos % kv.page_size;
+    }
+    return (s >= 0 && s < kv.n_slots) ? s : -1;
+}
+
+// Issues the loads of this thread's share of `tile` into registers (`ref`:
+// row_issue of its rows' positions for a row tile).
+__device__ __forceinline__ void gather(const Ctx &c, int tile, const RowRef &ref, int r, int h, Raw &raw)
 {
     const UnitDev &U = *c.U;
     raw.valid = false;
+    raw.valid1 = false;
     raw.scale = 0.0f;
     raw.app = -1;
     if (!tile_is_window(U, tile)) {
-        const uint8_t *ptr = nullptr;
-        if (pos >= 0) {
-            const int64_t slot = pos < c.L ? slot_of(U.kv, c.b, pos) : -1;
-            if (slot < 0) {
-                if (h == 0) raise_flag(c.flags, kFlagBounds);
-            } else {
-                ptr = U.kv.data + slot * kKvRow;
-            }
-        }
-        raw.valid = ptr != nullptr;
-        if (ptr) {
+        const int q = row_quarter(threadIdx.x);
 #pragma unroll
-            for (int k = 0; k < kChunks; ++k) {
-                const uint4 *codes = reinterpret_cast<const uint4 *>(ptr + 64 * k + 32 * h);
-                raw.g[2 * k] = __ldcg(codes);
-                raw.g[2 * k + 1] = __ldcg(codes + 1);
-                (&raw.g[8].x)[k] = __ldcg(reinterpret_cast<const uint32_t *>(ptr + kKvCodes + 8 * k + 4 * h));
+        for (int g = 0; g < 2; ++g) {
+            if (g > 0 && !c.quarter) break;
+            const uint8_t *ptr = nullptr;
+            if (ref.pos[g] >= 0) {
+                const int64_t slot = row_slot(c, ref.pos[g], ref.phys[g]);
+                if (slot < 0) {
+                    if ((c.quarter ? q : h) == 0) raise_flag(c.flags, kFlagBounds);
+                } else {
+                    ptr = U.kv.data + slot * kKvRow;
+                }
+            }
+            if (g == 0) raw.valid = ptr != nullptr;
+            else raw.valid1 = ptr != nullptr;
+            if (!ptr) continue;
+            if (c.quarter) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    raw.g[4 * g + p] = __ldcg(reinterpret_cast<const uint4 *>(ptr + 64 * q + 16 * p));
+                const uint2 sc = __ldcg(reinterpret_cast<const uint2 *>(ptr + kKvCodes + 8 * q));
+                (&raw.g[8].x)[2 * g] = sc.x;
+                (&raw.g[8].x)[2 * g + 1] = sc.y;
+            } else {
+#pragma unroll
+                for (int k = 0; k < kChunks; ++k) {
+                    const uint4 *codes = reinterpret_cast<const uint4 *>(ptr + 64 * k + 32 * h);
+                    raw.g[2 * k] = __ldcg(codes);
+                    raw.g[2 * k + 1] = __ldcg(codes + 1);
+                    (&raw.g[8].x)[k] = __ldcg(reinterpret_cast<const uint32_t *>(ptr + kKvCodes + 8 * k + 4 * h));
+                }
             }
         }
     } else {
@@ -269,10 +362,9 @@ __device__ __forceinline__ void gather(const Ctx &c, int tile, int32_t pos, int 
     }
 }
 
-// Dequantises this thread's part of channel chunk k of its row into the tile
-// buffer (exact fp16): channels 128 k + 64 h .. + 63.
-__device__ __forceinline__ void dequant_chunk(const Ctx &c, bool window, int r, int h, int k, const Raw &raw,
-                                              uint8_t *T)
+// Dequantises this thread's part of channel chunk k of its window row into
+// the tile buffer (exact fp16): channels 128 k + 64 h .. + 63.
+__device__ __forceinline__ void dequant_window_chunk(const Ctx &c, int r, int h, int k, const Raw &raw, uint8_t *T)
 {
     const int ch0 = 128 * k + 64 * h;
     if (!raw.valid) {
@@ -280,48 +372,107 @@ __device__ __forceinline__ void dequant_chunk(const Ctx &c, bool window, int r, 
         for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 8 * g)) = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
-    if (!window) {
-        const uint32_t sw = (&raw.g[8].x)[k];  // the four 16-channel blocks' scales
+    const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));  // 2^-8
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            const __half2 s2 = __half2half2(__float2half_rn(e4m3_value((sw >> (8 * blk)) & 0xFFu)));
-            const uint4 cw = raw.g[2 * k + (blk >> 1)];
-            const uint32_t w0 = (blk & 1) ? cw.z : cw.x, w1 = (blk & 1) ? cw.w : cw.y;  // 16 codes
-            uint32_t hv[8];
+    for (int i = 0; i < 4; ++i) {
+        uint4 cw = raw.g[4 * k + i];
+        if (raw.app >= 0) cw = *reinterpret_cast<const uint4 *>(&c.M->app[raw.app][ch0 + 16 * i]);
+        const int ch = ch0 + 16 * i;
+        *reinterpret_cast<uint4 *>(T + cm_off(r, ch)) =
+            make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.x & 0xFFFFu), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.x >> 16), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.y & 0xFFFFu), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.y >> 16), k2m8)));
+        *reinterpret_cast<uint4 *>(T + cm_off(r, ch + 8)) =
+            make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.z & 0xFFFFu), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.z >> 16), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.w & 0xFFFFu), k2m8)),
+                       pack_h2(__hmul2(e4m3x2_half2(cw.w >> 16), k2m8)));
+    }
+}
+
+// Dequantises this thread's quarters of its two rows of a row tile into the
+// tile buffer (exact fp16: an E2M1 value times an E4M3 scale).  Piece s of
+// quarter q is channels 128 q + 32 s .. + 31, two 16-channel blocks whose
+// scales are bytes 2 s, 2 s + 1 of the quarter's eight.
+__device__ __forceinline__ void dequant_rows(const Raw &raw, uint8_t *T)
+{
+    const int tid = threadIdx.x, q = row_quarter(tid);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t bits = e2m1x2_half2_bits(((i < 4 ? w0 : w1) >> (8 * (i & 3))) & 0xFFu);
-                hv[i] = pack_h2(__hmul2(*reinterpret_cast<const __half2 *>(&bits), s2));
+    for (int g = 0; g < 2; ++g) {
+        const int R = quarter_row(tid, g);
+        const bool ok = g == 0 ? raw.valid : raw.valid1;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int ch = 128 * q + 32 * p;
+            if (!ok) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(T + cm_off(R, ch + 8 * j)) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
             }
-            *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk + 8)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-        }
-    } else {
-        const __half2 k2m8 = __half2half2(__float2half_rn(0.00390625f));  // 2^-8
+            const uint32_t sw = (&raw.g[8].x)[2 * g + (p >> 1)];
+            const __half2 sp = e4m3x2_half2((p & 1) ? (sw >> 16) : (sw & 0xFFFFu));  // the piece's two block scales
+            const uint4 cw = raw.g[4 * g + p];  // 32 codes, channel 2 b in the low nibble of byte b
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 cw = raw.g[4 * k + i];
-            if (raw.app >= 0) cw = *reinterpret_cast<const uint4 *>(&c.M->app[raw.app][ch0 + 16 * i]);
-            const int ch = ch0 + 16 * i;
-            *reinterpret_cast<uint4 *>(T + cm_off(r, ch)) =
-                make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.x & 0xFFFFu), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.x >> 16), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.y & 0xFFFFu), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.y >> 16), k2m8)));
-            *reinterpret_cast<uint4 *>(T + cm_off(r, ch + 8)) =
-                make_uint4(pack_h2(__hmul2(e4m3x2_half2(cw.z & 0xFFFFu), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.z >> 16), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.w & 0xFFFFu), k2m8)),
-                           pack_h2(__hmul2(e4m3x2_half2(cw.w >> 16), k2m8)));
+            for (int blk = 0; blk < 2; ++blk) {
+                const __half2 s2 = blk ? __high2half2(sp) : __low2half2(sp);
+                const uint32_t w0 = blk ? cw.z : cw.x, w1 = blk ? cw.w : cw.y;  // 16 codes
+                uint32_t hv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t bits = e2m1x2_half2_bits(((i < 4 ? w0 : w1) >> (8 * (i & 3))) & 0xFFu);
+                    hv[i] = pack_h2(__hmul2(*reinterpret_cast<const __half2 *>(&bits), s2));
+                }
+                *reinterpret_cast<uint4 *>(T + cm_off(R, ch + 16 * blk)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(T + cm_off(R, ch + 16 * blk + 8)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
         }
     }
 }
 
-// Dequantises this thread's whole share of its row (every channel chunk).
+// Dequantises this thread's half of channel chunk k of its row of a row tile
+// (half rows; exact fp16): channels 128 k + 64 h .. + 63, four 16-channel
+// blocks whose scales are byte blk of word k.
+__device__ __forceinline__ void dequant_half_chunk(int r, int h, int k, const Raw &raw, uint8_t *T)
+{
+    const int ch0 = 128 * k + 64 * h;
+    if (!raw.valid) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 8 * g)) = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
+    const uint32_t sw = (&raw.g[8].x)[k];  // the four blocks' scales, block 0 in the low byte
+    const __half2 s01 = e4m3x2_half2(sw & 0xFFFFu), s23 = e4m3x2_half2(sw >> 16);
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        const __half2 sp = blk < 2 ? s01 : s23;
+        const __half2 s2 = (blk & 1) ? __high2half2(sp) : __low2half2(sp);
+        const uint4 cw = raw.g[2 * k + (blk >> 1)];
+        const uint32_t w0 = (blk & 1) ? cw.z : cw.x, w1 = (blk & 1) ? cw.w : cw.y;  // 16 codes
+        uint32_t hv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t bits = e2m1x2_half2_bits(((i < 4 ? w0 : w1) >> (8 * (i & 3))) & 0xFFu);
+            hv[i] = pack_h2(__hmul2(*reinterpret_cast<const __half2 *>(&bits), s2));
+        }
+        *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        *reinterpret_cast<uint4 *>(T + cm_off(r, ch0 + 16 * blk + 8)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+    }
+}
+
+// Dequantises this thread's whole share of the tile.
 __device__ __forceinline__ void dequant(const Ctx &c, bool window, int r, int h, const Raw &raw, uint8_t *T)
 {
+    if (!window && c.quarter) {
+        dequant_rows(raw, T);
+        return;
+    }
 #pragma unroll
-    for (int k = 0; k < kChunks; ++k) dequant_chunk(c, window, r, h, k, raw, T);
+    for (int k = 0; k < kChunks; ++k) {
+        if (window) dequant_window_chunk(c, r, h, k, raw, T);
+        else dequant_half_chunk(r, h, k, raw, T);
+    }
 }
 
 // Quantises a layer's appended window row into its ring slot at position
@@ -535,7 +686,7 @@ __device__ __forceinline__ void slice_reduce(int ns, int n_sat, int n4, int c_lo
     }
 }
 
-template <int NL>
+template <int NL, bool QR>
 __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant__ AttnParams P, int *flags)
 {
     constexpr int NQ = 16 * NL;
@@ -578,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     c.b = blockIdx.y;
     c.L = 0;
     c.W = P.window;
+    c.quarter = QR;  // a constant: every branch on it is resolved at compile time
     // this CTA's tiles: every (split cs)-th of the unit's, from its index in
     // the (unit, sequence): the first cluster's CTAs, then the satellites'
     const int gc = part * cs + rank, stride = P.split * cs;
@@ -586,20 +738,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
     const int r = tid & (kRows - 1), h = tid >> 7;
 
     Raw raw;
-    int32_t pos_next = -1;
+    RowPos pos_next = no_rows();
     auto first_gather = [&]() {
         // the length and the positions are independent loads: both in flight at once
         const int32_t Lraw = __ldcg(P.seq_lens + c.b);
-        const int32_t pos0 = n_my > 0 ? load_pos(c, t0, r) : -1;
-        if (n_my > 1) pos_next = load_pos(c, t0 + stride, r);
+        const RowPos pos0 = n_my > 0 ? load_pos(c, t0) : no_rows();
+        if (n_my > 1) pos_next = load_pos(c, t0 + stride);
         c.L = max(0, Lraw);
-        if (n_my > 0) gather(c, t0, pos0, r, h, raw);
+        if (n_my > 0) gather(c, t0, row_issue(c, pos0), r, h, raw);
     };
     auto row_masks = [&](bool window) {
-        if (h == 0) {
-            const uint32_t m = __ballot_sync(0xFFFFFFFFu, raw.valid);
-            if (lane == 0) M.vmask[warp] = m;
-            M.rowfac[r] = window ? (raw.app >= 0 ? M.app_scale[raw.app] : raw.scale) * 256.0f : 1.0f;
+        if (window || !c.quarter) {
+            if (h == 0) {
+                const uint32_t m = __ballot_sync(0xFFFFFFFFu, raw.valid);
+                if (lane == 0) M.vmask[warp] = m;
+                M.rowfac[r] = window ? (raw.app >= 0 ? M.app_scale[raw.app] : raw.scale) * 256.0f : 1.0f;
+            }
+        } else {
+            // rows 16 warp + lane and 16 warp + 8 + lane (lanes 0..7) in one 16-bit half of a mask word
+            const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, raw.valid), m1 = __ballot_sync(0xFFFFFFFFu, raw.valid1);
+            if (lane == 0) reinterpret_cast<uint16_t *>(M.vmask)[warp] = (uint16_t)((m0 & 0xFFu) | ((m1 & 0xFFu) << 8));
+            if (lane < 8) {
+                M.rowfac[16 * warp + lane] = 1.0f;
+                M.rowfac[16 * warp + 8 + lane] = 1.0f;
+            }
         }
     };
     // the queries' and appended window rows' lines into L2 while the previous kernel runs
@@ -620,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         dequant(c, tile_is_window(U, t0), r, h, raw, T);
         row_masks(tile_is_window(U, t0));
         if (n_my > 1) {
-            gather(c, t0 + stride, pos_next, r, h, raw);
-            pos_next = n_my > 2 ? load_pos(c, t0 + 2 * stride, r) : -1;
+            gather(c, t0 + stride, row_issue(c, pos_next), r, h, raw);
+            pos_next = n_my > 2 ? load_pos(c, t0 + 2 * stride) : no_rows();
         }
     }
     tc::pdl_wait();
@@ -684,14 +846,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_kernel(const __grid_constant
         const int tile = t0 + it * stride;
         const bool window = tile_is_window(U, tile);
         if (it > 0 || !pre) {
+            // the next tile's page-table loads (its positions arrived during the
+            // previous tile) in flight across the wait and this tile's dequantisation
+            const RowRef ref_next = row_issue(c, pos_next);
             if (it > 0 && tid == 0 && !tc::mbar_wait(&M.bar_pv, (it - 1) & 1)) M.ok = 0;  // tile and P buffers free
             __syncthreads();
             tc::fence_after_sync();
             dequant(c, window, r, h, raw, T);
             row_masks(window);
             if (it + 1 < n_my) {  // in flight during this tile
-                gather(c, tile + stride, pos_next, r, h, raw);
-                pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * stride, r) : -1;
+                gather(c, tile + stride, ref_next, r, h, raw);
+                pos_next = it + 2 < n_my ? load_pos(c, tile + 2 * stride) : no_rows();
             }
         }
         tc::fence_async_smem();
@@ -951,14 +1116,17 @@ cudaError_t prepare_kernel(int dev)
 {
     static bool done[64] = {};
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem_bytes<NL>());
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel<NL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaSuccess;
+    for (auto *k : {attn_kernel<NL, false>, attn_kernel<NL, true>}) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NL>());
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
-// Clusters of `cs` CTAs of attn_kernel<NL> that fit on the device at once.
+// Clusters of `cs` CTAs of attn_kernel<NL, *> that fit on the device at once (both gathers take the same
+// threads and shared memory, one CTA per SM).
 template <int NL>
 int active_clusters(int dev, int cs)
 {
@@ -976,7 +1144,7 @@ int active_clusters(int dev, int cs)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<NL>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, attn_kernel<NL, false>, &cfg);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         log_plan("attention NL=%d: cluster size %d not available (%s)", NL, cs, cudaGetErrorString(e));
@@ -1053,6 +1221,8 @@ cudaError_t launch_nl(AttnParams &p, int max_tiles, const AttnPlan &plan, int *f
                                       plan.workspace ? plan.workspace_bytes : 0);
     p.cs = sh.cs;
     p.split = sh.split;
+    // quarter-row gathers when some CTA takes more than one tile
+    const bool quarter = (std::max(1, max_tiles) + sh.split * sh.cs - 1) / (sh.split * sh.cs) > 1;
     if (sh.split > 1) {
         uint8_t *ws = static_cast<uint8_t *>(plan.workspace);
         const size_t groups = (size_t)p.n_units * plan.batch;
@@ -1076,7 +1246,8 @@ cudaError_t launch_nl(AttnParams &p, int max_tiles, const AttnPlan &plan, int *f
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = plan.pdl ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, attn_kernel<NL>, p, flags);
+    e = quarter ? cudaLaunchKernelEx(&cfg, attn_kernel<NL, true>, p, flags)
+                : cudaLaunchKernelEx(&cfg, attn_kernel<NL, false>, p, flags);
     count_launches(1);
     return e == cudaSuccess ? cudaGetLastError() : e;
 }
